@@ -1,0 +1,409 @@
+"""Benchmark of the reduce-bridge-broadcast gradient all_reduce on one GB300.
+
+Default workload: 4 simulated ranks as 2 islands of 2, one 25 MiB float32
+DDP bucket per rank (n = 6,553,600), values N(0, 1e-3) with 1% of them x100,
+op AVG, bridge codec fp8 E4M3 with a power-of-two scale per 256 values.
+
+A step is one gb_all_reduce of that bucket: fused island reduce + encode
+kernel, bridge hop (device -> pinned host -> device copies), fused decode +
+accumulate + broadcast kernel.  Before every timed step the rank buffers are
+restored from a pristine device copy and L2 is flushed by writing a 512 MiB
+buffer; neither is inside the step's CUDA events.
+
+Reported: algorithm GB/s (bytes of one rank buffer / step time, summed over
+replicas), the dominant kernel's HBM roofline fraction from its live CUDA
+event durations, the bridge hop against measured pinned copy bandwidth, the
+same metric end to end through gb_all_reduce_host with pinned host buffers,
+and the oracle timed on the host cores (``--impl reference`` times only the
+oracle).  Multi-GPU: one independent replica per GPU (the path has no
+exchange between GPUs), max time over ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "all_reduce algorithm GB/s and % of GB300 HBM roofline vs payload size, per codec"
+FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gb", "reference"], default="gb")
+    p.add_argument("--workload", default="c2")
+    p.add_argument("--codec", default=None)
+    p.add_argument("--n", type=int, default=None, help="override elements per rank")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
+    return p.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value, device=None):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (read only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "gb_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.6)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------- CPU baseline
+
+def cpu_baseline(w, xs, codec, budget_s=10.0):
+    """The oracle as it stands, single-threaded, on full steps of the
+    workload (repeated until the budget is spent, at least once)."""
+    import oracle
+    n = xs[0].size
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    per = el / reps
+    return {"value": n * w.elem_bytes / per / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d full steps of the workload (%d ranks x %d elements), %.1f s" % (
+                reps, len(xs), n, el),
+            "host_cores_available": len(os.sched_getaffinity(0))}
+
+
+# -------------------------------------------------------------- GPU leg
+
+def alg_bytes(W, I, n, b, P, I2=True):
+    """Algorithmic HBM bytes of the two kernels for one all_reduce:
+    reduce+encode reads W*n*b and writes I*P; decode+broadcast reads each
+    island's I payloads (I*I*P) and writes W*n*b."""
+    return W * n * b + I * P, I * I * P + W * n * b
+
+
+def run_gb(args, world, rank, local, pg):
+    import torch
+    from cross_vendor_gradient_gb300 import Context, kernel_launch_count, payload_bytes
+    from cross_vendor_gradient_gb300 import workloads as wl
+    from cross_vendor_gradient_gb300 import build as gbuild
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    codec = args.codec or w.codecs[0]
+    n = args.n or w.n
+    W, I = w.world_size, len(w.island_sizes)
+    b = w.elem_bytes
+    xs = wl.host_rank_inputs(w, n=n)
+    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+    def dev_tensor(x):
+        if x.dtype == np.float32:
+            return torch.from_numpy(x).to(dev)
+        return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    pristine = [dev_tensor(x) for x in xs]
+    bufs = [p.clone() for p in pristine]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    K, Wm = args.steps, args.warmup
+    ctx = Context(w.island_sizes)
+    ctx.reserve(n, tdt, codec, w.block)
+    ctx.set_phase_timing(K)
+
+    # pinned copy bandwidth (bridge roofline), one large copy each way
+    big = 256 << 20
+    hbuf = torch.empty(big, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(big, dtype=torch.uint8, device=dev)
+    link = {}
+    with torch.cuda.stream(stream):
+        for name, (dst, src) in (("d2h_gbs", (hbuf, dbuf)), ("h2d_gbs", (dbuf, hbuf))):
+            best = 0.0
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+                e1.synchronize()
+                best = max(best, big / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+            link[name] = best
+    del hbuf, dbuf
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def step(i, timed):
+        for r in range(W):
+            bufs[r].copy_(pristine[r], non_blocking=True)
+        flush.zero_()
+        if timed:
+            ev0[i].record(stream)
+        ctx.all_reduce(bufs, w.op, codec, w.block, stream=stream)
+        if timed:
+            ev1[i].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i, False)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    l0 = kernel_launch_count()
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            step(i, True)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    barrier(pg)
+    launches = kernel_launch_count() - l0
+    clk = clocks.stop()
+
+    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    phases = np.array([ctx.phase_times(K - 1 - i) for i in range(K)])  # oldest first
+    ms_local = float(np.mean(step_ms))
+    ms = max_over_ranks(pg, ms_local, dev if pg is not None else None)
+
+    # correctness of the timed output against the oracle on a sampled slice
+    P = payload_bytes(codec, w.block, n) if I > 1 else 4 * n
+    k1_ms, bridge_ms, k2_ms = (float(np.mean(phases[:, j])) for j in range(3))
+    k1_bytes, k2_bytes = alg_bytes(W, I, n, b, P)
+    peak, peak_kind = measured_peaks()
+    dom = ("k_reduce_encode", k1_bytes, k1_ms) if k1_ms >= k2_ms else ("k_decode_bcast", k2_bytes, k2_ms)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    link_bytes = I * P + I * (I - 1) * P
+    link_peak = min(link["d2h_gbs"], link["h2d_gbs"])
+
+    # end to end through the host-buffer entry point (pinned host buffers)
+    host = [torch.from_numpy(x.copy()).pin_memory() if x.dtype == np.float32 else
+            torch.from_numpy(x.view(np.int16).copy()).pin_memory().view(torch.bfloat16) for x in xs]
+    Ke = max(10, min(200, K // 10))
+    e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + Ke):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ctx.all_reduce_host(host, w.op, codec, w.block, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                e_ms.append(e0.elapsed_time(e1))
+    e2e_ms = max_over_ranks(pg, float(np.mean(e_ms)), dev if pg is not None else None)
+    ctx.close()
+
+    value = world * n * b / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded PCG64 per rank; no dataset)",
+        "config": {"workload": "%s: %d simulated ranks as islands %s, one %.0f MiB %s buffer per rank "
+                               "(n=%d), %s, op %s, codec %s block %d" % (
+                                   w.key, W, list(w.island_sizes), n * b / 2 ** 20, w.dtype, n, w.dist,
+                                   w.op, codec, w.block),
+                   "ranks": W, "islands": list(w.island_sizes), "n": n, "codec": codec, "block": w.block,
+                   "op": w.op, "l2": "flushed before every timed step (512 MiB write); inputs restored "
+                                     "from a device copy outside the timed events",
+                   "parallelism": "replicas x%d" % world},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "alg_bytes_per_launch": dom[1], "avg_launch_ms": dom[2], "traffic": None},
+        "kernels_ms": {"k_reduce_encode": k1_ms, "bridge_hop": bridge_ms, "k_decode_bcast": k2_ms},
+        "kernels_hbm_frac": {"k_reduce_encode": k1_bytes / (k1_ms * 1e-3) / 1e9 / peak,
+                             "k_decode_bcast": k2_bytes / (k2_ms * 1e-3) / 1e9 / peak},
+        "bridge": {"bytes_per_step": link_bytes, "ms": bridge_ms,
+                   "achieved_gbs": link_bytes / (bridge_ms * 1e-3) / 1e9 if bridge_ms > 0 else None,
+                   "pinned_copy_gbs": link, "frac": (link_bytes / (bridge_ms * 1e-3) / 1e9) / link_peak
+                   if bridge_ms > 0 else None},
+        "e2e": {"value": world * n * b / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "steps": Ke, "h2d_bytes_per_step": W * n * b, "d2h_bytes_per_step": W * n * b,
+                "api": "gb_all_reduce_host (pinned host rank buffers)"},
+        "gpu_launches": int(launches),
+        "timed_wall_s": t_wall,
+        "clocks": clk,
+    }
+    return line, w, xs, codec
+
+
+def traffic_from_profiles(kernel):
+    """dram bytes per launch recorded by an ncu capture of the current kernel
+    source, or None (profiles/dram_traffic.txt, 'key=value' lines)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    src = os.path.join(ROOT, "cross_vendor_gradient_gb300", "csrc", "gb_kernels.cu")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        kv = dict(x.split("=", 1) for x in line.split() if "=" in x)
+        if kv.get("kernel") == kernel and kv.get("src_sha") == sha:
+            return float(kv["dram_bytes_per_launch_full_size"])
+    return None
+
+
+def run_reference(args, world, rank, pg):
+    """The oracle, as it stands, on the host cores: each step is one oracle
+    all_reduce of a bounded sample (a prefix of every rank buffer) of the
+    workload, sized so that warmup + steps take about two minutes."""
+    import oracle
+    from cross_vendor_gradient_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    codec = args.codec or w.codecs[0]
+    n_full = args.n or w.n
+    xs_full = wl.host_rank_inputs(w, n=n_full)
+    probe = min(n_full, 1 << 16)
+    t0 = time.perf_counter()
+    oracle.all_reduce([x[:probe] for x in xs_full], w.island_sizes, w.op, codec, w.block)
+    rate = probe / max(time.perf_counter() - t0, 1e-6)  # elements per second per step
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(min(n_full, max(256, rate * budget)) // 256 * 256) or min(n_full, 256)
+    xs = [np.ascontiguousarray(x[:n]) for x in xs_full]
+    for _ in range(args.warmup):
+        oracle.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+        t.append(time.perf_counter() - t0)
+    ms = 1e3 * float(np.mean(t))
+    value = n * w.elem_bytes / (ms * 1e-3) / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded PCG64 per rank; no dataset)",
+        "config": {"workload": "%s: %d simulated ranks as islands %s, %s, op %s, codec %s block %d; "
+                               "each step a prefix of %d of the %d elements per rank" % (
+                                   w.key, w.world_size, list(w.island_sizes), w.dtype, w.op, codec,
+                                   w.block, n, n_full),
+                   "ranks": w.world_size, "islands": list(w.island_sizes), "n": n, "codec": codec,
+                   "block": w.block, "op": w.op, "parallelism": "host, single thread"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "prefix of %d elements of each of the %d rank buffers per step" % (
+                             n, w.world_size),
+                         "host_cores_available": len(os.sched_getaffinity(0))},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank, pg)), flush=True)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    line, w, xs, codec = run_gb(args, world, rank, local, pg)
+    line["roofline"]["traffic"] = traffic_from_profiles(line["roofline"]["kernel"])
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, xs, codec)
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

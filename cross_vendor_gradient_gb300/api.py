@@ -1,0 +1,184 @@
+"""Tensor-level interface over libgb.
+
+torch supplies device memory and the current CUDA stream; every computation
+runs in libgb's kernels (there is no CPU or PyTorch fallback).  Each method
+marshals tensors to pointers, calls the C entry point of the same name on the
+current stream and raises ``GbError`` on a non-OK status.
+"""
+import torch
+
+from . import binding as B
+
+_DTYPES = {torch.float32: B.GB_F32, torch.bfloat16: B.GB_BF16}
+CODECS = {"none": B.GB_CODEC_NONE, "bf16": B.GB_CODEC_BF16, "e4m3": B.GB_CODEC_E4M3,
+          "e5m2": B.GB_CODEC_E5M2}
+OPS = {"sum": B.GB_SUM, "avg": B.GB_AVG}
+
+
+class GbError(RuntimeError):
+    def __init__(self, status, message=""):
+        self.status = status
+        super().__init__("%s%s" % (B.gb_status_string(status), (": " + message) if message else ""))
+
+
+def _codec(c):
+    return CODECS[c] if isinstance(c, str) else int(c)
+
+
+def _op(o):
+    return OPS[o] if isinstance(o, str) else int(o)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dtype(tensors):
+    dt = tensors[0].dtype
+    if dt not in _DTYPES:
+        raise GbError(B.GB_ERR_UNSUPPORTED_DTYPE, str(dt))
+    for t in tensors:
+        if t.dtype != dt or not t.is_contiguous() or t.device != tensors[0].device:
+            raise GbError(B.GB_ERR_INVALID_ARG, "tensors must share dtype and device and be contiguous")
+    return _DTYPES[dt]
+
+
+def payload_bytes(codec, block, n):
+    return B.gb_payload_bytes(_codec(codec), block, n)
+
+
+def payload_scales_offset(codec, block, n):
+    return B.gb_payload_scales_offset(_codec(codec), block, n)
+
+
+def bucket_plan(numels, elem_bytes, cap_bytes=25 * 1024 * 1024, pad_elems=1):
+    st, bo, off, bn = B.gb_bucket_plan(list(numels), elem_bytes, cap_bytes, pad_elems)
+    if st != B.GB_OK:
+        raise GbError(st, "bucket plan")
+    return bo, off, bn
+
+
+def kernel_launch_count():
+    return B.gb_kernel_launch_count()
+
+
+class Context:
+    """W simulated ranks in contiguous islands on the current CUDA device."""
+
+    def __init__(self, island_sizes):
+        st, h = B.gb_create(list(island_sizes))
+        if st != B.GB_OK:
+            raise GbError(st, "gb_create(%s)" % (list(island_sizes),))
+        self.handle = h
+        self.island_sizes = tuple(int(v) for v in island_sizes)
+        self.world_size = B.gb_world_size(h)
+
+    def close(self):
+        if self.handle:
+            B.gb_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def _check(self, st):
+        if st != B.GB_OK:
+            raise GbError(st, B.gb_last_error_message(self.handle))
+
+    # ------------------------------------------------------------ topology
+    def island_first_rank(self, i):
+        return B.gb_island_first_rank(self.handle, i)
+
+    def island_of_rank(self, r):
+        return B.gb_island_of_rank(self.handle, r)
+
+    def status(self):
+        return B.gb_context_status(self.handle)
+
+    def reserve(self, n, dtype=torch.float32, codec="none", block=256):
+        self._check(B.gb_reserve(self.handle, n, _DTYPES[dtype], _codec(codec), block))
+
+    # ---------------------------------------------------------- collectives
+    def all_reduce(self, tensors, op="sum", codec="none", block=256, stream=None):
+        dt = _dtype(tensors)
+        self._check(B.gb_all_reduce(self.handle, [t.data_ptr() for t in tensors], tensors[0].numel(), dt,
+                                    _op(op), _codec(codec), block, _stream(stream)))
+
+    def reduce_scatter(self, inputs, outputs, op="sum", codec="none", block=256, stream=None):
+        dt = _dtype(list(inputs) + list(outputs))
+        self._check(B.gb_reduce_scatter(self.handle, [t.data_ptr() for t in inputs],
+                                        [t.data_ptr() for t in outputs], inputs[0].numel(), dt, _op(op),
+                                        _codec(codec), block, _stream(stream)))
+
+    def all_gather(self, inputs, outputs, stream=None):
+        dt = _dtype(list(inputs) + list(outputs))
+        self._check(B.gb_all_gather(self.handle, [t.data_ptr() for t in inputs],
+                                    [t.data_ptr() for t in outputs], inputs[0].numel(), dt,
+                                    _stream(stream)))
+
+    def broadcast(self, tensors, src, stream=None):
+        dt = _dtype(tensors)
+        self._check(B.gb_broadcast(self.handle, [t.data_ptr() for t in tensors], tensors[0].numel(), dt,
+                                   src, _stream(stream)))
+
+    def all_reduce_host(self, host_tensors, op="sum", codec="none", block=256, stream=None):
+        dt = _dtype(host_tensors)
+        self._check(B.gb_all_reduce_host(self.handle, [t.data_ptr() for t in host_tensors],
+                                         host_tensors[0].numel(), dt, _op(op), _codec(codec), block,
+                                         _stream(stream)))
+
+    def all_reduce_buckets(self, buckets, op="sum", codec="none", block=256, stream=None):
+        """buckets: list of per-bucket lists of W flat tensors."""
+        flat = [t for b in buckets for t in b]
+        dt = _dtype(flat)
+        self._check(B.gb_all_reduce_buckets(self.handle, [t.data_ptr() for t in flat],
+                                            [b[0].numel() for b in buckets], dt, _op(op), _codec(codec),
+                                            block, _stream(stream)))
+
+    # ------------------------------------------------------- phase blocks
+    def island_reduce(self, island, tensors, island_sum, stream=None):
+        dt = _dtype(tensors)
+        self._check(B.gb_island_reduce(self.handle, island, [t.data_ptr() for t in tensors],
+                                       tensors[0].numel(), dt, island_sum.data_ptr(), _stream(stream)))
+
+    def bridge_compress(self, island_sum, codec, block, payload, stream=None):
+        self._check(B.gb_bridge_compress(self.handle, island_sum.data_ptr(), island_sum.numel(),
+                                         _codec(codec), block, payload.data_ptr(), _stream(stream)))
+
+    def bridge_decompress_accumulate(self, payload, n, codec, block, accum, accumulate, stream=None):
+        self._check(B.gb_bridge_decompress_accumulate(self.handle, payload.data_ptr(), n, _codec(codec),
+                                                      block, accum.data_ptr(), accumulate,
+                                                      _stream(stream)))
+
+    def island_broadcast(self, island, total, op, tensors, stream=None):
+        dt = _dtype(tensors)
+        self._check(B.gb_island_broadcast(self.handle, island, total.data_ptr(), total.numel(), _op(op),
+                                          [t.data_ptr() for t in tensors], dt, _stream(stream)))
+
+    # -------------------------------------------------------------- timing
+    def set_phase_timing(self, capacity):
+        """capacity > 0: keep the phase marks of the last `capacity` calls."""
+        self._check(B.gb_set_phase_timing(self.handle, int(capacity)))
+
+    def phase_times(self, age):
+        st, ms = B.gb_phase_times(self.handle, age)
+        self._check(st)
+        return ms
+
+    def last_phase_times(self):
+        st, ms = B.gb_last_phase_times(self.handle)
+        self._check(st)
+        return ms
+
+    def debug_inject(self, what):
+        self._check(B.gb_debug_inject(self.handle, what))

@@ -1,0 +1,148 @@
+// Device-side helpers of libgb: lane layouts, streaming vector memory access,
+// and the bf16 / OCP fp8 conversions written as inline PTX.
+//
+// Everything on the hot path is HBM-streaming work (a handful of float32 adds
+// per 4-8 bytes moved), so the kernels are built around 128-bit coalesced
+// loads and stores, enough bytes in flight per SM, and warp-shuffle block
+// maxima; there is no dense contraction and no tensor-core work.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gb.h"
+
+namespace gb {
+
+constexpr int kTile = 256;        // elements per warp tile
+constexpr int kWarp = 32;
+constexpr int kPerLane = kTile / kWarp;  // 8 elements per lane
+
+// ---------------------------------------------------------------- layouts
+// A warp tile is 256 consecutive elements.  float32 buffers: lane l owns the
+// two 16-byte vectors at elements 4l and 128 + 4l (two fully coalesced 512 B
+// warp accesses).  bf16 buffers: lane l owns the 16-byte vector at element 8l
+// (one coalesced 512 B warp access).  Element k (0..7) of a lane:
+template <typename T> struct Lay;
+template <> struct Lay<float> {
+    static constexpr int kVec = 4;  // elements per 16-byte vector
+    __device__ __forceinline__ static unsigned idx(int lane, int k) {
+        return (unsigned)((k >> 2) * 128 + lane * 4 + (k & 3));
+    }
+};
+template <> struct Lay<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static unsigned idx(int lane, int k) { return (unsigned)(lane * 8 + k); }
+};
+
+// ------------------------------------------------------- memory accesses
+// Rank buffers are read once per collective: stream them past L1 and mark
+// them evict-first in L2.  Payloads are re-read by the copy engines and the
+// decode kernel, so they are stored normally.
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint4 ld_u4(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_u2(const void *p) {
+    uint2 r;
+    asm("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint32_t ld_u1(const void *p) {
+    uint32_t r;
+    asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st_u4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_u2(void *p, uint2 v) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_u1(void *p, uint32_t v) {
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ------------------------------------------------------------ conversions
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
+
+// Two float32 -> packed bf16x2, round to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two float32 -> packed OCP fp8x2, round to nearest even, saturating to the
+// largest finite value (lo in the low byte).
+template <int CODEC>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+    unsigned short r;
+    if (CODEC == GB_CODEC_E4M3)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Packed fp8x2 (low 16 bits of `pair`) -> two float32 (exact: every E4M3 and
+// E5M2 value is a binary16 value, and every binary16 value a binary32 one).
+template <int CODEC>
+__device__ __forceinline__ void fp8x2_to_f32(uint32_t pair, float &lo, float &hi) {
+    uint32_t h2;
+    unsigned short p = (unsigned short)pair;
+    if (CODEC == GB_CODEC_E4M3)
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(p));
+    else
+        asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(h2) : "h"(p));
+    unsigned short l16 = (unsigned short)(h2 & 0xFFFFu), h16 = (unsigned short)(h2 >> 16);
+    asm("cvt.f32.f16 %0, %1;" : "=f"(lo) : "h"(l16));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(hi) : "h"(h16));
+}
+
+// Largest finite value of the format as M = 0.875 * 2^E.
+template <int CODEC> struct Fp8Fmt;
+template <> struct Fp8Fmt<GB_CODEC_E4M3> { static constexpr int E = 9; };
+template <> struct Fp8Fmt<GB_CODEC_E5M2> { static constexpr int E = 16; };
+
+// Block scale exponent from the bits of the block's largest magnitude m >= 0:
+// the smallest k with m * 2^-k <= 0.875 * 2^E, clamped to k >= -126, and 0
+// for m == 0.  With m = 1.f * 2^(ef - 127), m * 2^-k <= 0.875 * 2^E holds for
+// k = ef - 126 - E exactly when 1.f <= 1.75, i.e. the fraction bits are at
+// most 0x600000; otherwise one more power of two is needed.
+template <int CODEC>
+__device__ __forceinline__ int block_scale_exp(float m) {
+    const uint32_t b = __float_as_uint(m);
+    if (b == 0u) return 0;
+    const int ef = (int)(b >> 23);
+    if (ef == 0) return -126;  // subnormal magnitude: clamped
+    int k = ef - 126 - Fp8Fmt<CODEC>::E + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return k < -126 ? -126 : k;
+}
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
+
+// ---------------------------------------------------------- payload layout
+__host__ __device__ __forceinline__ size_t code_bytes(int codec) {
+    return codec == GB_CODEC_NONE ? 4 : codec == GB_CODEC_BF16 ? 2 : 1;
+}
+__host__ __device__ __forceinline__ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace gb

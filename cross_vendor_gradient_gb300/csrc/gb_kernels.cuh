@@ -1,0 +1,86 @@
+// Kernel argument blocks and launchers of libgb (host-visible declarations).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gb.h"
+
+namespace gb {
+
+// Fused island reduce + bridge encode over every island at once.
+// Island i's ranks are src[first[i] .. first[i+1]); its payload goes to
+// payload[i] (codes at offset 0, fp8 scales at scales_off).
+struct ReduceEncodeArgs {
+    const void *src[GB_MAX_RANKS];
+    void *payload[GB_MAX_ISLANDS];
+    int first[GB_MAX_ISLANDS + 1];
+    int n_islands;
+    uint64_t n;
+    uint64_t tiles;       // warp tiles per island = ceil(n / 256)
+    uint64_t scales_off;  // byte offset of the fp8 scales in a payload
+};
+
+// Fused decode + accumulate + broadcast.
+// Output group g (an island for all_reduce) reads the n_src payloads
+// payload[g][0..n_src) (island order), adds their decoded values in float32,
+// divides by `world` for AVG, rounds to the rank dtype and writes the result.
+//   all_reduce (rs == 0): work item (g, tile), written to every rank buffer
+//     dst[first[g] .. first[g+1]) at the same element index;
+//   reduce_scatter (rs == 1): work item (rank r, tile of its slice of m
+//     elements), global elements [r*m, (r+1)*m) written to dst[r]; group
+//     g = the island of r.  vec == 0 forces the element-wise path (used when
+//     m is not a multiple of 8, which would misalign 16-byte accesses).
+struct DecodeBcastArgs {
+    void *dst[GB_MAX_RANKS];
+    const void *payload[GB_MAX_ISLANDS][GB_MAX_ISLANDS];
+    int first[GB_MAX_ISLANDS + 1];
+    int group_of_rank[GB_MAX_RANKS];
+    int n_groups;
+    int n_src;
+    int avg;
+    float world;
+    uint64_t n;           // elements of the full buffer
+    uint64_t scales_off;
+    int rs;
+    int vec;
+    uint64_t m;           // reduce_scatter slice length
+    uint64_t tiles;       // all_reduce: tiles per group; reduce_scatter: tiles per slice
+};
+
+// accum = dec(payload) or accum + dec(payload).
+struct DecompressAccArgs {
+    const void *payload;
+    float *accum;
+    uint64_t n;
+    uint64_t scales_off;
+    int accumulate;
+};
+
+// Exact copies: job j copies `bytes` from src[j] into dst[d] + dst_off[j]
+// for every d in [dst_lo[j], dst_hi[j]), skipping a destination that is the
+// source itself.
+struct CopyArgs {
+    const unsigned char *src[GB_MAX_RANKS];
+    uint64_t dst_off[GB_MAX_RANKS];
+    int dst_lo[GB_MAX_RANKS];
+    int dst_hi[GB_MAX_RANKS];
+    unsigned char *dst[GB_MAX_RANKS];
+    int n_jobs;
+    uint64_t bytes;
+    int vec;  // all addresses and `bytes` multiples of 16
+};
+
+// Launchers: return the cudaError_t of the launch.
+cudaError_t launch_reduce_encode(const ReduceEncodeArgs &a, int dtype, int codec, int block,
+                                 cudaStream_t s);
+cudaError_t launch_decode_bcast(const DecodeBcastArgs &a, int dtype, int codec, int block,
+                                cudaStream_t s);
+cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, int block,
+                                         cudaStream_t s);
+cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s);
+
+uint64_t launches();
+
+}  // namespace gb

@@ -1,0 +1,277 @@
+/*
+ * gb.h - C ABI of libgb: the reduce-bridge-broadcast gradient all_reduce of
+ * gpubridge, for simulated ranks that all live on one GB300 GPU.
+ *
+ * Model (gpubridge README, island / bridge paragraph and "all_reduce uses
+ * reduce-bridge-broadcast"): W ranks form I islands; island i is the
+ * contiguous block of global ranks [first_i, first_i + K_i), its leader is
+ * its lowest rank.  An all_reduce
+ *   1. sums each island's rank buffers onto the leader (float32, ascending
+ *      rank order),
+ *   2. encodes the island sum for the bridge (codec none / bf16 / fp8),
+ *   3. moves the payloads between leaders through pinned host memory
+ *      (device -> host -> device copies on the caller's stream),
+ *   4. decodes every island's payload and adds them in float32, in island
+ *      order (AVG then divides once by W),
+ *   5. writes the total, rounded to the rank dtype, to every rank buffer.
+ * Each simulated rank's buffer is a separate device allocation owned by the
+ * caller.  Steps 1+2 and 4+5 run as one fused kernel each.
+ *
+ * Conventions for every call below:
+ *   - Pointers named *_bufs / rank_bufs / in / out are arrays of W (or K_i)
+ *     DEVICE pointers, in global rank order, each 16-byte aligned
+ *     (GB_ERR_MISALIGNED otherwise).  The caller owns them.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call validates all of its arguments first and returns an error with
+ *     nothing enqueued; otherwise it enqueues its work on `stream` and returns
+ *     without waiting for it (stream order, as torch.distributed's NCCL
+ *     collectives: gpubridge README, "Stream semantics").  Inputs must not be
+ *     written, and outputs not read, before that work completes.
+ *   - n = 0 is a valid no-op.
+ *   - A context owns its pinned host slots and device staging buffers.  They
+ *     grow to the largest call made so far and are released by gb_destroy
+ *     (gpubridge README, "Pinned staging").  Growing frees and re-allocates,
+ *     which waits for the device; gb_reserve grows ahead of time.
+ *   - Calls on one context are ordered: each call waits (on the device) for
+ *     the previous call's use of the staging buffers, even on another stream.
+ *     Use one context per thread if calls come from several host threads.
+ *   - Sticky failure (gpubridge README, "Async collectives": after a failed
+ *     collective every later one refuses to start): if anything fails after
+ *     work was enqueued (a CUDA error, an allocation failure, an injected
+ *     bridge fault), the call returns that error and every later call on the
+ *     context returns GB_ERR_CONTEXT_FAILED.  Argument errors are not sticky.
+ */
+#ifndef GB_H
+#define GB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef void *gb_stream;
+
+typedef enum {
+    GB_OK = 0,
+    GB_ERR_INVALID_ARG = 1,       /* null pointer, bad layout, bad size, bad rank index   */
+    GB_ERR_UNSUPPORTED_DTYPE = 2, /* dtype other than GB_F32 / GB_BF16                    */
+    GB_ERR_UNSUPPORTED_OP = 3,    /* op other than GB_SUM / GB_AVG                        */
+    GB_ERR_UNSUPPORTED_CODEC = 4, /* unknown codec, or fp8 block not 128 / 256            */
+    GB_ERR_MISALIGNED = 5,        /* a device buffer not 16-byte aligned                  */
+    GB_ERR_ALLOC = 6,             /* pinned or device staging allocation failed (sticky)  */
+    GB_ERR_CUDA = 7,              /* a CUDA runtime call failed (sticky)                  */
+    GB_ERR_BRIDGE = 8,            /* the bridge hop failed (sticky)                       */
+    GB_ERR_CONTEXT_FAILED = 9,    /* an earlier call on this context failed               */
+    GB_ERR_NO_DEVICE = 10         /* no CUDA device is usable                             */
+} gb_status;
+
+typedef enum { GB_F32 = 0, GB_BF16 = 1 } gb_dtype;
+
+/* gpubridge README, API table, all_reduce row: SUM, or AVG = the SUM divided
+ * by the world size, identically on every rank (floating dtypes only). */
+typedef enum { GB_SUM = 0, GB_AVG = 1 } gb_op;
+
+/* gpubridge README, "Bridge compression".
+ *   GB_CODEC_NONE: the payload is the float32 island sum (4n bytes).
+ *   GB_CODEC_BF16: bf16 of the island sum, rounded to nearest even (2n bytes).
+ *   GB_CODEC_E4M3 / GB_CODEC_E5M2: OCP 8-bit floats with one power-of-two
+ *     float32 scale per `block` elements (block 128 or 256; blocks start at
+ *     element 0, the last may be short).  For a block with largest magnitude
+ *     m, the scale is 2^k, k the smallest integer with m * 2^-k <= the
+ *     format's largest finite value (448 / 57344), clamped to k >= -126; k = 0
+ *     for an all-zero block.  code = round-to-nearest-even(x * 2^-k) with
+ *     saturation; decoded value = code value * 2^k (exact).
+ * Compression applies only where there is a bridge (two or more islands);
+ * with one island the codec argument is ignored (gpubridge README: a
+ * single-vendor job has no bridge), and broadcast / all_gather never
+ * compress. */
+typedef enum {
+    GB_CODEC_NONE = 0,
+    GB_CODEC_BF16 = 1,
+    GB_CODEC_E4M3 = 2,
+    GB_CODEC_E5M2 = 3
+} gb_codec;
+
+#define GB_MAX_RANKS 64
+#define GB_MAX_ISLANDS 8
+
+typedef struct gb_ctx gb_ctx;
+
+/* ---------------------------------------------------------------- context */
+
+/* Create a context for W = sum(island_sizes[0..n_islands)) simulated ranks in
+ * n_islands contiguous islands (1 <= n_islands <= GB_MAX_ISLANDS, every size
+ * >= 1, W <= GB_MAX_RANKS).  Makes no CUDA call: the device is the current
+ * CUDA device at the first call that enqueues work, and stays bound.
+ * Errors: GB_ERR_INVALID_ARG (nothing allocated, *out untouched),
+ * GB_ERR_ALLOC (host memory). */
+gb_status gb_create(gb_ctx **out, int n_islands, const int *island_sizes);
+
+/* Wait for the context's outstanding work, free its pinned and device
+ * staging, free the context.  NULL is a no-op. */
+gb_status gb_destroy(gb_ctx *ctx);
+
+/* Topology queries (gpubridge README, Topology: islands, ranks, leaders).
+ * Return -1 for a NULL context or an index out of range. */
+int gb_world_size(const gb_ctx *ctx);
+int gb_n_islands(const gb_ctx *ctx);
+int gb_island_size(const gb_ctx *ctx, int island);
+int gb_island_first_rank(const gb_ctx *ctx, int island); /* = the island's leader */
+int gb_island_of_rank(const gb_ctx *ctx, int rank);
+
+/* Grow the context's staging so that collectives on up to n elements of
+ * `dtype` with `codec` / `block` need no further allocation (for example
+ * before capturing calls in a CUDA graph).  Enqueues nothing. */
+gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int block);
+
+/* The context's sticky status (GB_OK until a call fails after enqueueing)
+ * and a one-line description of the last error on this context. */
+gb_status gb_context_status(const gb_ctx *ctx);
+const char *gb_last_error_message(const gb_ctx *ctx);
+const char *gb_status_string(gb_status status);
+
+/* --------------------------------------------------------------- payloads */
+
+/* Bytes of one island's bridge payload for n elements.  Layout: codes first
+ * (n float32 for none, n bf16 for bf16, n bytes for fp8), then for fp8 the
+ * ceil(n / block) float32 scales, starting at gb_payload_scales_offset (the
+ * code bytes rounded up to 16).  Returns 0 for an unknown codec or block. */
+size_t gb_payload_bytes(gb_codec codec, int block, size_t n);
+size_t gb_payload_scales_offset(gb_codec codec, int block, size_t n);
+
+/* -------------------------------------------------- phase-level building
+ * blocks (gpubridge README, observer phases: island-reduce, compress,
+ * bridge, decompress, island-broadcast).  Composing them as
+ *   island_reduce -> bridge_compress -> (caller moves payloads) ->
+ *   bridge_decompress_accumulate (island 0 with accumulate = 0, then islands
+ *   1..I-1 with accumulate = 1) -> island_broadcast
+ * gives bit for bit what gb_all_reduce gives. */
+
+/* island_sum[j] = ((x_0[j] + x_1[j]) + ...) + x_{K-1}[j] in float32, over the
+ * K = gb_island_size(ctx, island) buffers of `rank_bufs` (that island's
+ * ranks, in rank order).  island_sum: n float32, device, 16-byte aligned,
+ * must not overlap the inputs. */
+gb_status gb_island_reduce(gb_ctx *ctx, int island, const void *const *rank_bufs, size_t n,
+                           gb_dtype dtype, float *island_sum, gb_stream stream);
+
+/* Encode n float32 values (device) into `payload` (device, 16-byte aligned,
+ * gb_payload_bytes(codec, block, n) bytes, laid out as described above).
+ * block is ignored for none / bf16. */
+gb_status gb_bridge_compress(gb_ctx *ctx, const float *island_sum, size_t n, gb_codec codec,
+                             int block, void *payload, gb_stream stream);
+
+/* accum[j] = dec(payload)[j] (accumulate == 0) or accum[j] + dec(payload)[j]
+ * (accumulate != 0), float32, round to nearest even.  accum: n float32,
+ * device, 16-byte aligned. */
+gb_status gb_bridge_decompress_accumulate(gb_ctx *ctx, const void *payload, size_t n,
+                                          gb_codec codec, int block, float *accum, int accumulate,
+                                          gb_stream stream);
+
+/* Write total[j] (SUM) or total[j] / W (AVG, float32 division), rounded to
+ * `dtype` (nearest even for bf16), into the K = gb_island_size(ctx, island)
+ * buffers of `rank_bufs`. */
+gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_t n, gb_op op,
+                              void *const *rank_bufs, gb_dtype dtype, gb_stream stream);
+
+/* ------------------------------------------------------------ collectives */
+
+/* In-place all_reduce of W rank buffers of n elements (gpubridge README, API
+ * table, all_reduce row, and "all_reduce uses reduce-bridge-broadcast").
+ * Every rank buffer ends with the same bits. */
+gb_status gb_all_reduce(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype dtype, gb_op op,
+                        gb_codec codec, int block, gb_stream stream);
+
+/* reduce_scatter (API table, reduce_scatter_tensor row): out_r (n_in / W
+ * elements) receives elements [r * n_in / W, (r + 1) * n_in / W) of what
+ * gb_all_reduce would compute on `in`; the island sums are encoded whole,
+ * with the same codec blocks as gb_all_reduce.  n_in must be a multiple of W.
+ * `in` is not modified; out buffers must not overlap the inputs. */
+gb_status gb_reduce_scatter(gb_ctx *ctx, const void *const *in, void *const *out, size_t n_in,
+                            gb_dtype dtype, gb_op op, gb_codec codec, int block,
+                            gb_stream stream);
+
+/* all_gather (API table, all_gather_into_tensor row): out_r (W * n_in
+ * elements) = in_0 | in_1 | ... | in_{W-1}, exact, for every r.  Data from
+ * another island crosses the bridge (pinned host slots) uncompressed. */
+gb_status gb_all_gather(gb_ctx *ctx, const void *const *in, void *const *out, size_t n_in,
+                        gb_dtype dtype, gb_stream stream);
+
+/* broadcast (API table, broadcast row; three hops: src -> its island, its
+ * leader -> the other leaders over the bridge, each leader -> its island):
+ * every rank buffer receives rank src's n elements, exact, in place. */
+gb_status gb_broadcast(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype dtype, int src,
+                       gb_stream stream);
+
+/* gb_all_reduce for W HOST buffers (pinned, for asynchronous copies): the
+ * buffers are staged onto the GPU in context-owned device buffers, reduced
+ * there and copied back (gpubridge README, torch.distributed backend, CPU
+ * tensors: staged onto the rank's GPU, carried by the same topology and
+ * copied back).  Host buffers need no alignment; they must not be touched
+ * until `stream` has completed the call. */
+gb_status gb_all_reduce_host(gb_ctx *ctx, void *const *host_bufs, size_t n, gb_dtype dtype,
+                             gb_op op, gb_codec codec, int block, gb_stream stream);
+
+/* ------------------------------------------------------ gradient buckets */
+
+/* Greedy bucket plan (gpubridge README, DDP comm hook: one all_reduce per
+ * DDP gradient bucket): walk n_tensors tensors of numel[t] elements of
+ * elem_bytes in the given order; append each to the open bucket unless the
+ * bucket already holds elements and the tensor would take it past cap_bytes,
+ * in which case a new bucket opens (a tensor larger than the cap sits
+ * alone).  Tensors are packed without gaps: tensor t is elements
+ * [offset[t], offset[t] + numel[t]) of bucket bucket_of[t].  Each bucket's
+ * element count is rounded up to a multiple of pad_elems (0 or 1: none).
+ * Host-only; makes no CUDA call.  GB_ERR_INVALID_ARG if more than
+ * max_buckets would be needed. */
+gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, size_t cap_bytes,
+                         size_t pad_elems, int *bucket_of, size_t *offset, size_t *bucket_numel,
+                         int max_buckets, int *n_buckets);
+
+/* One gb_all_reduce per bucket, in bucket order.  bucket_bufs holds
+ * n_buckets * W device pointers, bucket-major (bucket b, rank r at
+ * [b * W + r]); bucket b has bucket_numel[b] elements.  The tensors of the
+ * plan are views into these flat buffers, so nothing is copied in or out. */
+gb_status gb_all_reduce_buckets(gb_ctx *ctx, int n_buckets, void *const *bucket_bufs,
+                                const size_t *bucket_numel, gb_dtype dtype, gb_op op,
+                                gb_codec codec, int block, gb_stream stream);
+
+/* --------------------------------------------------------- phase timing */
+
+/* gpubridge README, "Observing collectives": timing marks per phase, taken
+ * with CUDA events on GPUs, never synchronising the call.  With capacity > 0
+ * every collective records four events on its stream (start, after island
+ * reduce + compress, after the bridge hop, after decompress + broadcast) and
+ * the marks of the last `capacity` collectives are kept; 0 turns the marks
+ * off.  Changing the capacity waits for the context's outstanding work. */
+#define GB_N_PHASES 3 /* 0: island reduce + compress, 1: bridge hop, 2: decompress + broadcast */
+gb_status gb_set_phase_timing(gb_ctx *ctx, int capacity);
+
+/* Milliseconds of each phase of the collective `age` calls back (0 = the
+ * most recent one that recorded marks); waits for its events.  A phase that
+ * collective did not have reads 0.  GB_ERR_INVALID_ARG if no such record. */
+gb_status gb_phase_times(gb_ctx *ctx, int age, float *ms /* [GB_N_PHASES] */);
+gb_status gb_last_phase_times(gb_ctx *ctx, float *ms /* [GB_N_PHASES] */);
+
+/* ------------------------------------------------------------ test hooks */
+
+/* Fault injection for tests, all on the host, none touching the GPU:
+ *   GB_INJECT_BRIDGE: the next bridge hop fails before it enqueues its
+ *     copies (the call returns GB_ERR_BRIDGE, no rank buffer is written,
+ *     the context becomes failed);
+ *   GB_INJECT_ALLOC: the next staging allocation fails (GB_ERR_ALLOC, the
+ *     context becomes failed). */
+#define GB_INJECT_BRIDGE 1
+#define GB_INJECT_ALLOC 2
+gb_status gb_debug_inject(gb_ctx *ctx, int what);
+
+/* Number of kernels this library has launched in this process. */
+uint64_t gb_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB_H */

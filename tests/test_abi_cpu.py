@@ -1,0 +1,149 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/gb.h declares, its host-only logic (payload sizes, bucket plan)
+matches the oracle, and argument validation answers before touching CUDA."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as orc
+from cross_vendor_gradient_gb300 import binding as B
+from cross_vendor_gradient_gb300 import build as gbuild
+from cross_vendor_gradient_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    gbuild.build()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "gb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gb_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    names = _declared()
+    assert len(names) >= 28
+    L = ctypes.CDLL(B.LIB_PATH)
+    for name in names:
+        assert hasattr(L, name), name
+        assert name in B.SIGNATURES, "binding lacks %s" % name
+        assert hasattr(B, name), "binding function %s" % name
+    assert set(B.SIGNATURES) == set(names)
+
+
+def test_status_strings():
+    for s in range(11):
+        assert B.gb_status_string(s).startswith("GB_")
+    assert B.gb_status_string(B.GB_OK) == "GB_OK"
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128),
+                                         ("e4m3", 128)])
+def test_payload_bytes_hold_the_oracle_payload(codec, block):
+    cid = {"none": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}[codec]
+    for n in (1, 7, 255, 256, 257, 1000, 6_553_600):
+        s = np.zeros(min(n, 4096), np.float32)
+        codes, scales = orc.encode(s, codec, block)
+        per = codes.itemsize
+        nsc = orc.n_blocks(n, block) if codec in ("e4m3", "e5m2") else 0
+        P = B.gb_payload_bytes(cid, block, n)
+        off = B.gb_payload_scales_offset(cid, block, n)
+        assert off >= n * per and off % 16 == 0 or nsc == 0
+        assert P == (off + 4 * nsc if nsc else n * per)
+    assert B.gb_payload_bytes(2, 64, 100) == 0 and B.gb_payload_bytes(9, 256, 100) == 0
+
+
+def test_fp8_payload_ratio_is_the_pages_3_9():
+    n = 256 * 25600
+    assert round(4 * n / B.gb_payload_bytes(B.GB_CODEC_E4M3, 256, n), 1) == 3.9
+    assert 4 * n / B.gb_payload_bytes(B.GB_CODEC_BF16, 256, n) == 2.0
+
+
+def test_bucket_plan_matches_oracle():
+    rng = np.random.default_rng(61)
+    cases = [([wl.numel(s) for s in wl.gpt2_small_shapes()], 2, wl.BUCKET_CAP_BYTES, 1),
+             ([wl.numel(s) for s in wl.llama_1b_shapes()], 2, wl.BUCKET_CAP_BYTES, 64)]
+    for _ in range(100):
+        T = int(rng.integers(1, 40))
+        cases.append((list(rng.integers(0, 3000, T)), int(rng.choice([2, 4])), int(rng.integers(1, 9000)),
+                      int(rng.choice([1, 8, 64]))))
+    for numels, eb, cap, pad in cases:
+        st, bo, off, bn = B.gb_bucket_plan(numels, eb, cap, pad)
+        assert st == B.GB_OK
+        obo, ooff, obn = orc.bucket_plan(numels, eb, cap, pad)
+        assert bo == list(obo) and off == [int(v) for v in ooff] and bn == [int(v) for v in obn]
+    st, *_ = B.gb_bucket_plan([10, 10, 10], 4, 40, 1, max_buckets=2)
+    assert st == B.GB_ERR_INVALID_ARG
+
+
+def test_gpt2_and_llama_bucket_counts():
+    st, bo, off, bn = B.gb_bucket_plan([wl.numel(s) for s in wl.gpt2_small_shapes()], 2, wl.BUCKET_CAP_BYTES)
+    assert st == 0 and len(bn) == 9 and bn[0] == 50257 * 768
+    st, bo, off, bn = B.gb_bucket_plan([wl.numel(s) for s in wl.llama_1b_shapes()], 2, wl.BUCKET_CAP_BYTES)
+    assert st == 0 and len(bn) == 90
+
+
+def test_create_validation_and_topology():
+    assert B.gb_create([])[0] == B.GB_ERR_INVALID_ARG
+    assert B.gb_create([2, 0])[0] == B.GB_ERR_INVALID_ARG
+    assert B.gb_create([1] * 9)[0] == B.GB_ERR_INVALID_ARG
+    assert B.gb_create([40, 30])[0] == B.GB_ERR_INVALID_ARG
+    st, ctx = B.gb_create([2, 3, 1])
+    assert st == B.GB_OK and ctx
+    try:
+        assert B.gb_world_size(ctx) == 6 and B.gb_n_islands(ctx) == 3
+        assert [B.gb_island_first_rank(ctx, i) for i in range(3)] == [0, 2, 5]
+        assert [B.gb_island_of_rank(ctx, r) for r in range(6)] == [0, 0, 1, 1, 1, 2]
+        assert B.gb_island_size(ctx, 1) == 3 and B.gb_island_size(ctx, 3) == -1
+        assert B.gb_context_status(ctx) == B.GB_OK
+    finally:
+        assert B.gb_destroy(ctx) == B.GB_OK
+
+
+def test_argument_errors_need_no_device():
+    """Every malformed call is refused before any CUDA call; fake pointers
+    are never dereferenced."""
+    st, ctx = B.gb_create([2, 2])
+    fake = [0x10000 * (r + 1) for r in range(4)]
+    try:
+        assert B.gb_all_reduce(0, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        assert B.gb_all_reduce(ctx, fake, 10, 7, 0, 0, 256) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert B.gb_all_reduce(ctx, fake, 10, 0, 2, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 2, 64) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 5, 256) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_all_reduce(ctx, fake[:3] + [0], 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        assert B.gb_all_reduce(ctx, fake[:3] + [0x10008], 10, 0, 0, 0, 256) == B.GB_ERR_MISALIGNED
+        assert B.gb_reduce_scatter(ctx, fake, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG  # 10 % 4
+        assert B.gb_broadcast(ctx, fake, 10, 0, 4) == B.GB_ERR_INVALID_ARG
+        assert B.gb_island_reduce(ctx, 2, fake, 10, 0, fake[0]) == B.GB_ERR_INVALID_ARG
+        assert B.gb_island_reduce(ctx, 0, fake, 10, 0, fake[0] + 4) == B.GB_ERR_MISALIGNED
+        assert B.gb_all_reduce(ctx, fake, 1 << 39, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        # n == 0 is a valid no-op, answered without a device
+        assert B.gb_all_reduce(ctx, fake, 0, 0, 0, 2, 256) == B.GB_OK
+        assert B.gb_all_gather(ctx, fake, fake, 0, 1) == B.GB_OK
+        # none of these is sticky
+        assert B.gb_context_status(ctx) == B.GB_OK
+        assert B.gb_debug_inject(ctx, 77) == B.GB_ERR_INVALID_ARG
+    finally:
+        B.gb_destroy(ctx)
+
+
+def test_no_device_is_reported_not_sticky():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    st, ctx = B.gb_create([1, 1])
+    fake = [0x10000, 0x20000]
+    try:
+        assert B.gb_all_reduce(ctx, fake, 16, 0, 0, 0, 256) == B.GB_ERR_NO_DEVICE
+        assert B.gb_context_status(ctx) == B.GB_OK
+        assert "device" in B.gb_last_error_message(ctx)
+    finally:
+        B.gb_destroy(ctx)

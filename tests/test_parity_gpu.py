@@ -1,0 +1,266 @@
+"""CUDA path vs the oracle, element by element and bit for bit, through the
+C ABI, at sizes that span several warp tiles and codec blocks and end in a
+ragged tail, for every codec, layout, rank dtype and op."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from cross_vendor_gradient_gb300 import Context, payload_bytes, payload_scales_offset
+from cross_vendor_gradient_gb300 import binding as B
+from cross_vendor_gradient_gb300 import workloads as wl
+from tests.gpu_util import assert_bits_equal, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+CODECS = [("none", 256), ("bf16", 256), ("e4m3", 256), ("e4m3", 128), ("e5m2", 128), ("e5m2", 256)]
+LAYOUTS = [(1,), (1, 1), (2, 2), (1, 3), (4, 4), (2, 1, 3), (8,), (1, 1, 1, 1, 1, 1, 1, 1)]
+SIZES = [1, 7, 8, 255, 256, 257, 1000, 4096 + 13, 65536 + 200]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def inputs(sizes, n, dtype="f32", dist="normal_1e-3_outliers", cid=11):
+    w = wl.Workload("t", cid, tuple(sizes), dtype, dist, "sum", ())
+    return wl.host_rank_inputs(w, n=n)
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("sizes", LAYOUTS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_reduce_matches_oracle(codec, block, sizes, dtype):
+    with Context(sizes) as ctx:
+        for n in SIZES:
+            for op in ("sum", "avg"):
+                xs = inputs(sizes, n, dtype, cid=n % 97)
+                bufs = [to_dev(x) for x in xs]
+                ctx.all_reduce(bufs, op, codec, block)
+                want = orc.all_reduce(xs, sizes, op, codec, block)
+                torch.cuda.synchronize()
+                for r, b in enumerate(bufs):
+                    assert_bits_equal(to_host(b), want[r], "%s/%d %s n=%d %s rank %d" % (
+                        codec, block, sizes, n, op, r))
+
+
+@pytest.mark.parametrize("dist", ["uniform_pm1", "student_t3_1e-3", "normal_1e-3_zero_blocks", "integers"])
+@pytest.mark.parametrize("codec,block", CODECS)
+def test_all_reduce_distributions(dist, codec, block):
+    sizes = (2, 2)
+    n = 128 * 1000 + 77
+    xs = inputs(sizes, n, "f32", dist, cid=5)
+    with Context(sizes) as ctx:
+        bufs = [to_dev(x) for x in xs]
+        ctx.all_reduce(bufs, "sum", codec, block)
+        want = orc.all_reduce(xs, sizes, "sum", codec, block)
+        torch.cuda.synchronize()
+        for r, b in enumerate(bufs):
+            assert_bits_equal(to_host(b), want[r], "%s %s rank %d" % (dist, codec, r))
+
+
+def test_special_blocks():
+    """Zero, signed-zero, subnormal, huge and mixed-binade blocks."""
+    B_ = 256
+    n = B_ * 12 + 5
+    rng = np.random.default_rng(3)
+    base = rng.standard_normal(n).astype(np.float32)
+    x0 = base.copy()
+    x1 = (-base).copy()                      # block 0 cancels to exact zeros
+    x0[B_:2 * B_] = -0.0
+    x1[B_:2 * B_] = -0.0                     # all -0.0: sum -0.0
+    x0[2 * B_:3 * B_] *= np.float32(1e-39)   # subnormal sums
+    x1[2 * B_:3 * B_] = 0
+    x0[3 * B_:4 * B_] *= np.float32(1e37)    # near the top of float32
+    x1[3 * B_:4 * B_] = 0
+    x0[4 * B_:5 * B_] = np.float32(448.0)
+    x1[4 * B_:5 * B_] = np.float32(0.0)      # absmax exactly M
+    x0[5 * B_] = np.float32(448.0 * 2.0 ** 10 * (1 + 2.0 ** -20))  # just above M * 2^10
+    x0[6 * B_:7 * B_] = np.exp2(rng.integers(-60, 60, B_)).astype(np.float32)  # mixed binades
+    xs = [x0, x1]
+    x1[:B_] = -x0[:B_]
+    for codec, block in CODECS:
+        with Context((1, 1)) as ctx:
+            bufs = [to_dev(x) for x in xs]
+            ctx.all_reduce(bufs, "sum", codec, block)
+            want = orc.all_reduce(xs, (1, 1), "sum", codec, block)
+            torch.cuda.synchronize()
+            for r, b in enumerate(bufs):
+                assert_bits_equal(to_host(b), want[r], "special %s/%d rank %d" % (codec, block, r))
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_phase_blocks_match_oracle_and_compose_to_all_reduce(codec, block, dtype):
+    """island_reduce, bridge_compress, bridge_decompress_accumulate and
+    island_broadcast each match the oracle's step bit for bit, and their
+    composition equals the fused all_reduce."""
+    sizes = (2, 3)
+    n = 3000 + 11
+    xs = inputs(sizes, n, dtype, cid=23)
+    _, mid = orc.rbb_total(xs, sizes, "avg", codec, block, intermediates=True)
+    with Context(sizes) as ctx:
+        bufs = [to_dev(x) for x in xs]
+        first = [0, 2]
+        payloads = []
+        for i, K in enumerate(sizes):
+            s = torch.empty(n, dtype=torch.float32, device="cuda")
+            ctx.island_reduce(i, bufs[first[i]:first[i] + K], s)
+            torch.cuda.synchronize()
+            assert_bits_equal(to_host(s), mid["island_sums"][i], "island sum %d" % i)
+            P = payload_bytes(codec, block, n)
+            p = torch.empty(P, dtype=torch.uint8, device="cuda")
+            ctx.bridge_compress(s, codec, block, p)
+            torch.cuda.synchronize()
+            ph = to_host(p)
+            cd = orc.code_dtype(codec)
+            cb = np.dtype(cd).itemsize
+            assert_bits_equal(ph[:n * cb].view(cd), mid["codes"][i], "codes %d" % i)
+            if codec in ("e4m3", "e5m2"):
+                off = payload_scales_offset(codec, block, n)
+                nb = orc.n_blocks(n, block)
+                assert_bits_equal(ph[off:off + 4 * nb].view(np.float32), mid["scales"][i], "scales %d" % i)
+                dec = orc.decode(mid["codes"][i], mid["scales"][i], codec, block)
+            else:
+                dec = orc.decode(mid["codes"][i], np.zeros(0, np.float32), codec, block)
+            one = torch.empty(n, dtype=torch.float32, device="cuda")
+            ctx.bridge_decompress_accumulate(p, n, codec, block, one, False)
+            torch.cuda.synchronize()
+            assert_bits_equal(to_host(one), dec, "decode %d" % i)
+            payloads.append(p)
+        total = torch.empty(n, dtype=torch.float32, device="cuda")
+        for i, p in enumerate(payloads):
+            ctx.bridge_decompress_accumulate(p, n, codec, block, total, i > 0)
+        outs = [torch.empty_like(b) for b in bufs]
+        for i, K in enumerate(sizes):
+            ctx.island_broadcast(i, total, "avg", outs[first[i]:first[i] + K])
+        ctx.all_reduce(bufs, "avg", codec, block)
+        want = orc.all_reduce(xs, sizes, "avg", codec, block)
+        torch.cuda.synchronize()
+        for r in range(sum(sizes)):
+            assert_bits_equal(to_host(outs[r]), want[r], "composed rank %d" % r)
+            assert_bits_equal(to_host(bufs[r]), want[r], "fused rank %d" % r)
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (4, 4), (1, 2), (3,), (2, 1, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_reduce_scatter_and_all_gather(codec, block, sizes, dtype):
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        for m in (1, 5, 8, 300, 4096, 4099):  # slice lengths: 8 | m uses 16-byte accesses
+            n = W * m
+            xs = inputs(sizes, n, dtype, cid=m % 13)
+            ins = [to_dev(x) for x in xs]
+            outs = [torch.empty(m, dtype=ins[0].dtype, device="cuda") for _ in range(W)]
+            ctx.reduce_scatter(ins, outs, "avg", codec, block)
+            want = orc.reduce_scatter(xs, sizes, "avg", codec, block)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(outs[r]), want[r], "RS %s m=%d rank %d" % (sizes, m, r))
+                assert_bits_equal(to_host(ins[r]), xs[r], "RS input untouched %d" % r)
+            gathered = [torch.empty(n, dtype=ins[0].dtype, device="cuda") for _ in range(W)]
+            ctx.all_gather(outs, gathered)
+            ar = orc.all_reduce(xs, sizes, "avg", codec, block)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(gathered[r]), ar[r], "RS then AG == AR rank %d" % r)
+
+
+@pytest.mark.parametrize("sizes", [(1,), (1, 1), (2, 2), (1, 3), (3, 2, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_gather_and_broadcast_exact(sizes, dtype):
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        for m in (1, 3, 8, 1001, 4096):
+            xs = inputs(sizes, m, dtype, cid=m % 7)
+            ins = [to_dev(x) for x in xs]
+            outs = [torch.empty(W * m, dtype=ins[0].dtype, device="cuda") for _ in range(W)]
+            ctx.all_gather(ins, outs)
+            want = orc.all_gather(xs)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(outs[r]), want[r], "AG m=%d rank %d" % (m, r))
+            for src in range(W):
+                bufs = [to_dev(x) for x in xs]
+                ctx.broadcast(bufs, src)
+                want = orc.broadcast(xs, src)
+                torch.cuda.synchronize()
+                for r in range(W):
+                    assert_bits_equal(to_host(bufs[r]), want[r], "bcast src %d rank %d" % (src, r))
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+def test_all_reduce_host_buffers(codec, block):
+    sizes = (2, 2)
+    n = 70000 + 3
+    xs = inputs(sizes, n, "f32", cid=31)
+    with Context(sizes) as ctx:
+        host = [torch.from_numpy(x.copy()).pin_memory() for x in xs]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            ctx.all_reduce_host(host, "avg", codec, block)
+        s.synchronize()
+        want = orc.all_reduce(xs, sizes, "avg", codec, block)
+        for r in range(4):
+            assert_bits_equal(host[r].numpy(), want[r], "host rank %d" % r)
+
+
+def test_bucketed_all_reduce_small_model():
+    """A scaled-down gradient set (a handful of tensors of mixed sizes) with
+    a small cap so that it spans several buckets, bf16 ranks, e5m2/128."""
+    sizes = (2, 2)
+    W = 4
+    shapes = [(300, 7), (64,), (33, 33), (5,), (1000,), (128, 9), (2,)]
+    numels = [wl.numel(s) for s in shapes]
+    bo, off, bn = orc.bucket_plan(numels, 2, 4096, 8)
+    assert len(bn) >= 3
+    with Context(sizes) as ctx:
+        buckets, hosts = [], []
+        for b, nb_ in enumerate(bn):
+            xs = inputs(sizes, int(nb_), "bf16", cid=40 + b)
+            hosts.append(xs)
+            buckets.append([to_dev(x) for x in xs])
+        ctx.all_reduce_buckets(buckets, "sum", "e5m2", 128)
+        torch.cuda.synchronize()
+        for b in range(len(bn)):
+            want = orc.all_reduce(hosts[b], sizes, "sum", "e5m2", 128)
+            for r in range(W):
+                assert_bits_equal(to_host(buckets[b][r]), want[r], "bucket %d rank %d" % (b, r))
+
+
+def test_other_stream_and_phase_timing():
+    sizes = (2, 2)
+    n = 1 << 20
+    xs = inputs(sizes, n, "f32", cid=77)
+    with Context(sizes) as ctx:
+        ctx.set_phase_timing(4)
+        s = torch.cuda.Stream()
+        bufs = [to_dev(x) for x in xs]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            ctx.all_reduce(bufs, "sum", "e4m3", 256)
+        ms = ctx.last_phase_times()
+        s.synchronize()
+        assert all(v > 0 for v in ms), ms
+        want = orc.all_reduce(xs, sizes, "sum", "e4m3", 256)
+        for r in range(4):
+            assert_bits_equal(to_host(bufs[r]), want[r], "stream rank %d" % r)
+        # a second call on the default stream is ordered after the first
+        ctx.all_reduce(bufs, "sum", "none", 256)
+        torch.cuda.synchronize()
+        want2 = orc.all_reduce(want, sizes, "sum", "none", 256)
+        assert_bits_equal(to_host(bufs[0]), want2[0], "second call")
+
+
+def test_empty_inputs_are_noops():
+    with Context((2, 2)) as ctx:
+        bufs = [torch.zeros(16, device="cuda") for _ in range(4)]
+        st = B.gb_all_reduce(ctx.handle, [b.data_ptr() for b in bufs], 0, 0, 0, 2, 256, 0)
+        assert st == B.GB_OK
+        st = B.gb_reduce_scatter(ctx.handle, [b.data_ptr() for b in bufs], [b.data_ptr() for b in bufs],
+                                 0, 0, 0, 0, 256, 0)
+        assert st == B.GB_OK

@@ -23,6 +23,7 @@ GB_ERR_CUDA = 7
 GB_ERR_BRIDGE = 8
 GB_ERR_CONTEXT_FAILED = 9
 GB_ERR_NO_DEVICE = 10
+GB_ERR_TOO_LARGE = 11
 # gb_dtype / gb_op / gb_codec
 GB_F32, GB_BF16 = 0, 1
 GB_SUM, GB_AVG = 0, 1
@@ -32,6 +33,8 @@ GB_MAX_ISLANDS = 8
 GB_N_PHASES = 3
 GB_INJECT_BRIDGE = 1
 GB_INJECT_ALLOC = 2
+GB_NOALLOC_DEVICE_BYTES = 64 << 20
+GB_NOALLOC_HOST_BYTES = 32 << 20
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -68,6 +71,7 @@ SIGNATURES = {
     "gb_phase_times": (_i, [_vp, _i, _P(ctypes.c_float)]),
     "gb_last_phase_times": (_i, [_vp, _P(ctypes.c_float)]),
     "gb_debug_inject": (_i, [_vp, _i]),
+    "gb_all_reduce_noalloc": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_kernel_launch_count": (ctypes.c_uint64, []),
 }
 
@@ -237,6 +241,10 @@ def gb_last_phase_times(ctx):
 
 def gb_debug_inject(ctx, what):
     return lib().gb_debug_inject(ctx, what)
+
+
+def gb_all_reduce_noalloc(ctx, rank_bufs, n, dtype, op, codec, block, stream=0):
+    return lib().gb_all_reduce_noalloc(ctx, _ptrs(rank_bufs), n, dtype, op, codec, block, stream)
 
 
 def gb_kernel_launch_count():

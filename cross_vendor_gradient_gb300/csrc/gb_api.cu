@@ -433,6 +433,7 @@ const char *gb_status_string(gb_status s) {
     case GB_ERR_BRIDGE: return "GB_ERR_BRIDGE";
     case GB_ERR_CONTEXT_FAILED: return "GB_ERR_CONTEXT_FAILED";
     case GB_ERR_NO_DEVICE: return "GB_ERR_NO_DEVICE";
+    case GB_ERR_TOO_LARGE: return "GB_ERR_TOO_LARGE";
     default: return "GB_ERR_UNKNOWN";
     }
 }

@@ -1,0 +1,159 @@
+// gb_all_reduce_noalloc: the reduce-bridge-broadcast all_reduce without any
+// memory allocation, for callers that must not allocate.
+//
+// Who needs it: code that runs where a cudaMalloc / cudaHostAlloc is not an
+// option -- a gradient hook inside a training step whose framework has
+// already reserved nearly all device memory in its own caching allocator (a
+// cudaMalloc there can fail, and the cudaFree that growing staging implies
+// waits for the whole device), or a host process that must not pin more
+// memory.  gb_all_reduce grows context-owned device and pinned staging on
+// demand; this variant instead uses
+//   - one file-scope __device__ array of GB_NOALLOC_DEVICE_BYTES for the
+//     payloads (own + received), present on every GPU that loads the
+//     library until the process exits, and
+//   - one file-scope host array of GB_NOALLOC_HOST_BYTES for the bridge
+//     slots, in ordinary pageable memory (the copies are then synchronous
+//     for the host, like the pageable default of the pages' bridge).
+// It produces the same bits as gb_all_reduce (same kernels, same payload
+// layout per island, same island order).
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "gb.h"
+#include "gb_device.cuh"
+#include "gb_kernels.cuh"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_scratch[GB_NOALLOC_DEVICE_BYTES];
+alignas(256) static unsigned char g_host_slots[GB_NOALLOC_HOST_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mu;
+void *g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device (looked up once per
+// device).  In host code `g_scratch` only names a host-side shadow symbol,
+// so the kernels must be given this address, never &g_scratch.
+gb_status scratch_address(int dev, unsigned char **out) {
+    if (dev < 0 || dev >= kMaxDevices) return GB_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+        if (e != cudaSuccess || !p) {
+            cudaGetLastError();
+            return GB_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = (unsigned char *)g_scratch_addr[dev];
+    return GB_OK;
+}
+
+size_t payload_bytes_of(int codec, int block, size_t n) {
+    switch (codec) {
+    case GB_CODEC_NONE: return 4 * n;
+    case GB_CODEC_BF16: return 2 * n;
+    default: return gb::round_up(n, 16) + 4 * ((n + block - 1) / block);
+    }
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace
+
+extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, size_t n,
+                                           gb_dtype dtype, gb_op op, gb_codec codec, int block,
+                                           gb_stream stream) {
+    // ---- validation: the same rules as gb_all_reduce, plus the size limit
+    if (!ctx) return GB_ERR_INVALID_ARG;
+    if (gb_context_status(ctx) != GB_OK) return GB_ERR_CONTEXT_FAILED;
+    if (dtype != GB_F32 && dtype != GB_BF16) return GB_ERR_UNSUPPORTED_DTYPE;
+    if (op != GB_SUM && op != GB_AVG) return GB_ERR_UNSUPPORTED_OP;
+    if (gb_payload_bytes(codec, block, 1) == 0) return GB_ERR_UNSUPPORTED_CODEC;
+    const int I = gb_n_islands(ctx), W = gb_world_size(ctx);
+    if (!rank_bufs) return GB_ERR_INVALID_ARG;
+    for (int r = 0; r < W; ++r) {
+        if (!rank_bufs[r]) return GB_ERR_INVALID_ARG;
+        if (!aligned16(rank_bufs[r])) return GB_ERR_MISALIGNED;
+    }
+    if (n == 0) return GB_OK;
+    const int eff = I == 1 ? GB_CODEC_NONE : (int)codec;
+    const int blk = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? block : 256;
+    const size_t P = payload_bytes_of(eff, blk, n);
+    const size_t slot = gb::round_up(P, 256);
+    // own payloads (I slots), then each leader's received payloads (I - 1 slots each)
+    if (n > (size_t)GB_NOALLOC_DEVICE_BYTES || slot > GB_NOALLOC_DEVICE_BYTES / ((size_t)I * I) ||
+        (I > 1 && slot > GB_NOALLOC_HOST_BYTES / (size_t)I))
+        return GB_ERR_TOO_LARGE;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GB_ERR_NO_DEVICE;
+    }
+    unsigned char *scratch = nullptr;
+    gb_status st = scratch_address(dev, &scratch);
+    if (st != GB_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    int first[GB_MAX_ISLANDS + 1];
+    for (int i = 0; i < I; ++i) first[i] = gb_island_first_rank(ctx, i);
+    first[I] = W;
+
+    // ---- island reduce + encode into the own-payload slots
+    gb::ReduceEncodeArgs ra;
+    memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < W; ++r) ra.src[r] = rank_bufs[r];
+    for (int i = 0; i < I; ++i) ra.payload[i] = scratch + (size_t)i * slot;
+    for (int i = 0; i <= I; ++i) ra.first[i] = first[i];
+    ra.n_islands = I;
+    ra.n = n;
+    ra.tiles = (n + gb::kTile - 1) / gb::kTile;
+    ra.scales_off = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? gb::round_up(n, 16) : P;
+    if (gb::launch_reduce_encode(ra, dtype, eff, blk, s) != cudaSuccess) return GB_ERR_CUDA;
+
+    // ---- bridge hop through the host slots: own slots out, others' in
+    unsigned char *inbox = scratch + (size_t)I * slot;
+    if (I > 1) {
+        if (cudaMemcpyAsync(g_host_slots, scratch, (size_t)(I - 1) * slot + P, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+            return GB_ERR_BRIDGE;
+        for (int g = 0; g < I; ++g) {
+            unsigned char *mine = inbox + (size_t)g * (I - 1) * slot;
+            if (g > 0 && cudaMemcpyAsync(mine, g_host_slots, (size_t)(g - 1) * slot + P,
+                                         cudaMemcpyHostToDevice, s) != cudaSuccess)
+                return GB_ERR_BRIDGE;
+            if (g < I - 1 && cudaMemcpyAsync(mine + (size_t)g * slot, g_host_slots + (size_t)(g + 1) * slot,
+                                             (size_t)(I - g - 2) * slot + P, cudaMemcpyHostToDevice,
+                                             s) != cudaSuccess)
+                return GB_ERR_BRIDGE;
+        }
+    }
+
+    // ---- decode + accumulate (island order) + broadcast to every rank
+    gb::DecodeBcastArgs da;
+    memset(&da, 0, sizeof da);
+    for (int r = 0; r < W; ++r) {
+        da.dst[r] = rank_bufs[r];
+        da.group_of_rank[r] = gb_island_of_rank(ctx, r);
+    }
+    for (int g = 0; g < I; ++g)
+        for (int j = 0; j < I; ++j)
+            da.payload[g][j] = (j == g) ? (const void *)(scratch + (size_t)j * slot)
+                                        : (const void *)(inbox + ((size_t)g * (I - 1) + (j < g ? j : j - 1)) * slot);
+    for (int i = 0; i <= I; ++i) da.first[i] = first[i];
+    da.n_groups = I;
+    da.n_src = I;
+    da.avg = op == GB_AVG;
+    da.world = (float)W;
+    da.n = n;
+    da.scales_off = ra.scales_off;
+    da.rs = 0;
+    da.vec = 1;
+    da.tiles = ra.tiles;
+    if (gb::launch_decode_bcast(da, dtype, eff, blk, s) != cudaSuccess) return GB_ERR_CUDA;
+    return GB_OK;
+}

@@ -65,7 +65,8 @@ typedef enum {
     GB_ERR_CUDA = 7,              /* a CUDA runtime call failed (sticky)                  */
     GB_ERR_BRIDGE = 8,            /* the bridge hop failed (sticky)                       */
     GB_ERR_CONTEXT_FAILED = 9,    /* an earlier call on this context failed               */
-    GB_ERR_NO_DEVICE = 10         /* no CUDA device is usable                             */
+    GB_ERR_NO_DEVICE = 10,        /* no CUDA device is usable                             */
+    GB_ERR_TOO_LARGE = 11         /* exceeds the fixed buffers of gb_all_reduce_noalloc   */
 } gb_status;
 
 typedef enum { GB_F32 = 0, GB_BF16 = 1 } gb_dtype;
@@ -266,6 +267,43 @@ gb_status gb_last_phase_times(gb_ctx *ctx, float *ms /* [GB_N_PHASES] */);
 #define GB_INJECT_BRIDGE 1
 #define GB_INJECT_ALLOC 2
 gb_status gb_debug_inject(gb_ctx *ctx, int what);
+
+/* ------------------------------------------- all_reduce without allocation
+ * No counterpart on the gpubridge page: an addition of this library.
+ *
+ * For callers that cannot allocate memory at the point where they sync
+ * gradients: for example a hook running inside a training step whose
+ * framework has already reserved almost all device memory in its own caching
+ * allocator (a cudaMalloc there can fail, and freeing staging to grow it
+ * waits for the whole device), or a process that must not pin more host
+ * memory.  gb_all_reduce grows context-owned device and pinned host staging
+ * on demand; gb_all_reduce_noalloc computes the same bits without any
+ * allocation:
+ *   - its payload staging is one fixed device array of
+ *     GB_NOALLOC_DEVICE_BYTES, defined in the library, which every GPU that
+ *     loads the library holds until the process exits;
+ *   - its bridge slots are one fixed host array of GB_NOALLOC_HOST_BYTES in
+ *     ordinary pageable memory, so the device -> host copy blocks the
+ *     calling thread until the first kernel and the copy have finished.
+ * Limits: with I islands and P = gb_payload_bytes(codec, block, n) (the
+ * float32 sum, 4n, when I == 1), I * I * round_up(P, 256) must fit the
+ * device array and I * round_up(P, 256) the host array; larger calls return
+ * GB_ERR_TOO_LARGE with nothing enqueued.  Other arguments are checked as in
+ * gb_all_reduce.
+ * Sharing: every call in the process uses the same two arrays, which keep
+ * the last call's contents; nothing in them needs to start at zero (each
+ * call reads only what it wrote).  Calls that overlap on the GPU -- from
+ * several host threads, or on several streams without ordering between
+ * them -- race on the arrays; order them.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ * The context supplies only the island layout: this call neither uses the
+ * context's staging nor marks it failed; a failed context is refused. */
+#define GB_NOALLOC_DEVICE_BYTES (64u << 20)
+#define GB_NOALLOC_HOST_BYTES (32u << 20)
+gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                gb_op op, gb_codec codec, int block, gb_stream stream);
 
 /* Number of kernels this library has launched in this process. */
 uint64_t gb_kernel_launch_count(void);

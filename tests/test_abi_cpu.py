@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported_and_bound():
 
 
 def test_status_strings():
-    for s in range(11):
+    for s in range(12):
         assert B.gb_status_string(s).startswith("GB_")
     assert B.gb_status_string(B.GB_OK) == "GB_OK"
 

@@ -8,7 +8,8 @@ A step is one gb_all_reduce of that bucket: fused island reduce + encode
 kernel, bridge hop (device -> pinned host -> device copies), fused decode +
 accumulate + broadcast kernel.  Before every timed step the rank buffers are
 restored from a pristine device copy and L2 is flushed by writing a 512 MiB
-buffer; neither is inside the step's CUDA events.
+buffer and then reading a separate 256 MiB one (so no dirty line is left to
+be written back during the step); neither is inside the step's CUDA events.
 
 Reported: algorithm GB/s (bytes of one rank buffer / step time, summed over
 replicas), the dominant kernel's HBM roofline fraction from its live CUDA
@@ -45,6 +46,9 @@ def parse():
     p.add_argument("--workload", default="c2")
     p.add_argument("--codec", default=None)
     p.add_argument("--n", type=int, default=None, help="override elements per rank")
+    p.add_argument("--chunk-kib", type=int, default=None,
+                   help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
+    p.add_argument("--no-graphs", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
     return p.parse_args()
@@ -200,9 +204,12 @@ def run_gb(args, world, rank, local, pg):
     pristine = [dev_tensor(x) for x in xs]
     bufs = [p.clone() for p in pristine]
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     K, Wm = args.steps, args.warmup
     ctx = Context(w.island_sizes)
+    chunk_bytes = 4 << 20 if args.chunk_kib is None else args.chunk_kib << 10
+    ctx.set_pipeline(chunk_bytes, not args.no_graphs)
     ctx.reserve(n, tdt, codec, w.block)
     ctx.set_phase_timing(K)
 
@@ -230,7 +237,8 @@ def run_gb(args, world, rank, local, pg):
     def step(i, timed):
         for r in range(W):
             bufs[r].copy_(pristine[r], non_blocking=True)
-        flush.zero_()
+        flush.zero_()   # L2 flush: write 512 MiB ...
+        clean.amax()    # ... then read 256 MiB, so the lines left in L2 are clean
         if timed:
             ev0[i].record(stream)
         ctx.all_reduce(bufs, w.op, codec, w.block, stream=stream)
@@ -299,8 +307,13 @@ def run_gb(args, world, rank, local, pg):
                                    w.key, W, list(w.island_sizes), n * b / 2 ** 20, w.dtype, n, w.dist,
                                    w.op, codec, w.block),
                    "ranks": W, "islands": list(w.island_sizes), "n": n, "codec": codec, "block": w.block,
-                   "op": w.op, "l2": "flushed before every timed step (512 MiB write); inputs restored "
-                                     "from a device copy outside the timed events",
+                   "op": w.op,
+                   "policy": ("pipelined-reduce-bridge-broadcast, %d KiB payload chunks%s" % (
+                       chunk_bytes >> 10, ", CUDA graph replay" if not args.no_graphs else "")
+                              if chunk_bytes else "reduce-bridge-broadcast"),
+                   "l2": "flushed before every timed step (512 MiB write, then a 256 MiB "
+                                     "read so that no dirty line is left); inputs restored from a device "
+                                     "copy outside the timed events",
                    "parallelism": "replicas x%d" % world},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -322,15 +335,26 @@ def run_gb(args, world, rank, local, pg):
     return line, w, xs, codec
 
 
-def traffic_from_profiles(kernel):
-    """dram bytes per launch recorded by an ncu capture of the current kernel
-    source, or None (profiles/dram_traffic.txt, 'key=value' lines)."""
+KERNEL_SOURCES = ("gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_device.cuh", "gb_kernels.cuh")
+
+
+def kernel_source_sha():
+    """sha256[:16] over the kernel sources (the key of a recorded capture)."""
     import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "cross_vendor_gradient_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel
+    sources, or None (profiles/dram_traffic.txt, 'key=value' lines)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    src = os.path.join(ROOT, "cross_vendor_gradient_gb300", "csrc", "gb_kernels.cu")
     if not os.path.exists(path):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha()
     for line in open(path):
         line = line.strip()
         if not line or line.startswith("#"):

@@ -105,6 +105,11 @@ class Context:
     def status(self):
         return B.gb_context_status(self.handle)
 
+    def set_pipeline(self, chunk_bytes, use_graphs=True):
+        """chunk_bytes > 0: pipelined bridge in chunks of that many rank-buffer
+        bytes (default 4 MiB); 0: one bridge hop per call."""
+        self._check(B.gb_set_pipeline(self.handle, chunk_bytes, use_graphs))
+
     def reserve(self, n, dtype=torch.float32, codec="none", block=256):
         self._check(B.gb_reserve(self.handle, n, _DTYPES[dtype], _codec(codec), block))
 

@@ -51,6 +51,7 @@ SIGNATURES = {
     "gb_island_first_rank": (_i, [_vp, _i]),
     "gb_island_of_rank": (_i, [_vp, _i]),
     "gb_reserve": (_i, [_vp, _sz, _i, _i, _i]),
+    "gb_set_pipeline": (_i, [_vp, _sz, _i]),
     "gb_context_status": (_i, [_vp]),
     "gb_last_error_message": (ctypes.c_char_p, [_vp]),
     "gb_status_string": (ctypes.c_char_p, [_i]),
@@ -141,6 +142,10 @@ def gb_island_of_rank(ctx, rank):
 
 def gb_reserve(ctx, n, dtype, codec, block):
     return lib().gb_reserve(ctx, n, dtype, codec, block)
+
+
+def gb_set_pipeline(ctx, chunk_bytes, use_graphs=1):
+    return lib().gb_set_pipeline(ctx, int(chunk_bytes), 1 if use_graphs else 0)
 
 
 def gb_context_status(ctx):

@@ -15,6 +15,31 @@
 
 using gb::round_up;
 
+namespace {
+constexpr int kMaxChunks = 32;
+// timing marks of one collective: 0 start, 1 end of island reduce + encode,
+// 2 bridge start, 3 bridge end, then decode start / end per chunk
+constexpr int kMarks = 4 + 2 * kMaxChunks;
+constexpr int kMaxGraphs = 16;
+}  // namespace
+
+// Identity of a captured all_reduce (every value its graph bakes in).
+struct GraphKey {
+    const void *in[GB_MAX_RANKS];
+    uint64_t n, chunk;
+    int dtype, op, codec, block, timed, pad;
+    const void *d_stage, *h_stage;
+};
+
+struct GraphEntry {
+    GraphKey key;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;  // null: seen once, not captured yet
+    cudaGraphNode_t mark_node[kMarks] = {};
+    int n_marks = 0;
+    uint64_t last_use = 0;
+};
+
 struct gb_ctx {
     int I = 0, W = 0;
     int size[GB_MAX_ISLANDS] = {};
@@ -24,10 +49,11 @@ struct gb_ctx {
     gb_status sticky = GB_OK;
     char msg[256] = {};
     int inject = 0;
-    // device staging: I own-payload slots, then I x I inbox slots
+    // device staging, chunk-major: C x I own-payload parts, then I leaders x
+    // C x I received parts
     unsigned char *d_stage = nullptr;
     size_t d_stage_bytes = 0;
-    // pinned host staging: the bridge slots
+    // pinned host staging: the bridge slots, C x I parts
     unsigned char *h_stage = nullptr;
     size_t h_stage_bytes = 0;
     // device copies of host rank buffers (gb_all_reduce_host)
@@ -37,11 +63,22 @@ struct gb_ctx {
     cudaEvent_t done = nullptr;
     bool done_recorded = false;
     cudaStream_t last_stream = nullptr;
-    // phase timing (observer marks): a ring of `tcap` records of 4 events
+    // pipelined-reduce-bridge-broadcast: chunk size, copy streams, events
+    size_t chunk_bytes = 4u << 20;
+    int use_graphs = 1;
+    cudaStream_t sd = nullptr, sh = nullptr, scap = nullptr;
+    cudaEvent_t ev_k1[kMaxChunks] = {}, ev_d2h[kMaxChunks] = {}, ev_h2d[kMaxChunks] = {};
+    cudaEvent_t ev_join_d = nullptr, ev_join_h = nullptr;
+    cudaEvent_t cap_mark[kMarks] = {};  // stand-ins recorded while capturing
+    GraphEntry graphs[kMaxGraphs];
+    int n_graphs = 0;
+    uint64_t clock = 0;
+    // phase timing (observer marks): a ring of `tcap` records of kMarks events
     int tcap = 0;
     cudaEvent_t *tev = nullptr;
-    long long tcount = 0;   // collectives recorded so far
-    bool ev_bridge = false;
+    int *tnk2 = nullptr;
+    unsigned char *tbridge = nullptr;
+    long long tcount = 0;  // collectives recorded so far
 };
 
 namespace {
@@ -130,7 +167,8 @@ gb_status check_dev_ptr(gb_ctx *c, const void *p, const char *name) {
         if (_s != GB_OK) return _s;          \
     } while (0)
 
-// Bind the context to the current device on first use.
+// Bind the context to the current device on first use (creates its streams
+// and events there).
 gb_status bind(gb_ctx *c) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -141,6 +179,21 @@ gb_status bind(gb_ctx *c) {
     if (c->device < 0) {
         if ((e = cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming)) != cudaSuccess)
             return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+        cudaStream_t *streams[3] = {&c->sd, &c->sh, &c->scap};
+        for (cudaStream_t *st : streams)
+            if ((e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking)) != cudaSuccess)
+                return fail(c, GB_ERR_CUDA, "cudaStreamCreate", e);
+        for (int i = 0; i < kMaxChunks; ++i) {
+            cudaEvent_t *evs[3] = {&c->ev_k1[i], &c->ev_d2h[i], &c->ev_h2d[i]};
+            for (cudaEvent_t *ev : evs)
+                if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
+                    return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+        }
+        if ((e = cudaEventCreateWithFlags(&c->ev_join_d, cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->ev_join_h, cudaEventDisableTiming)) != cudaSuccess)
+            return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+        for (int i = 0; i < kMarks; ++i)
+            if ((e = cudaEventCreate(&c->cap_mark[i])) != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
         c->device = dev;
     } else if (dev != c->device) {
         return set_msg(c, GB_ERR_INVALID_ARG, "context is bound to device %d, current device is %d",
@@ -166,25 +219,67 @@ gb_status end(gb_ctx *c, cudaStream_t s) {
     return GB_OK;
 }
 
-gb_status mark(gb_ctx *c, int i, cudaStream_t s) {
-    if (c->tcap <= 0) return GB_OK;
-    cudaEvent_t &ev = c->tev[(size_t)(c->tcount % c->tcap) * 4 + i];
-    cudaError_t e = cudaSuccess;
-    if (!ev && (e = cudaEventCreate(&ev)) != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
-    if ((e = cudaEventRecord(ev, s)) != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventRecord", e);
-    if (i == 3) ++c->tcount;
+// Timing marks.  mode 0: off; 1: record the ring slot's event (direct
+// launches); 2: record the stand-in event as an event-record node of a graph
+// being captured (re-pointed at the ring slot's event before each launch).
+enum { kMarkOff = 0, kMarkDirect = 1, kMarkCapture = 2 };
+
+gb_status ring_event(gb_ctx *c, long long slot, int idx, cudaEvent_t *out) {
+    cudaEvent_t &ev = c->tev[(size_t)slot * kMarks + idx];
+    if (!ev) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+    }
+    *out = ev;
     return GB_OK;
+}
+
+gb_status mark(gb_ctx *c, int mode, int idx, cudaStream_t s) {
+    if (mode == kMarkOff) return GB_OK;
+    cudaEvent_t ev;
+    unsigned flags = cudaEventRecordDefault;
+    if (mode == kMarkCapture) {
+        ev = c->cap_mark[idx];
+        flags = cudaEventRecordExternal;
+    } else {
+        GB_TRY(ring_event(c, c->tcount % c->tcap, idx, &ev));
+    }
+    cudaError_t e = cudaEventRecordWithFlags(ev, s, flags);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventRecord", e);
+    return GB_OK;
+}
+
+// The marks of one collective are complete: remember its shape, advance.
+void commit_marks(gb_ctx *c, int n_decode, bool bridge) {
+    if (c->tcap <= 0) return;
+    const long long slot = c->tcount % c->tcap;
+    c->tnk2[slot] = n_decode;
+    c->tbridge[slot] = bridge ? 1 : 0;
+    ++c->tcount;
 }
 
 void free_marks(gb_ctx *c) {
     if (c->tev) {
-        for (int i = 0; i < 4 * c->tcap; ++i)
+        for (size_t i = 0; i < (size_t)c->tcap * kMarks; ++i)
             if (c->tev[i]) cudaEventDestroy(c->tev[i]);
         delete[] c->tev;
     }
+    delete[] c->tnk2;
+    delete[] c->tbridge;
     c->tev = nullptr;
+    c->tnk2 = nullptr;
+    c->tbridge = nullptr;
     c->tcap = 0;
     c->tcount = 0;
+}
+
+void drop_graphs(gb_ctx *c) {
+    for (int i = 0; i < c->n_graphs; ++i) {
+        if (c->graphs[i].exec) cudaGraphExecDestroy(c->graphs[i].exec);
+        if (c->graphs[i].graph) cudaGraphDestroy(c->graphs[i].graph);
+        c->graphs[i] = GraphEntry();
+    }
+    c->n_graphs = 0;
 }
 
 gb_status grow_device(gb_ctx *c, unsigned char **buf, size_t *have, size_t need) {
@@ -194,6 +289,7 @@ gb_status grow_device(gb_ctx *c, unsigned char **buf, size_t *have, size_t need)
         return fail(c, GB_ERR_ALLOC, "device staging allocation failed (injected)");
     }
     if (*buf) {
+        if (buf == &c->d_stage) drop_graphs(c);
         cudaFree(*buf);  // waits for the device
         *buf = nullptr;
         *have = 0;
@@ -215,6 +311,7 @@ gb_status grow_host(gb_ctx *c, size_t need) {
         return fail(c, GB_ERR_ALLOC, "pinned staging allocation failed (injected)");
     }
     if (c->h_stage) {
+        drop_graphs(c);
         cudaFreeHost(c->h_stage);  // waits for the device
         c->h_stage = nullptr;
         c->h_stage_bytes = 0;
@@ -243,13 +340,61 @@ size_t scales_offset(int codec, size_t n) {
     return (codec == GB_CODEC_E4M3 || codec == GB_CODEC_E5M2) ? round_up(n, 16) : payload_bytes(codec, 256, n);
 }
 
-// Staging needed by a reduce-bridge-broadcast over n elements.
-void rbb_staging(const gb_ctx *c, size_t n, int codec, int block, size_t *dev, size_t *host,
-                 size_t *slot) {
-    const int eff = c->I == 1 ? GB_CODEC_NONE : codec;
-    *slot = round_up(payload_bytes(eff, block, n), 256);
-    *dev = (size_t)(c->I + (c->I > 1 ? c->I * c->I : 0)) * *slot;
-    *host = c->I > 1 ? (size_t)c->I * *slot : 0;
+// Shape of one reduce-bridge-broadcast: the element range is cut into C
+// chunks of whole 256-element tiles (so whole codec blocks); every chunk's
+// payload parts have a fixed stride `part`.  C == 1 is the plain policy.
+struct Plan {
+    int I = 0, W = 0;
+    uint64_t n = 0;
+    gb_dtype dtype = GB_F32;
+    gb_op op = GB_SUM;
+    int eff = GB_CODEC_NONE, blk = 256, rs = 0;
+    size_t eb = 4, cb = 4;
+    uint64_t chunk = 0;
+    int C = 1;
+    size_t part = 0;
+    size_t dev_bytes = 0, host_bytes = 0;
+};
+
+bool is_fp8(int codec) { return codec == GB_CODEC_E4M3 || codec == GB_CODEC_E5M2; }
+
+size_t part_bytes(const Plan &p, uint64_t m) {
+    size_t b = round_up(m * p.cb, 16);
+    if (is_fp8(p.eff)) b += 4 * ((m + p.blk - 1) / p.blk);
+    return b;
+}
+
+Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs) {
+    Plan p;
+    p.I = c->I;
+    p.W = c->W;
+    p.n = n;
+    p.dtype = dtype;
+    p.op = op;
+    p.rs = rs;
+    p.eff = c->I == 1 ? GB_CODEC_NONE : (int)codec;
+    p.blk = is_fp8(p.eff) ? block : 256;
+    p.eb = elem_bytes(dtype);
+    p.cb = p.eff == GB_CODEC_NONE ? 4 : p.eff == GB_CODEC_BF16 ? 2 : 1;
+    p.chunk = n;
+    if (!rs && c->I > 1 && c->chunk_bytes > 0) {
+        // chunk_bytes of one island's payload per chunk
+        const double per_elem = (double)p.cb + (is_fp8(p.eff) ? 4.0 / p.blk : 0.0);
+        uint64_t ch = (uint64_t)((double)c->chunk_bytes / per_elem) / gb::kTile * gb::kTile;
+        if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
+        const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
+        if (ch < min_ch) ch = min_ch;
+        if (ch < n) p.chunk = ch;
+    }
+    p.C = (int)((n + p.chunk - 1) / p.chunk);
+    p.part = round_up(part_bytes(p, p.chunk), 256);
+    // received parts: two islands share one mirror of the host slots (leader
+    // 1 holds island 0's part, leader 0 island 1's); more islands keep one
+    // I-part region per leader
+    const int recv = p.I == 1 ? 0 : p.I == 2 ? 2 : p.I * p.I;
+    p.dev_bytes = (size_t)(p.I + recv) * p.C * p.part;
+    p.host_bytes = p.I > 1 ? (size_t)p.I * p.C * p.part : 0;
+    return p;
 }
 
 gb_status check_launch(gb_ctx *c, cudaError_t e, const char *what) {
@@ -265,95 +410,254 @@ gb_status copy_async(gb_ctx *c, void *dst, const void *src, size_t bytes, cudaMe
     return GB_OK;
 }
 
-// The bridge hop of reduce-bridge-broadcast: every island's payload (slot i
-// of the device outbox) goes to pinned host slot i; every leader i receives
-// the other islands' slots into its inbox.  All on the caller's stream.
-gb_status bridge_exchange(gb_ctx *c, size_t P, size_t slot, cudaStream_t s) {
-    const int I = c->I;
-    if (c->inject == GB_INJECT_BRIDGE) {
-        c->inject = 0;
-        return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+gb_status wait_on(gb_ctx *c, cudaStream_t s, cudaEvent_t ev) {
+    cudaError_t e = cudaStreamWaitEvent(s, ev, 0);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamWaitEvent", e);
+    return GB_OK;
+}
+
+gb_status record(gb_ctx *c, cudaEvent_t ev, cudaStream_t s) {
+    cudaError_t e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventRecord", e);
+    return GB_OK;
+}
+
+// Enqueue one reduce-bridge-broadcast.  Kernels run on s.  With multi (and
+// more than one island) the bridge copies run on the context's copy streams
+// so that, chunk by chunk, encode, device -> host, host -> device and
+// decode overlap: chunk c's copies wait for its encode, and its decode waits
+// for its copies.  Staging (see Plan): own parts outbox(c, i), host slots
+// host(c, j), leader g's received parts inbox(g, c, j).
+gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *const *out, cudaStream_t s,
+                      int markmode, bool multi) {
+    const int I = p.I;
+    auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
+    // leader g's received copy of island j's part of chunk ch (j != g)
+    auto inbox = [&](int g, int ch, int j) {
+        unsigned char *base = c->d_stage + (size_t)I * p.C * p.part;
+        if (I == 2) return base + ((size_t)ch * I + j) * p.part;  // mirror of the host slots
+        return base + (((size_t)g * p.C + ch) * I + j) * p.part;
+    };
+    auto host = [&](int ch, int j) { return c->h_stage + ((size_t)ch * I + j) * p.part; };
+    multi = multi && I > 1 && p.C > 1;
+
+    // 1. island reduce + encode, chunk by chunk
+    GB_TRY(mark(c, markmode, 0, s));
+    for (int ch = 0; ch < p.C; ++ch) {
+        const uint64_t e0 = (uint64_t)ch * p.chunk;
+        const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+        gb::ReduceEncodeArgs ra;
+        memset(&ra, 0, sizeof ra);
+        for (int r = 0; r < p.W; ++r) ra.src[r] = (const unsigned char *)in[r] + e0 * p.eb;
+        for (int i = 0; i < I; ++i) ra.payload[i] = outbox(ch, i);
+        for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
+        ra.n_islands = I;
+        ra.n = m;
+        ra.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
+        ra.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
+        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        if (multi) GB_TRY(record(c, c->ev_k1[ch], s));
     }
-    unsigned char *outbox = c->d_stage;
-    unsigned char *inbox = c->d_stage + (size_t)I * slot;
-    // leaders -> host (the own-payload slots are contiguous: one copy)
-    GB_TRY(copy_async(c, c->h_stage, outbox, (size_t)(I - 1) * slot + P, cudaMemcpyDeviceToHost, s));
-    // host -> every leader, the slots of the other islands
-    for (int i = 0; i < I; ++i) {
-        unsigned char *mine = inbox + (size_t)i * I * slot;
-        if (i > 0)
-            GB_TRY(copy_async(c, mine, c->h_stage, (size_t)(i - 1) * slot + P, cudaMemcpyHostToDevice, s));
-        if (i < I - 1)
-            GB_TRY(copy_async(c, mine + (size_t)(i + 1) * slot, c->h_stage + (size_t)(i + 1) * slot,
-                              (size_t)(I - i - 2) * slot + P, cudaMemcpyHostToDevice, s));
+    GB_TRY(mark(c, markmode, 1, s));
+
+    // 2. the bridge hop: own parts to the host slots, others' parts to every leader
+    if (I > 1) {
+        if (c->inject == GB_INJECT_BRIDGE) {
+            c->inject = 0;
+            return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+        }
+        cudaStream_t D = multi ? c->sd : s, H = multi ? c->sh : s;
+        for (int ch = 0; ch < p.C; ++ch) {
+            const uint64_t e0 = (uint64_t)ch * p.chunk;
+            const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+            const size_t pb = part_bytes(p, m);
+            if (multi) GB_TRY(wait_on(c, D, c->ev_k1[ch]));
+            if (ch == 0) GB_TRY(mark(c, markmode, 2, D));
+            GB_TRY(copy_async(c, host(ch, 0), outbox(ch, 0), (size_t)(I - 1) * p.part + pb, cudaMemcpyDeviceToHost, D));
+            if (multi) {
+                GB_TRY(record(c, c->ev_d2h[ch], D));
+                GB_TRY(wait_on(c, H, c->ev_d2h[ch]));
+            }
+            if (I == 2) {  // island 0's part to leader 1, island 1's part to leader 0: one copy
+                GB_TRY(copy_async(c, inbox(1, ch, 0), host(ch, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+            } else {
+                for (int g = 0; g < I; ++g) {
+                    if (g > 0)
+                        GB_TRY(copy_async(c, inbox(g, ch, 0), host(ch, 0), (size_t)(g - 1) * p.part + pb,
+                                          cudaMemcpyHostToDevice, H));
+                    if (g < I - 1)
+                        GB_TRY(copy_async(c, inbox(g, ch, g + 1), host(ch, g + 1),
+                                          (size_t)(I - g - 2) * p.part + pb, cudaMemcpyHostToDevice, H));
+                }
+            }
+            if (multi) GB_TRY(record(c, c->ev_h2d[ch], H));
+        }
+        GB_TRY(mark(c, markmode, 3, H));
+    }
+
+    // 3. decode + accumulate + broadcast, chunk by chunk
+    for (int ch = 0; ch < p.C; ++ch) {
+        const uint64_t e0 = (uint64_t)ch * p.chunk;
+        const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+        if (multi) GB_TRY(wait_on(c, s, c->ev_h2d[ch]));
+        GB_TRY(mark(c, markmode, 4 + 2 * ch, s));
+        gb::DecodeBcastArgs da;
+        memset(&da, 0, sizeof da);
+        for (int r = 0; r < p.W; ++r) {
+            da.dst[r] = (unsigned char *)out[r] + (p.rs ? 0 : e0 * p.eb);
+            da.group_of_rank[r] = c->island_of[r];
+        }
+        for (int g = 0; g < I; ++g)
+            for (int j = 0; j < I; ++j)
+                da.payload[g][j] = (j == g) ? (const void *)outbox(ch, j) : (const void *)inbox(g, ch, j);
+        for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
+        da.n_groups = I;
+        da.n_src = I;
+        da.avg = p.op == GB_AVG;
+        da.world = (float)p.W;
+        da.world_pow2 = (p.W & (p.W - 1)) == 0;
+        da.inv_world = 1.0f / (float)p.W;
+        da.n = m;
+        da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
+        if (p.rs) {  // one chunk: slices of the full range
+            da.rs = 1;
+            da.m = p.n / (uint64_t)p.W;
+            da.vec = (da.m % 8) == 0;
+            da.tiles = (uint32_t)((da.m + gb::kTile - 1) / gb::kTile);
+        } else {
+            da.rs = 0;
+            da.vec = 1;
+            da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
+        }
+        if (da.tiles > 0)
+            GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        GB_TRY(mark(c, markmode, 5 + 2 * ch, s));
+    }
+    if (multi) {  // the copy streams' last work precedes the end of the call
+        GB_TRY(record(c, c->ev_join_d, c->sd));
+        GB_TRY(record(c, c->ev_join_h, c->sh));
+        GB_TRY(wait_on(c, s, c->ev_join_d));
+        GB_TRY(wait_on(c, s, c->ev_join_h));
     }
     return GB_OK;
 }
 
+// Capture one pipelined all_reduce on the context's capture stream and
+// instantiate it.  The stand-in mark events become event-record nodes.
+gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, bool timed, GraphEntry *ge) {
+    cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
+    gb_status st = enqueue_rbb(c, p, in, (void *const *)in, c->scap, timed ? kMarkCapture : kMarkOff, true);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(c->scap, &g);
+    if (st != GB_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamEndCapture", e);
+    cudaGraphExec_t x = nullptr;
+    if ((e = cudaGraphInstantiate(&x, g, 0)) != cudaSuccess) {
+        cudaGraphDestroy(g);
+        return fail(c, GB_ERR_CUDA, "cudaGraphInstantiate", e);
+    }
+    ge->graph = g;
+    ge->exec = x;
+    ge->n_marks = 0;
+    if (timed) {
+        size_t count = 0;
+        cudaGraphGetNodes(g, nullptr, &count);
+        cudaGraphNode_t *nodes = new (std::nothrow) cudaGraphNode_t[count ? count : 1];
+        if (!nodes) return fail(c, GB_ERR_ALLOC, "graph node list");
+        cudaGraphGetNodes(g, nodes, &count);
+        for (size_t i = 0; i < count; ++i) {
+            cudaGraphNodeType t;
+            cudaEvent_t ev;
+            if (cudaGraphNodeGetType(nodes[i], &t) != cudaSuccess || t != cudaGraphNodeTypeEventRecord) continue;
+            if (cudaGraphEventRecordNodeGetEvent(nodes[i], &ev) != cudaSuccess) continue;
+            for (int k = 0; k < kMarks; ++k)
+                if (c->cap_mark[k] == ev) {
+                    ge->mark_node[k] = nodes[i];
+                    ++ge->n_marks;
+                }
+        }
+        delete[] nodes;
+    }
+    return GB_OK;
+}
+
+GraphEntry *find_graph(gb_ctx *c, const GraphKey &k) {
+    for (int i = 0; i < c->n_graphs; ++i)
+        if (memcmp(&c->graphs[i].key, &k, sizeof k) == 0) return &c->graphs[i];
+    return nullptr;
+}
+
+GraphEntry *new_graph_slot(gb_ctx *c) {
+    if (c->n_graphs < kMaxGraphs) return &c->graphs[c->n_graphs++];
+    int lru = 0;
+    for (int i = 1; i < c->n_graphs; ++i)
+        if (c->graphs[i].last_use < c->graphs[lru].last_use) lru = i;
+    GraphEntry &g = c->graphs[lru];
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+    if (g.graph) cudaGraphDestroy(g.graph);
+    g = GraphEntry();
+    return &g;
+}
+
 // Reduce-bridge-broadcast over W rank buffers `in` (n elements).  rs == 0:
 // the total goes to out[r] (all n elements; out may equal in).  rs == 1:
-// out[r] receives slice r (n / W elements).
+// out[r] receives slice r (n / W elements).  A pipelined in-place
+// all_reduce runs as a CUDA graph captured on the second call with the same
+// buffers and shape (the first runs directly) and replayed afterwards.
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
                   gb_op op, gb_codec codec, int block, cudaStream_t s, int rs) {
-    const int I = c->I;
-    const int eff = I == 1 ? GB_CODEC_NONE : (int)codec;
-    const int blk = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? block : 256;
-    size_t dev, host, slot;
-    rbb_staging(c, n, eff, blk, &dev, &host, &slot);
-    const size_t P = payload_bytes(eff, blk, n);
-    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, dev));
-    if (host) GB_TRY(grow_host(c, host));
+    const Plan p = make_plan(c, n, dtype, op, codec, block, rs);
+    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
+    if (p.host_bytes) GB_TRY(grow_host(c, p.host_bytes));
     GB_TRY(begin(c, s));
-    GB_TRY(mark(c, 0, s));
-
-    gb::ReduceEncodeArgs ra;
-    memset(&ra, 0, sizeof ra);
-    for (int r = 0; r < c->W; ++r) ra.src[r] = in[r];
-    for (int i = 0; i < I; ++i) ra.payload[i] = c->d_stage + (size_t)i * slot;
-    for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
-    ra.n_islands = I;
-    ra.n = n;
-    ra.tiles = (n + gb::kTile - 1) / gb::kTile;
-    ra.scales_off = scales_offset(eff, n);
-    GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, dtype, eff, blk, s), "island reduce + encode"));
-    GB_TRY(mark(c, 1, s));
-
-    if (I > 1) GB_TRY(bridge_exchange(c, P, slot, s));
-    c->ev_bridge = I > 1;
-    GB_TRY(mark(c, 2, s));
-
-    gb::DecodeBcastArgs da;
-    memset(&da, 0, sizeof da);
-    for (int r = 0; r < c->W; ++r) {
-        da.dst[r] = out[r];
-        da.group_of_rank[r] = c->island_of[r];
+    const bool timed = c->tcap > 0;
+    const bool graphable = !rs && p.C > 1 && c->use_graphs && (const void *)in == (const void *)out;
+    if (!graphable) {
+        GB_TRY(enqueue_rbb(c, p, in, out, s, timed ? kMarkDirect : kMarkOff, p.C > 1));
+        commit_marks(c, p.C, p.I > 1);
+        return end(c, s);
     }
-    unsigned char *inbox = c->d_stage + (size_t)I * slot;
-    for (int g = 0; g < I; ++g)
-        for (int j = 0; j < I; ++j)
-            da.payload[g][j] = (j == g) ? (const void *)(c->d_stage + (size_t)j * slot)
-                                        : (const void *)(inbox + ((size_t)g * I + j) * slot);
-    for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
-    da.n_groups = I;
-    da.n_src = I;
-    da.avg = op == GB_AVG;
-    da.world = (float)c->W;
-    da.n = n;
-    da.scales_off = scales_offset(eff, n);
-    if (rs) {
-        da.rs = 1;
-        da.m = n / (size_t)c->W;
-        da.vec = (da.m % 8) == 0;
-        da.tiles = (da.m + gb::kTile - 1) / gb::kTile;
-    } else {
-        da.rs = 0;
-        da.vec = 1;
-        da.m = 0;
-        da.tiles = (n + gb::kTile - 1) / gb::kTile;
+    GraphKey k;
+    memset(&k, 0, sizeof k);
+    for (int r = 0; r < c->W; ++r) k.in[r] = in[r];
+    k.n = n;
+    k.chunk = p.chunk;
+    k.dtype = dtype;
+    k.op = op;
+    k.codec = p.eff;
+    k.block = p.blk;
+    k.timed = timed;
+    k.d_stage = c->d_stage;
+    k.h_stage = c->h_stage;
+    GraphEntry *ge = find_graph(c, k);
+    if (!ge) {  // first time: run directly (loads modules, sizes grids), remember the shape
+        ge = new_graph_slot(c);
+        ge->key = k;
+        ge->last_use = ++c->clock;
+        GB_TRY(enqueue_rbb(c, p, in, out, s, timed ? kMarkDirect : kMarkOff, true));
+        commit_marks(c, p.C, true);
+        return end(c, s);
     }
-    if (da.tiles > 0)
-        GB_TRY(check_launch(c, gb::launch_decode_bcast(da, dtype, eff, blk, s), "decode + broadcast"));
-    GB_TRY(mark(c, 3, s));
+    ge->last_use = ++c->clock;
+    if (!ge->exec) GB_TRY(capture_rbb(c, p, in, timed, ge));
+    if (timed) {
+        const long long slot = c->tcount % c->tcap;
+        for (int idx = 0; idx < kMarks; ++idx) {
+            if (!ge->mark_node[idx]) continue;
+            cudaEvent_t ev;
+            GB_TRY(ring_event(c, slot, idx, &ev));
+            cudaError_t e = cudaGraphExecEventRecordNodeSetEvent(ge->exec, ge->mark_node[idx], ev);
+            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphExecEventRecordNodeSetEvent", e);
+        }
+    }
+    cudaError_t e = cudaGraphLaunch(ge->exec, s);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphLaunch", e);
+    for (int k = 0; k < 2 * p.C; ++k) gb::count_launch();  // the graph's kernel nodes
+    commit_marks(c, p.C, true);
     return end(c, s);
 }
 
@@ -404,7 +708,20 @@ gb_status gb_destroy(gb_ctx *c) {
         if (c->d_ranks) cudaFree(c->d_ranks);
         if (c->h_stage) cudaFreeHost(c->h_stage);
         if (c->done) cudaEventDestroy(c->done);
+        drop_graphs(c);
         free_marks(c);
+        cudaStream_t streams[3] = {c->sd, c->sh, c->scap};
+        for (cudaStream_t st : streams)
+            if (st) cudaStreamDestroy(st);
+        for (int i = 0; i < kMaxChunks; ++i) {
+            cudaEvent_t evs[3] = {c->ev_k1[i], c->ev_d2h[i], c->ev_h2d[i]};
+            for (cudaEvent_t ev : evs)
+                if (ev) cudaEventDestroy(ev);
+        }
+        if (c->ev_join_d) cudaEventDestroy(c->ev_join_d);
+        if (c->ev_join_h) cudaEventDestroy(c->ev_join_h);
+        for (int i = 0; i < kMarks; ++i)
+            if (c->cap_mark[i]) cudaEventDestroy(c->cap_mark[i]);
         if (cur >= 0 && cur != c->device) cudaSetDevice(cur);
     }
     delete c;
@@ -454,11 +771,23 @@ gb_status gb_reserve(gb_ctx *c, size_t n, gb_dtype dtype, gb_codec codec, int bl
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
     GB_TRY(bind(c));
-    size_t dev, host, slot;
-    rbb_staging(c, n, codec, block, &dev, &host, &slot);
+    const Plan ar = make_plan(c, n, dtype, GB_SUM, codec, block, 0);
+    const Plan rs = make_plan(c, n, dtype, GB_SUM, codec, block, 1);
     const size_t ag_host = (size_t)c->W * n * elem_bytes(dtype);
+    const size_t dev = ar.dev_bytes > rs.dev_bytes ? ar.dev_bytes : rs.dev_bytes;
+    size_t host = ar.host_bytes > rs.host_bytes ? ar.host_bytes : rs.host_bytes;
+    if (ag_host > host) host = ag_host;
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, dev));
-    GB_TRY(grow_host(c, host > ag_host ? host : ag_host));
+    GB_TRY(grow_host(c, host));
+    return GB_OK;
+}
+
+gb_status gb_set_pipeline(gb_ctx *c, size_t chunk_bytes, int use_graphs) {
+    if (!c) return GB_ERR_INVALID_ARG;
+    if (c->device >= 0 && c->done_recorded) cudaEventSynchronize(c->done);
+    drop_graphs(c);
+    c->chunk_bytes = chunk_bytes;
+    c->use_graphs = use_graphs ? 1 : 0;
     return GB_OK;
 }
 
@@ -482,7 +811,7 @@ gb_status gb_island_reduce(gb_ctx *c, int island, const void *const *rank_bufs, 
     ra.first[1] = K;
     ra.n_islands = 1;
     ra.n = n;
-    ra.tiles = (n + gb::kTile - 1) / gb::kTile;
+    ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
     ra.scales_off = 0;
     return check_launch(c, gb::launch_reduce_encode(ra, dtype, GB_CODEC_NONE, 256, s), "island reduce");
 }
@@ -505,7 +834,7 @@ gb_status gb_bridge_compress(gb_ctx *c, const float *island_sum, size_t n, gb_co
     ra.first[1] = 1;
     ra.n_islands = 1;
     ra.n = n;
-    ra.tiles = (n + gb::kTile - 1) / gb::kTile;
+    ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
     ra.scales_off = scales_offset(codec, n);
     return check_launch(c, gb::launch_reduce_encode(ra, GB_F32, codec, blk, (cudaStream_t)stream),
                         "bridge compress");
@@ -553,11 +882,13 @@ gb_status gb_island_broadcast(gb_ctx *c, int island, const float *total, size_t 
     da.n_src = 1;
     da.avg = op == GB_AVG;
     da.world = (float)c->W;
+    da.world_pow2 = (c->W & (c->W - 1)) == 0;
+    da.inv_world = 1.0f / (float)c->W;
     da.n = n;
     da.scales_off = 0;
     da.rs = 0;
     da.vec = 1;
-    da.tiles = (n + gb::kTile - 1) / gb::kTile;
+    da.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
     return check_launch(c, gb::launch_decode_bcast(da, dtype, GB_CODEC_NONE, 256, (cudaStream_t)stream),
                         "island broadcast");
 }
@@ -600,13 +931,15 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
     const size_t mb = n_in * elem_bytes(dtype);
     if (I > 1) GB_TRY(grow_host(c, (size_t)W * mb));
     GB_TRY(begin(c, s));
-    GB_TRY(mark(c, 0, s));
-    GB_TRY(mark(c, 1, s));
+    const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
+    GB_TRY(mark(c, mm, 0, s));
+    GB_TRY(mark(c, mm, 1, s));
     if (I > 1) {
         if (c->inject == GB_INJECT_BRIDGE) {
             c->inject = 0;
             return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
         }
+        GB_TRY(mark(c, mm, 2, s));
         // every rank's block goes to the host slots ...
         for (int q = 0; q < W; ++q)
             GB_TRY(copy_async(c, c->h_stage + (size_t)q * mb, in[q], mb, cudaMemcpyDeviceToHost, s));
@@ -617,9 +950,9 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
             GB_TRY(copy_async(c, lead, c->h_stage, lo, cudaMemcpyHostToDevice, s));
             GB_TRY(copy_async(c, lead + hi, c->h_stage + hi, (size_t)W * mb - hi, cudaMemcpyHostToDevice, s));
         }
+        GB_TRY(mark(c, mm, 3, s));
     }
-    c->ev_bridge = I > 1;
-    GB_TRY(mark(c, 2, s));
+    GB_TRY(mark(c, mm, 4, s));
     // each island: own ranks' blocks from the inputs, the others from the
     // leader's received copy, into every rank of the island
     for (int i = 0; i < I; ++i) {
@@ -639,7 +972,8 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
         for (int k = 0; k < c->size[i]; ++k) a.dst[k] = (unsigned char *)out[c->first[i] + k];
         GB_TRY(check_launch(c, gb::launch_copy(a, s), "all_gather copy"));
     }
-    GB_TRY(mark(c, 3, s));
+    GB_TRY(mark(c, mm, 5, s));
+    commit_marks(c, 1, I > 1);
     return end(c, s);
 }
 
@@ -658,22 +992,24 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
     const size_t nb = n * elem_bytes(dtype);
     if (I > 1) GB_TRY(grow_host(c, nb));
     GB_TRY(begin(c, s));
-    GB_TRY(mark(c, 0, s));
-    GB_TRY(mark(c, 1, s));
+    const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
+    GB_TRY(mark(c, mm, 0, s));
+    GB_TRY(mark(c, mm, 1, s));
     if (I > 1) {
         if (c->inject == GB_INJECT_BRIDGE) {
             c->inject = 0;
             return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
         }
+        GB_TRY(mark(c, mm, 2, s));
         // src's island leader sends over the bridge (the bytes are src's);
         // every other leader receives in place
         GB_TRY(copy_async(c, c->h_stage, rank_bufs[src], nb, cudaMemcpyDeviceToHost, s));
         for (int i = 0; i < I; ++i)
             if (i != si)
                 GB_TRY(copy_async(c, rank_bufs[c->first[i]], c->h_stage, nb, cudaMemcpyHostToDevice, s));
+        GB_TRY(mark(c, mm, 3, s));
     }
-    c->ev_bridge = I > 1;
-    GB_TRY(mark(c, 2, s));
+    GB_TRY(mark(c, mm, 4, s));
     // each island: its source (src, or the leader that received) -> its ranks
     gb::CopyArgs a;
     memset(&a, 0, sizeof a);
@@ -688,7 +1024,8 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
         a.dst_hi[i] = c->first[i + 1];
     }
     GB_TRY(check_launch(c, gb::launch_copy(a, s), "broadcast copy"));
-    GB_TRY(mark(c, 3, s));
+    GB_TRY(mark(c, mm, 5, s));
+    commit_marks(c, 1, I > 1);
     return end(c, s);
 }
 
@@ -766,10 +1103,16 @@ gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bu
 gb_status gb_set_phase_timing(gb_ctx *c, int capacity) {
     if (!c || capacity < 0 || capacity > (1 << 20)) return GB_ERR_INVALID_ARG;
     if (c->tev && c->done_recorded) cudaEventSynchronize(c->done);
+    drop_graphs(c);
     free_marks(c);
     if (capacity > 0) {
-        c->tev = new (std::nothrow) cudaEvent_t[(size_t)capacity * 4]();
-        if (!c->tev) return set_msg(c, GB_ERR_ALLOC, "phase timing records");
+        c->tev = new (std::nothrow) cudaEvent_t[(size_t)capacity * kMarks]();
+        c->tnk2 = new (std::nothrow) int[capacity]();
+        c->tbridge = new (std::nothrow) unsigned char[capacity]();
+        if (!c->tev || !c->tnk2 || !c->tbridge) {
+            free_marks(c);
+            return set_msg(c, GB_ERR_ALLOC, "phase timing records");
+        }
         c->tcap = capacity;
     }
     return GB_OK;
@@ -780,12 +1123,20 @@ gb_status gb_phase_times(gb_ctx *c, int age, float *ms) {
     for (int i = 0; i < GB_N_PHASES; ++i) ms[i] = 0.0f;
     if (age < 0 || age >= c->tcap || age >= c->tcount)
         return set_msg(c, GB_ERR_INVALID_ARG, "no timed collective %d calls back", age);
-    const cudaEvent_t *ev = c->tev + (size_t)((c->tcount - 1 - age) % c->tcap) * 4;
-    cudaError_t e = cudaEventSynchronize(ev[3]);
+    const long long slot = (c->tcount - 1 - age) % c->tcap;
+    const cudaEvent_t *ev = c->tev + (size_t)slot * kMarks;
+    const int nd = c->tnk2[slot];
+    cudaError_t e = cudaEventSynchronize(ev[5 + 2 * (nd - 1)]);
     if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventSynchronize", e);
-    for (int i = 0; i < GB_N_PHASES; ++i) {
-        e = cudaEventElapsedTime(&ms[i], ev[i], ev[i + 1]);
-        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventElapsedTime", e);
+    float t = 0.0f;
+    if ((e = cudaEventElapsedTime(&ms[0], ev[0], ev[1])) != cudaSuccess)
+        return fail(c, GB_ERR_CUDA, "cudaEventElapsedTime", e);
+    if (c->tbridge[slot] && (e = cudaEventElapsedTime(&ms[1], ev[2], ev[3])) != cudaSuccess)
+        return fail(c, GB_ERR_CUDA, "cudaEventElapsedTime", e);
+    for (int j = 0; j < nd; ++j) {
+        if ((e = cudaEventElapsedTime(&t, ev[4 + 2 * j], ev[5 + 2 * j])) != cudaSuccess)
+            return fail(c, GB_ERR_CUDA, "cudaEventElapsedTime", e);
+        ms[2] += t;
     }
     return GB_OK;
 }

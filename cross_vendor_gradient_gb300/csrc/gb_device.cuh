@@ -1,10 +1,10 @@
-// Device-side helpers of libgb: lane layouts, streaming vector memory access,
+// Device-side helpers of libgb: lane layout, streaming vector memory access,
 // and the bf16 / OCP fp8 conversions written as inline PTX.
 //
 // Everything on the hot path is HBM-streaming work (a handful of float32 adds
-// per 4-8 bytes moved), so the kernels are built around 128-bit coalesced
-// loads and stores, enough bytes in flight per SM, and warp-shuffle block
-// maxima; there is no dense contraction and no tensor-core work.
+// per 4-8 bytes moved), so the kernels are built around wide coalesced loads
+// and stores, enough bytes in flight per SM, and warp-shuffle block maxima;
+// there is no dense contraction and no tensor-core work.
 #pragma once
 
 #include <cstdint>
@@ -15,43 +15,49 @@
 
 namespace gb {
 
-constexpr int kTile = 256;        // elements per warp tile
+constexpr int kTile = 256;  // elements per warp tile
 constexpr int kWarp = 32;
-constexpr int kPerLane = kTile / kWarp;  // 8 elements per lane
 
-// ---------------------------------------------------------------- layouts
-// A warp tile is 256 consecutive elements.  float32 buffers: lane l owns the
-// two 16-byte vectors at elements 4l and 128 + 4l (two fully coalesced 512 B
-// warp accesses).  bf16 buffers: lane l owns the 16-byte vector at element 8l
-// (one coalesced 512 B warp access).  Element k (0..7) of a lane:
-template <typename T> struct Lay;
-template <> struct Lay<float> {
-    static constexpr int kVec = 4;  // elements per 16-byte vector
-    __device__ __forceinline__ static unsigned idx(int lane, int k) {
-        return (unsigned)((k >> 2) * 128 + lane * 4 + (k & 3));
-    }
-};
-template <> struct Lay<__nv_bfloat16> {
-    static constexpr int kVec = 8;
-    __device__ __forceinline__ static unsigned idx(int lane, int k) { return (unsigned)(lane * 8 + k); }
-};
+// ---------------------------------------------------------------- layout
+// A warp tile is 256 consecutive elements; lane l owns elements 8l .. 8l+7.
+// float32: one 32-byte access per lane (a 1 KiB contiguous warp access);
+// bf16: one 16-byte access per lane (512 B per warp); fp8 codes: 8 bytes.
+// With codec blocks of 128, lanes 0..15 form block 2t and lanes 16..31
+// block 2t+1; with blocks of 256 the whole warp is one block.
+__device__ __forceinline__ unsigned lane_elem(int lane, int k) { return (unsigned)(lane * 8 + k); }
 
 // ------------------------------------------------------- memory accesses
-// Rank buffers are read once per collective: stream them past L1 and mark
-// them evict-first in L2.  Payloads are re-read by the copy engines and the
-// decode kernel, so they are stored normally.
+// Rank buffers are read once per collective: bypass L1 and mark the lines
+// evict-first in L2.  Payloads are re-read soon (copy engines, the decode
+// kernel), so they are stored and loaded normally.
+struct U8x32 { uint32_t w[8]; };
+
+__device__ __forceinline__ U8x32 ld_stream_v8(const void *p) {
+    U8x32 r;
+    asm("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+          "=r"(r.w[6]), "=r"(r.w[7])
+        : "l"(p));
+    return r;
+}
+__device__ __forceinline__ U8x32 ld_v8(const void *p) {
+    U8x32 r;
+    asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+          "=r"(r.w[6]), "=r"(r.w[7])
+        : "l"(p));
+    return r;
+}
 __device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
     return r;
 }
 __device__ __forceinline__ uint4 ld_u4(const void *p) {
     uint4 r;
-    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p));
+    asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
     return r;
 }
 __device__ __forceinline__ uint2 ld_u2(const void *p) {
@@ -59,26 +65,27 @@ __device__ __forceinline__ uint2 ld_u2(const void *p) {
     asm("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
     return r;
 }
-__device__ __forceinline__ uint32_t ld_u1(const void *p) {
-    uint32_t r;
-    asm("ld.global.nc.u32 %0, [%1];" : "=r"(r) : "l"(p));
-    return r;
+__device__ __forceinline__ void st_v8(void *p, const uint32_t w[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream_v8(void *p, const uint32_t w[8]) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
 }
 __device__ __forceinline__ void st_u4(void *p, uint4 v) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
 }
 __device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
                  : "memory");
 }
 __device__ __forceinline__ void st_u2(void *p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
-}
-__device__ __forceinline__ void st_u1(void *p, uint32_t v) {
-    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // ------------------------------------------------------------ conversions
@@ -140,9 +147,6 @@ __device__ __forceinline__ int block_scale_exp(float m) {
 __device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
 
 // ---------------------------------------------------------- payload layout
-__host__ __device__ __forceinline__ size_t code_bytes(int codec) {
-    return codec == GB_CODEC_NONE ? 4 : codec == GB_CODEC_BF16 ? 2 : 1;
-}
 __host__ __device__ __forceinline__ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace gb

@@ -1,6 +1,7 @@
 // Kernel argument blocks and launchers of libgb (host-visible declarations).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -9,29 +10,30 @@
 
 namespace gb {
 
-// Fused island reduce + bridge encode over every island at once.
-// Island i's ranks are src[first[i] .. first[i+1]); its payload goes to
-// payload[i] (codes at offset 0, fp8 scales at scales_off).
+// Fused island reduce + bridge encode over every island at once (grid y =
+// island).  Island i's ranks are src[first[i] .. first[i+1]); its payload
+// goes to payload[i] (codes at offset 0, fp8 scales at scales_off).
 struct ReduceEncodeArgs {
     const void *src[GB_MAX_RANKS];
     void *payload[GB_MAX_ISLANDS];
     int first[GB_MAX_ISLANDS + 1];
     int n_islands;
     uint64_t n;
-    uint64_t tiles;       // warp tiles per island = ceil(n / 256)
+    uint32_t tiles;       // warp tiles per island = ceil(n / 256)
     uint64_t scales_off;  // byte offset of the fp8 scales in a payload
 };
 
-// Fused decode + accumulate + broadcast.
+// Fused decode + accumulate + broadcast (grid y = output unit).
 // Output group g (an island for all_reduce) reads the n_src payloads
 // payload[g][0..n_src) (island order), adds their decoded values in float32,
-// divides by `world` for AVG, rounds to the rank dtype and writes the result.
-//   all_reduce (rs == 0): work item (g, tile), written to every rank buffer
-//     dst[first[g] .. first[g+1]) at the same element index;
-//   reduce_scatter (rs == 1): work item (rank r, tile of its slice of m
-//     elements), global elements [r*m, (r+1)*m) written to dst[r]; group
-//     g = the island of r.  vec == 0 forces the element-wise path (used when
-//     m is not a multiple of 8, which would misalign 16-byte accesses).
+// divides by W for AVG (an exact multiply by 1/W when W is a power of two),
+// rounds to the rank dtype and writes the result.
+//   all_reduce (rs == 0): unit = group g; every rank buffer
+//     dst[first[g] .. first[g+1]) receives the same elements;
+//   reduce_scatter (rs == 1): unit = rank r; global elements
+//     [r*m, (r+1)*m) go to dst[r]; group g = the island of r.  vec == 0
+//     forces the element-wise path (used when m is not a multiple of 8,
+//     which would misalign the vector accesses).
 struct DecodeBcastArgs {
     void *dst[GB_MAX_RANKS];
     const void *payload[GB_MAX_ISLANDS][GB_MAX_ISLANDS];
@@ -40,13 +42,15 @@ struct DecodeBcastArgs {
     int n_groups;
     int n_src;
     int avg;
+    int world_pow2;  // W is a power of two
     float world;
-    uint64_t n;           // elements of the full buffer
+    float inv_world;
+    uint64_t n;      // elements of the full buffer
     uint64_t scales_off;
     int rs;
     int vec;
-    uint64_t m;           // reduce_scatter slice length
-    uint64_t tiles;       // all_reduce: tiles per group; reduce_scatter: tiles per slice
+    uint64_t m;      // reduce_scatter slice length
+    uint32_t tiles;  // all_reduce: tiles per group; reduce_scatter: tiles per slice
 };
 
 // accum = dec(payload) or accum + dec(payload).
@@ -72,7 +76,8 @@ struct CopyArgs {
     int vec;  // all addresses and `bytes` multiples of 16
 };
 
-// Launchers: return the cudaError_t of the launch.
+// Launchers: return the cudaError_t of the launch.  `units` is the grid's y
+// extent (islands, or ranks for reduce_scatter).
 cudaError_t launch_reduce_encode(const ReduceEncodeArgs &a, int dtype, int codec, int block,
                                  cudaStream_t s);
 cudaError_t launch_decode_bcast(const DecodeBcastArgs &a, int dtype, int codec, int block,
@@ -82,5 +87,27 @@ cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, 
 cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s);
 
 uint64_t launches();
+void count_launch();
+int sm_count();
+
+// One resident wave of 256-thread blocks spread over `units` grid rows (or
+// fewer when there is less work); the kernels walk their tiles with a grid
+// stride.  The occupancy is looked up once per kernel instantiation.
+template <auto Kern, typename Args>
+cudaError_t launch_grid(uint64_t tiles_per_unit, unsigned units, const Args &a, cudaStream_t s) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int v = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, Kern, 256, 0);
+        per_sm = v > 0 ? v : 1;
+    }
+    const uint64_t cap = (uint64_t)per_sm * (uint64_t)sm_count();
+    const uint64_t per_unit_cap = cap / units > 0 ? cap / units : 1;
+    const uint64_t want = (tiles_per_unit + 7) / 8;  // 8 warps (tiles) per block
+    const uint64_t gx = want < per_unit_cap ? want : per_unit_cap;
+    Kern<<<dim3((unsigned)(gx ? gx : 1), units), 256, 0, s>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
 
 }  // namespace gb

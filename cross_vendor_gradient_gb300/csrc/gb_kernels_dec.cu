@@ -1,0 +1,300 @@
+// Decode + accumulate + broadcast, decompress-accumulate, and exact copies
+// (sm_103a).
+//
+// What is computed (gpubridge README, "Bridge compression" and "all_reduce
+// uses reduce-bridge-broadcast"): each leader decodes every island's payload
+// (its own included) and adds them in float32 in island order; AVG divides
+// once by the world size (API table, all_reduce row); the total, rounded to
+// the rank dtype, goes to every rank of the island.
+//
+// How: one warp per 256-element tile per output group (grid y), 8 contiguous
+// elements per lane; the payloads of a tile are all loaded before the first
+// add (compile-time count for 1 or 2 islands); the result leaves as one
+// 32-byte (float32) or 16-byte (bf16) streaming store per lane per rank.
+#include <atomic>
+#include <cuda_runtime.h>
+
+#include "gb_device.cuh"
+#include "gb_kernels.cuh"
+
+namespace gb {
+
+using bf16 = __nv_bfloat16;
+
+static std::atomic<uint64_t> g_launches{0};
+uint64_t launches() { return g_launches.load(); }
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int sm_count() {
+    static int count = 0;
+    if (count == 0) {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        count = v > 0 ? v : 1;
+    }
+    return count;
+}
+
+// Decode this lane's 8 elements of a payload.  `gbase` is the index, in the
+// full buffer, of the tile's first element; in the element-wise path only
+// elements whose index within the output unit (lbase + offset) is below
+// `limit` are read, the others decode as 0.
+template <int CODEC, int BLOCK>
+__device__ __forceinline__ void decode_lane(const void *payload, uint64_t scales_off, uint64_t gbase,
+                                            uint64_t lbase, uint64_t limit, int lane, bool full, float d[8]) {
+    if (full) {
+        if constexpr (CODEC == GB_CODEC_NONE) {
+            const U8x32 x = ld_v8((const float *)payload + gbase + 8 * lane);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) d[k] = __uint_as_float(x.w[k]);
+        } else if constexpr (CODEC == GB_CODEC_BF16) {
+            const uint4 x = ld_u4((const unsigned short *)payload + gbase + 8 * lane);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                d[2 * i] = __uint_as_float(w[i] << 16);
+                d[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        } else {
+            const uint64_t j0 = gbase + 8 * lane;
+            const uint2 x = ld_u2((const unsigned char *)payload + j0);
+            const float s = __ldg((const float *)((const unsigned char *)payload + scales_off) + j0 / BLOCK);
+            float c[8];
+            fp8x2_to_f32<CODEC>(x.x & 0xFFFFu, c[0], c[1]);
+            fp8x2_to_f32<CODEC>(x.x >> 16, c[2], c[3]);
+            fp8x2_to_f32<CODEC>(x.y & 0xFFFFu, c[4], c[5]);
+            fp8x2_to_f32<CODEC>(x.y >> 16, c[6], c[7]);
+            // code value * 2^k is exact in float32: k >= -126 keeps every
+            // product on or above the subnormal grid
+#pragma unroll
+            for (int k = 0; k < 8; ++k) d[k] = __fmul_rn(c[k], s);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint64_t off = lane_elem(lane, k);
+            d[k] = 0.0f;
+            if (lbase + off < limit) {
+                const uint64_t j = gbase + off;
+                if constexpr (CODEC == GB_CODEC_NONE) {
+                    d[k] = __ldg((const float *)payload + j);
+                } else if constexpr (CODEC == GB_CODEC_BF16) {
+                    d[k] = bf16_bits_to_f32(__ldg((const unsigned short *)payload + j));
+                } else {
+                    const float *sc = (const float *)((const unsigned char *)payload + scales_off);
+                    float lo, hi;
+                    fp8x2_to_f32<CODEC>(__ldg((const unsigned char *)payload + j), lo, hi);
+                    d[k] = __fmul_rn(lo, __ldg(sc + j / BLOCK));
+                }
+            }
+        }
+    }
+}
+
+// Write this lane's 8 float32 results to a rank buffer of type T (bf16:
+// round to nearest even), streaming.
+template <typename T>
+__device__ __forceinline__ void store_rank(void *p, uint64_t lbase, int lane, uint64_t limit, bool full,
+                                           const float t[8]) {
+    if constexpr (sizeof(T) == 4) {
+        float *f = (float *)p;
+        if (full) {
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(t[k]);
+            st_stream_v8(f + lbase + 8 * lane, w);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint64_t j = lbase + lane_elem(lane, k);
+                if (j < limit) f[j] = t[k];
+            }
+        }
+    } else {
+        unsigned short *h = (unsigned short *)p;
+        if (full) {
+            st_stream_u4(h + lbase + 8 * lane, make_uint4(cvt_bf16x2(t[0], t[1]), cvt_bf16x2(t[2], t[3]),
+                                                          cvt_bf16x2(t[4], t[5]), cvt_bf16x2(t[6], t[7])));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint64_t j = lbase + lane_elem(lane, k);
+                if (j < limit) h[j] = (unsigned short)(cvt_bf16x2(t[k], 0.0f) & 0xFFFFu);
+            }
+        }
+    }
+}
+
+// NS > 0: exactly NS payloads (loads unrolled); NS == 0: a.n_src of them.
+template <typename T, int CODEC, int BLOCK, int NS>
+__global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ DecodeBcastArgs a) {
+    const int u = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    int g, r_lo, r_hi;
+    uint64_t gofs, limit;
+    if (a.rs) {
+        g = a.group_of_rank[u];
+        r_lo = u;
+        r_hi = u + 1;
+        gofs = (uint64_t)u * a.m;
+        limit = a.m;
+    } else {
+        g = u;
+        r_lo = a.first[g];
+        r_hi = a.first[g + 1];
+        gofs = 0;
+        limit = a.n;
+    }
+    const int nsrc = NS > 0 ? NS : a.n_src;
+    const uint32_t wpb = blockDim.x >> 5;
+    const uint32_t stride = gridDim.x * wpb;
+    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < a.tiles; tile += stride) {
+        const uint64_t lbase = (uint64_t)tile * kTile;
+        const uint64_t gbase = gofs + lbase;
+        const bool full = a.vec && lbase + kTile <= limit;
+        float t[8];
+        if constexpr (NS > 0) {
+            float d[NS][8];
+#pragma unroll
+            for (int q = 0; q < NS; ++q)
+                decode_lane<CODEC, BLOCK>(a.payload[g][q], a.scales_off, gbase, lbase, limit, lane, full, d[q]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = d[0][k];
+#pragma unroll
+            for (int q = 1; q < NS; ++q)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);  // island order
+        } else {
+            decode_lane<CODEC, BLOCK>(a.payload[g][0], a.scales_off, gbase, lbase, limit, lane, full, t);
+            for (int j0 = 1; j0 < nsrc; j0 += 2) {  // two payloads in flight at a time
+                float d[2][8];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (j0 + q < nsrc)
+                        decode_lane<CODEC, BLOCK>(a.payload[g][j0 + q], a.scales_off, gbase, lbase, limit, lane,
+                                                  full, d[q]);
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+                    if (j0 + q < nsrc) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);
+                    }
+            }
+        }
+        if (a.avg) {
+            // t / W; for W = 2^e the product with 2^-e is the same correctly
+            // rounded quotient (one rounding of the same real number)
+            if (a.world_pow2) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(t[k], a.inv_world);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fdiv_rn(t[k], a.world);
+            }
+        }
+        for (int r = r_lo; r < r_hi; ++r) store_rank<T>(a.dst[r], lbase, lane, limit, full, t);
+    }
+}
+
+template <int CODEC, int BLOCK>
+__global__ void __launch_bounds__(256) k_decompress_acc(const __grid_constant__ DecompressAccArgs a) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t wpb = blockDim.x >> 5;
+    const uint32_t tiles = (uint32_t)((a.n + kTile - 1) / kTile);
+    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * wpb) {
+        const uint64_t base = (uint64_t)tile * kTile;
+        const bool full = base + kTile <= a.n;
+        float d[8];
+        decode_lane<CODEC, BLOCK>(a.payload, a.scales_off, base, base, a.n, lane, full, d);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint64_t j = base + lane_elem(lane, k);
+            if (j < a.n) a.accum[j] = a.accumulate ? __fadd_rn(a.accum[j], d[k]) : d[k];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a) {
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+    if (a.vec) {
+        const uint64_t chunks = a.bytes / 16;
+        const uint64_t total = chunks * (uint64_t)a.n_jobs;
+        for (uint64_t c = tid; c < total; c += nth) {
+            const int j = (int)(c / chunks);
+            const uint64_t off = (c - (uint64_t)j * chunks) * 16;
+            const unsigned char *s = a.src[j] + off;
+            const uint4 x = ld_stream_u4(s);
+            for (int d = a.dst_lo[j]; d < a.dst_hi[j]; ++d) {
+                unsigned char *p = a.dst[d] + a.dst_off[j] + off;
+                if (p != s) st_stream_u4(p, x);
+            }
+        }
+    } else {
+        const uint64_t total = a.bytes * (uint64_t)a.n_jobs;
+        for (uint64_t c = tid; c < total; c += nth) {
+            const int j = (int)(c / a.bytes);
+            const uint64_t off = c - (uint64_t)j * a.bytes;
+            const unsigned char *s = a.src[j] + off;
+            const unsigned char x = *s;
+            for (int d = a.dst_lo[j]; d < a.dst_hi[j]; ++d) {
+                unsigned char *p = a.dst[d] + a.dst_off[j] + off;
+                if (p != s) *p = x;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+template <typename T, int CODEC, int BLOCK>
+static cudaError_t dispatch_ns(const DecodeBcastArgs &a, cudaStream_t s) {
+    const unsigned units = a.rs ? (unsigned)a.first[a.n_groups] : (unsigned)a.n_groups;
+    switch (a.n_src) {
+    case 1: return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 1>>(a.tiles, units, a, s);
+    case 2: return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 2>>(a.tiles, units, a, s);
+    default: return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 0>>(a.tiles, units, a, s);
+    }
+}
+
+template <typename T>
+static cudaError_t dispatch_codec(const DecodeBcastArgs &a, int codec, int block, cudaStream_t s) {
+    switch (codec) {
+    case GB_CODEC_NONE: return dispatch_ns<T, GB_CODEC_NONE, 256>(a, s);
+    case GB_CODEC_BF16: return dispatch_ns<T, GB_CODEC_BF16, 256>(a, s);
+    case GB_CODEC_E4M3:
+        return block == 128 ? dispatch_ns<T, GB_CODEC_E4M3, 128>(a, s) : dispatch_ns<T, GB_CODEC_E4M3, 256>(a, s);
+    case GB_CODEC_E5M2:
+        return block == 128 ? dispatch_ns<T, GB_CODEC_E5M2, 128>(a, s) : dispatch_ns<T, GB_CODEC_E5M2, 256>(a, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_decode_bcast(const DecodeBcastArgs &a, int dtype, int codec, int block, cudaStream_t s) {
+    return dtype == GB_F32 ? dispatch_codec<float>(a, codec, block, s) : dispatch_codec<bf16>(a, codec, block, s);
+}
+
+cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, int block, cudaStream_t s) {
+    const uint64_t tiles = (a.n + kTile - 1) / kTile;
+    switch (codec) {
+    case GB_CODEC_NONE: return launch_grid<k_decompress_acc<GB_CODEC_NONE, 256>>(tiles, 1, a, s);
+    case GB_CODEC_BF16: return launch_grid<k_decompress_acc<GB_CODEC_BF16, 256>>(tiles, 1, a, s);
+    case GB_CODEC_E4M3:
+        return block == 128 ? launch_grid<k_decompress_acc<GB_CODEC_E4M3, 128>>(tiles, 1, a, s)
+                            : launch_grid<k_decompress_acc<GB_CODEC_E4M3, 256>>(tiles, 1, a, s);
+    case GB_CODEC_E5M2:
+        return block == 128 ? launch_grid<k_decompress_acc<GB_CODEC_E5M2, 128>>(tiles, 1, a, s)
+                            : launch_grid<k_decompress_acc<GB_CODEC_E5M2, 256>>(tiles, 1, a, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s) {
+    const uint64_t units = a.vec ? a.bytes / 16 : a.bytes;
+    const uint64_t threads = units * (uint64_t)a.n_jobs;
+    // launch_grid counts 8 warps of 32 threads per block: pass threads / 32 as "tiles"
+    return launch_grid<k_copy>((threads + 31) / 32, 1, a, s);
+}
+
+}  // namespace gb

@@ -111,7 +111,7 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
     for (int i = 0; i <= I; ++i) ra.first[i] = first[i];
     ra.n_islands = I;
     ra.n = n;
-    ra.tiles = (n + gb::kTile - 1) / gb::kTile;
+    ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
     ra.scales_off = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? gb::round_up(n, 16) : P;
     if (gb::launch_reduce_encode(ra, dtype, eff, blk, s) != cudaSuccess) return GB_ERR_CUDA;
 
@@ -149,6 +149,8 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
     da.n_src = I;
     da.avg = op == GB_AVG;
     da.world = (float)W;
+    da.world_pow2 = (W & (W - 1)) == 0;
+    da.inv_world = 1.0f / (float)W;
     da.n = n;
     da.scales_off = ra.scales_off;
     da.rs = 0;

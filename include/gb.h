@@ -124,9 +124,28 @@ int gb_island_first_rank(const gb_ctx *ctx, int island); /* = the island's leade
 int gb_island_of_rank(const gb_ctx *ctx, int rank);
 
 /* Grow the context's staging so that collectives on up to n elements of
- * `dtype` with `codec` / `block` need no further allocation (for example
- * before capturing calls in a CUDA graph).  Enqueues nothing. */
+ * `dtype` with `codec` / `block` need no further allocation.  Enqueues
+ * nothing. */
 gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int block);
+
+/* Collective policy of gb_all_reduce and gb_all_reduce_host when there are
+ * two or more islands (gpubridge README, policy table):
+ *   chunk_bytes == 0: reduce-bridge-broadcast, one bridge hop for the whole
+ *     buffer on the caller's stream;
+ *   chunk_bytes > 0 (default 4 MiB, the README's default chunk): pipelined-
+ *     reduce-bridge-broadcast.  The leaders' bridge step is cut into chunks
+ *     of about chunk_bytes of one island's payload (whole 256-element tiles,
+ *     at least one tile, at most 32 chunks per call); chunk c's device ->
+ *     host copy, chunk c-1's host -> device copy and the kernels of other
+ *     chunks overlap on the context's two copy streams, ordered with CUDA
+ *     events.  Chunks are whole codec blocks, so the result is the same
+ *     bits.
+ *   use_graphs != 0 (default): a pipelined call is captured into a CUDA
+ *     graph the second time the same buffers and shape are seen, and
+ *     replayed from then on (one launch instead of a few dozen).
+ * reduce_scatter, all_gather and broadcast always take one hop.  Waits for
+ * the context's outstanding work. */
+gb_status gb_set_pipeline(gb_ctx *ctx, size_t chunk_bytes, int use_graphs);
 
 /* The context's sticky status (GB_OK until a call fails after enqueueing)
  * and a one-line description of the last error on this context. */
@@ -243,11 +262,18 @@ gb_status gb_all_reduce_buckets(gb_ctx *ctx, int n_buckets, void *const *bucket_
 
 /* gpubridge README, "Observing collectives": timing marks per phase, taken
  * with CUDA events on GPUs, never synchronising the call.  With capacity > 0
- * every collective records four events on its stream (start, after island
- * reduce + compress, after the bridge hop, after decompress + broadcast) and
- * the marks of the last `capacity` collectives are kept; 0 turns the marks
- * off.  Changing the capacity waits for the context's outstanding work. */
-#define GB_N_PHASES 3 /* 0: island reduce + compress, 1: bridge hop, 2: decompress + broadcast */
+ * every collective records CUDA events around its phases and the marks of
+ * the last `capacity` collectives are kept; 0 turns the marks off.  Changing
+ * the capacity waits for the context's outstanding work.  Phases:
+ *   0: the island reduce + compress kernels (their launches run back to
+ *      back on the caller's stream; the window covers all of them),
+ *   1: the bridge hop, from the first device -> host copy's start to the
+ *      last host -> device copy's end (0 without a bridge),
+ *   2: the decompress + broadcast kernels (all_reduce / reduce_scatter) or
+ *      the copy kernels (all_gather / broadcast), the sum of their own
+ *      durations.
+ * With the pipelined policy the phases overlap in time. */
+#define GB_N_PHASES 3
 gb_status gb_set_phase_timing(gb_ctx *ctx, int capacity);
 
 /* Milliseconds of each phase of the collective `age` calls back (0 = the

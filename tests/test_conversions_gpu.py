@@ -66,10 +66,11 @@ def test_fp8_conversion_every_pattern(fmt, pool):
             cnt = pats.size
             nblk = -(-cnt // per_block)
             s = np.zeros(nblk * B, np.float32)
-            grid = s.reshape(nblk, B)
+            grid = s.reshape(nblk, B)  # a view of s
             grid[:, 0] = M  # pins the scale to 2^0
-            body = grid[:, 1:].reshape(-1)
+            body = np.zeros(nblk * per_block, np.float32)
             body[:cnt] = pats.view(np.float32)
+            grid[:, 1:] = body.reshape(nblk, per_block)
             sd = to_dev(s)
             n = s.size
             p = torch.empty(payload_bytes(fmt, B, n), dtype=torch.uint8, device="cuda")

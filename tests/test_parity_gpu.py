@@ -264,3 +264,64 @@ def test_empty_inputs_are_noops():
         st = B.gb_reduce_scatter(ctx.handle, [b.data_ptr() for b in bufs], [b.data_ptr() for b in bufs],
                                  0, 0, 0, 0, 256, 0)
         assert st == B.GB_OK
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (4, 4), (2, 1, 3), (1, 1, 1, 1, 1, 1, 1, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pipelined_all_reduce_matches_oracle(codec, block, sizes, dtype):
+    """The pipelined policy (chunked bridge on copy streams, replayed as a
+    CUDA graph) gives the oracle's bits: three calls on the same buffers
+    (direct, captured, replayed), several chunk sizes, ragged tails, and a
+    size that needs more than the 32-chunk cap."""
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        for chunk_bytes, n in ((1024, 5000), (4096, 256 * 37 + 5), (65536, 300_007), (1024, 40_000), (300, 70_001)):
+            ctx.set_pipeline(chunk_bytes, True)
+            xs = inputs(sizes, n, dtype, cid=n % 89)
+            want = orc.all_reduce(xs, sizes, "avg", codec, block)
+            bufs = [to_dev(x) for x in xs]
+            src = [to_dev(x) for x in xs]
+            for call in range(3):
+                for b, s_ in zip(bufs, src):
+                    b.copy_(s_)
+                ctx.all_reduce(bufs, "avg", codec, block)
+                torch.cuda.synchronize()
+                for r in range(W):
+                    assert_bits_equal(to_host(bufs[r]), want[r], "pipelined chunk=%d n=%d call %d rank %d" % (
+                        chunk_bytes, n, call, r))
+        ctx.set_pipeline(0, False)
+        xs = inputs(sizes, 9999, dtype, cid=3)
+        bufs = [to_dev(x) for x in xs]
+        ctx.all_reduce(bufs, "sum", codec, block)
+        want = orc.all_reduce(xs, sizes, "sum", codec, block)
+        torch.cuda.synchronize()
+        for r in range(W):
+            assert_bits_equal(to_host(bufs[r]), want[r], "plain policy rank %d" % r)
+
+
+def test_pipelined_graph_replay_timing_and_streams():
+    """Phase marks are recorded for direct, captured and replayed calls, and
+    a replay on another stream is ordered after the previous call."""
+    sizes = (2, 2)
+    n = 1 << 21
+    xs = inputs(sizes, n, "f32", cid=91)
+    want = orc.all_reduce(xs, sizes, "sum", "e4m3", 256)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(1 << 20, True)
+        ctx.set_phase_timing(8)
+        bufs = [to_dev(x) for x in xs]
+        src = [to_dev(x) for x in xs]
+        s2 = torch.cuda.Stream()
+        for call in range(4):
+            stream = s2 if call % 2 else torch.cuda.current_stream()
+            with torch.cuda.stream(stream):
+                for b, s_ in zip(bufs, src):
+                    b.copy_(s_)
+                ctx.all_reduce(bufs, "sum", "e4m3", 256)
+            stream.synchronize()
+            ms = ctx.last_phase_times()
+            assert ms[0] > 0 and ms[1] > 0 and ms[2] > 0, (call, ms)
+            for r in range(4):
+                assert_bits_equal(to_host(bufs[r]), want[r], "call %d rank %d" % (call, r))
+        assert len([ctx.phase_times(a) for a in range(4)]) == 4

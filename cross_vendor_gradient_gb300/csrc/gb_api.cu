@@ -64,7 +64,7 @@ struct gb_ctx {
     bool done_recorded = false;
     cudaStream_t last_stream = nullptr;
     // pipelined-reduce-bridge-broadcast: chunk size, copy streams, events
-    size_t chunk_bytes = 4u << 20;
+    size_t chunk_bytes = 2u << 20;
     int use_graphs = 1;
     cudaStream_t sd = nullptr, sh = nullptr, scap = nullptr;
     cudaEvent_t ev_k1[kMaxChunks] = {}, ev_d2h[kMaxChunks] = {}, ev_h2d[kMaxChunks] = {};

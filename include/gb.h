@@ -132,7 +132,8 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  * two or more islands (gpubridge README, policy table):
  *   chunk_bytes == 0: reduce-bridge-broadcast, one bridge hop for the whole
  *     buffer on the caller's stream;
- *   chunk_bytes > 0 (default 4 MiB, the README's default chunk): pipelined-
+ *   chunk_bytes > 0 (default 2 MiB, measured best on GB300 for 25 MiB
+ *     buckets; the README's policy defaults to 4M): pipelined-
  *     reduce-bridge-broadcast.  The leaders' bridge step is cut into chunks
  *     of about chunk_bytes of one island's payload (whole 256-element tiles,
  *     at least one tile, at most 32 chunks per call); chunk c's device ->

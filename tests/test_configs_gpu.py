@@ -1,0 +1,185 @@
+"""Parity at the full sizes of the five workloads, in the launch
+configuration the benchmark uses (default pipelined policy, repeated calls
+replayed as a CUDA graph).
+
+Small workloads are compared with the oracle element by element.  Large ones
+are compared on sampled 256-element tiles: codec blocks (128 / 256) never
+cross a tile and sums are elementwise, so the oracle run on the sampled
+tiles alone computes exactly those elements' bits.  Properties that hold at
+any size are checked on the whole buffers on the device: every rank holds
+the same bits, and reduce_scatter followed by all_gather equals all_reduce.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from cross_vendor_gradient_gb300 import Context, bucket_plan
+from cross_vendor_gradient_gb300 import workloads as wl
+from tests.gpu_util import assert_bits_equal, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+TILE = 256
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def sample_tiles(n, k, seed):
+    nt = -(-n // TILE)
+    rng = np.random.default_rng(seed)
+    picks = set(rng.choice(nt, size=min(k, nt), replace=False).tolist()) | {0, nt - 1}
+    return sorted(picks)
+
+
+def gather_tiles(t, tiles, n):
+    """Host copy (numpy, rank dtype) of the given tiles of a device buffer."""
+    parts = [t[i * TILE:min((i + 1) * TILE, n)] for i in tiles]
+    return to_host(torch.cat(parts))
+
+
+def check_sampled(inputs_dev, outputs_dev, sizes, op, codec, block, n, k, seed, what):
+    tiles = sample_tiles(n, k, seed)
+    xs = [gather_tiles(x, tiles, n) for x in inputs_dev]
+    want = orc.all_reduce(xs, sizes, op, codec, block)
+    for r, o in enumerate(outputs_dev):
+        assert_bits_equal(gather_tiles(o, tiles, n), want[r], "%s rank %d" % (what, r))
+
+
+def ranks_identical(bufs):
+    for b in bufs[1:]:
+        assert torch.equal(b.view(torch.int16) if b.dtype == torch.bfloat16 else b.view(torch.int32),
+                           bufs[0].view(torch.int16) if b.dtype == torch.bfloat16 else bufs[0].view(torch.int32))
+
+
+@pytest.mark.parametrize("codec", ["none", "bf16"])
+def test_c1_two_ranks_full(codec):
+    w = wl.WORKLOADS["c1"]
+    xs = wl.host_rank_inputs(w)
+    want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+    with Context(w.island_sizes) as ctx:
+        bufs = [to_dev(x) for x in xs]
+        src = [to_dev(x) for x in xs]
+        for call in range(3):
+            for b, s in zip(bufs, src):
+                b.copy_(s)
+            ctx.all_reduce(bufs, w.op, codec, w.block)
+            torch.cuda.synchronize()
+            for r in range(w.world_size):
+                assert_bits_equal(to_host(bufs[r]), want[r], "c1 %s call %d rank %d" % (codec, call, r))
+
+
+def test_c2_bucket_full():
+    w = wl.WORKLOADS["c2"]
+    xs = wl.host_rank_inputs(w)
+    codec = w.codecs[0]
+    want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+    with Context(w.island_sizes) as ctx:
+        bufs = [to_dev(x) for x in xs]
+        src = [to_dev(x) for x in xs]
+        for call in range(3):  # direct, captured, replayed
+            for b, s in zip(bufs, src):
+                b.copy_(s)
+            ctx.all_reduce(bufs, w.op, codec, w.block)
+            torch.cuda.synchronize()
+            for r in range(w.world_size):
+                assert_bits_equal(to_host(bufs[r]), want[r], "c2 call %d rank %d" % (call, r))
+        # the same bits through the host-buffer entry point
+        host = [torch.from_numpy(x.copy()).pin_memory() for x in xs]
+        ctx.all_reduce_host(host, w.op, codec, w.block)
+        torch.cuda.synchronize()
+        for r in range(w.world_size):
+            assert_bits_equal(host[r].numpy(), want[r], "c2 host rank %d" % r)
+
+
+@pytest.mark.parametrize("codec", ["none", "bf16", "e4m3"])
+def test_c3_payload_sweep(codec):
+    w = wl.WORKLOADS["c3"]
+    with Context(w.island_sizes) as ctx:
+        for lg in wl.SWEEP_LOG2:
+            n = 1 << lg
+            if lg <= 20:
+                xs = wl.host_rank_inputs(w, n=n)
+                want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+                bufs = [to_dev(x) for x in xs]
+                ctx.all_reduce(bufs, w.op, codec, w.block)
+                torch.cuda.synchronize()
+                for r in range(w.world_size):
+                    assert_bits_equal(to_host(bufs[r]), want[r], "c3 %s n=2^%d rank %d" % (codec, lg, r))
+            else:
+                ins = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), "cuda", torch.float32)
+                       for r in range(w.world_size)]
+                bufs = [x.clone() for x in ins]
+                for _ in range(2):  # direct, then captured
+                    for b, x in zip(bufs, ins):
+                        b.copy_(x)
+                    ctx.all_reduce(bufs, w.op, codec, w.block)
+                torch.cuda.synchronize()
+                ranks_identical(bufs)
+                check_sampled(ins, bufs, w.island_sizes, w.op, codec, w.block, n, 48, lg, "c3 %s n=2^%d" % (codec, lg))
+                del ins, bufs
+
+
+def _bucketed(w, pad):
+    numels = [wl.numel(s) for s in w.tensors]
+    bo, off, bn = bucket_plan(numels, w.elem_bytes, wl.BUCKET_CAP_BYTES, pad)
+    return [int(v) for v in bn]
+
+
+def test_c4_gpt2_small_buckets():
+    w = wl.WORKLOADS["c4"]
+    bn = _bucketed(w, 1)
+    assert len(bn) == 9 and sum(bn) == 124_439_808
+    codec = w.codecs[0]
+    with Context(w.island_sizes) as ctx:
+        ins, bufs = [], []
+        for b, nb in enumerate(bn):
+            row = [wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 100 * b, "cuda", torch.bfloat16)
+                   for r in range(w.world_size)]
+            ins.append(row)
+            bufs.append([x.clone() for x in row])
+        ctx.all_reduce_buckets(bufs, w.op, codec, w.block)
+        torch.cuda.synchronize()
+        for b, nb in enumerate(bn):
+            ranks_identical(bufs[b])
+            check_sampled(ins[b], bufs[b], w.island_sizes, w.op, codec, w.block, nb, 24, b, "c4 bucket %d" % b)
+        # the smallest bucket in full
+        b = int(np.argmin(bn))
+        xs = [to_host(x) for x in ins[b]]
+        want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
+        for r in range(w.world_size):
+            assert_bits_equal(to_host(bufs[b][r]), want[r], "c4 bucket %d full rank %d" % (b, r))
+
+
+def test_c5_llama_buckets_and_rs_ag():
+    w = wl.WORKLOADS["c5"]
+    W = w.world_size
+    bn = _bucketed(w, 8 * W)  # slices of whole 8-element vectors for reduce_scatter
+    assert len(bn) == 90
+    codec = w.codecs[0]
+    with Context(w.island_sizes) as ctx:
+        ins, bufs = [], []
+        for b, nb in enumerate(bn):
+            row = [wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 1000 * b, "cuda", torch.bfloat16)
+                   for r in range(W)]
+            ins.append(row)
+            bufs.append([x.clone() for x in row])
+        ctx.all_reduce_buckets(bufs, w.op, codec, w.block)
+        torch.cuda.synchronize()
+        for b in range(0, len(bn), 7):
+            check_sampled(ins[b], bufs[b], w.island_sizes, w.op, codec, w.block, bn[b], 8, b, "c5 bucket %d" % b)
+        # reduce_scatter then all_gather over the same inputs equals the all_reduce, everywhere
+        for b, nb in enumerate(bn):
+            ranks_identical(bufs[b])
+            rs = [torch.empty(nb // W, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+            ag = [torch.empty(nb, dtype=torch.bfloat16, device="cuda") for _ in range(W)]
+            ctx.reduce_scatter(ins[b], rs, w.op, codec, w.block)
+            ctx.all_gather(rs, ag)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert torch.equal(ag[r].view(torch.int16), bufs[b][0].view(torch.int16)), (b, r)
+            del rs, ag

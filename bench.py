@@ -50,6 +50,8 @@ def parse():
                    help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
     p.add_argument("--no-graphs", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--roofline-only", action="store_true",
+                   help="only the per-kernel timed region (one bridge hop per call); for profiling")
     p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
     return p.parse_args()
 
@@ -245,32 +247,34 @@ def run_gb(args, world, rank, local, pg):
 
     # ---- timed region 1: the step as a user runs it (pipelined policy, graph
     # replay, no phase marks: a CUDA event between kernels drains the stream)
-    ctx.set_pipeline(chunk_bytes, not args.no_graphs)
-    with torch.cuda.stream(stream):
-        for i in range(Wm):
-            step(i, False)
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local)
-    clocks.start()
-    barrier(pg)
-    torch.cuda.synchronize()
-    l0 = kernel_launch_count()
-    t_wall = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            step(i, True)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    barrier(pg)
-    launches = kernel_launch_count() - l0
-    clk = clocks.stop()
-    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
-    ms = max_over_ranks(pg, float(np.mean(step_ms)), dev if pg is not None else None)
+    launches, clk, t_wall, ms = 0, None, 0.0, None
+    if not args.roofline_only:
+        ctx.set_pipeline(chunk_bytes, not args.no_graphs)
+        with torch.cuda.stream(stream):
+            for i in range(Wm):
+                step(i, False)
+        torch.cuda.synchronize()
+        clocks = ClockSampler(local)
+        clocks.start()
+        barrier(pg)
+        torch.cuda.synchronize()
+        l0 = kernel_launch_count()
+        t_wall = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                step(i, True)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+        barrier(pg)
+        launches = kernel_launch_count() - l0
+        clk = clocks.stop()
+        step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+        ms = max_over_ranks(pg, float(np.mean(step_ms)), dev if pg is not None else None)
 
     # ---- timed region 2: per-kernel durations for the roofline.  One full
     # launch of each kernel per step (one bridge hop per call), CUDA events
     # around every phase on the launching stream.
-    Kr = min(K, 500)
+    Kr = args.steps if args.roofline_only else min(K, 500)
     ctx.set_pipeline(0, False)
     ctx.set_phase_timing(Kr)
     with torch.cuda.stream(stream):
@@ -281,6 +285,8 @@ def run_gb(args, world, rank, local, pg):
             step(i, True)
     torch.cuda.synchronize()
     plain_ms = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Kr)]))
+    if ms is None:
+        ms = plain_ms
     phases = np.array([ctx.phase_times(Kr - 1 - i) for i in range(Kr)])  # oldest first
     ctx.set_phase_timing(0)
     ctx.set_pipeline(chunk_bytes, not args.no_graphs)
@@ -295,20 +301,22 @@ def run_gb(args, world, rank, local, pg):
     link_peak = min(link["d2h_gbs"], link["h2d_gbs"])
 
     # end to end through the host-buffer entry point (pinned host buffers)
-    host = [torch.from_numpy(x.copy()).pin_memory() if x.dtype == np.float32 else
-            torch.from_numpy(x.view(np.int16).copy()).pin_memory().view(torch.bfloat16) for x in xs]
-    Ke = max(10, min(200, K // 10))
-    e_ms = []
-    with torch.cuda.stream(stream):
-        for i in range(3 + Ke):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            ctx.all_reduce_host(host, w.op, codec, w.block, stream=stream)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= 3:
-                e_ms.append(e0.elapsed_time(e1))
-    e2e_ms = max_over_ranks(pg, float(np.mean(e_ms)), dev if pg is not None else None)
+    e2e_ms, Ke = float("nan"), 0
+    if not args.roofline_only:
+        host = [torch.from_numpy(x.copy()).pin_memory() if x.dtype == np.float32 else
+                torch.from_numpy(x.view(np.int16).copy()).pin_memory().view(torch.bfloat16) for x in xs]
+        Ke = max(10, min(200, K // 10))
+        e_ms = []
+        with torch.cuda.stream(stream):
+            for i in range(3 + Ke):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                ctx.all_reduce_host(host, w.op, codec, w.block, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 3:
+                    e_ms.append(e0.elapsed_time(e1))
+        e2e_ms = max_over_ranks(pg, float(np.mean(e_ms)), dev if pg is not None else None)
     ctx.close()
 
     value = world * n * b / (ms * 1e-3) / 1e9

@@ -389,6 +389,80 @@ def traffic_from_profiles(kernel):
     return None
 
 
+def run_sweep(args, local):
+    """Payload sweep (workload c3): 4 KiB .. 256 MiB of float32 per rank at
+    2 islands x 2 ranks, codecs none / bf16 / e4m3; one JSON line per row.
+    Per row: the step as run by default (pipelined graph, no marks) for the
+    algorithm GB/s, then one-hop steps with phase marks for the kernels' HBM
+    roofline fractions and the bridge's fraction of pinned copy bandwidth.
+    L2 is flushed (write then clean read) before every timed step."""
+    import torch
+    from cross_vendor_gradient_gb300 import Context, payload_bytes
+    from cross_vendor_gradient_gb300 import workloads as wl
+    from cross_vendor_gradient_gb300 import build as gbuild
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS["c3"]
+    W, I = w.world_size, len(w.island_sizes)
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    codecs = [args.codec] if args.codec else list(w.codecs)
+    for lg in wl.SWEEP_LOG2:
+        n = 1 << lg
+        pristine = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), dev, torch.float32) for r in range(W)]
+        bufs = [p.clone() for p in pristine]
+        K = max(5, min(args.steps, int(4e9 // (n * 4 * W))))
+        for codec in codecs:
+            ctx = Context(w.island_sizes)
+            ctx.reserve(n, torch.float32, codec, w.block)
+            ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+            ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+            def steps(count, timed):
+                with torch.cuda.stream(stream):
+                    for i in range(count):
+                        for r in range(W):
+                            bufs[r].copy_(pristine[r], non_blocking=True)
+                        flush.zero_()
+                        clean.amax()
+                        if timed:
+                            ev0[i].record(stream)
+                        ctx.all_reduce(bufs, w.op, codec, w.block, stream=stream)
+                        if timed:
+                            ev1[i].record(stream)
+                torch.cuda.synchronize()
+                return float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(count)])) if timed else 0.0
+
+            chunk = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
+            ctx.set_pipeline(chunk, True)
+            steps(max(3, args.warmup), False)
+            ms = steps(K, True)
+            ctx.set_pipeline(0, False)
+            ctx.set_phase_timing(K)
+            steps(3, False)
+            plain = steps(K, True)
+            ph = np.array([ctx.phase_times(a) for a in range(K)])
+            ctx.close()
+            k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
+            P = payload_bytes(codec, w.block, n)
+            b1, b2 = alg_bytes(W, I, n, 4, P)
+            print(json.dumps({
+                "metric": METRIC, "sweep_row": True, "workload": "c3", "codec": codec, "n": n,
+                "bytes_per_rank": 4 * n, "value": 4 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+                "steps": K, "one_hop_ms_per_step": plain,
+                "hbm_frac": {"k_reduce_encode": b1 / (k1 * 1e-3) / 1e9 / peak,
+                             "k_decode_bcast": b2 / (k2 * 1e-3) / 1e9 / peak, "peak_gbs": peak,
+                             "peak_kind": peak_kind},
+                "kernels_ms": {"k_reduce_encode": k1, "bridge_hop": br, "k_decode_bcast": k2},
+                "bridge_gbs": (I * P + I * (I - 1) * P) / (br * 1e-3) / 1e9 if br > 0 else None,
+            }), flush=True)
+        del pristine, bufs
+
+
 def run_reference(args, world, rank, pg):
     """The oracle, as it stands, on the host cores: each step is one oracle
     all_reduce of a bounded sample (a prefix of every rank buffer) of the
@@ -440,6 +514,12 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank, pg)), flush=True)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args, local)
         if pg is not None:
             pg.destroy_process_group()
         return

@@ -73,6 +73,11 @@ def lib():
         L.orc_bucket_plan.restype = ctypes.c_int
         L.orc_bucket_plan.argtypes = [vp, ctypes.c_int, c_size, c_size, c_size, vp, vp, vp,
                                       ctypes.c_int]
+        L.orc_encode_ef.restype = None
+        L.orc_encode_ef.argtypes = [vp, c_size, ctypes.c_int, ctypes.c_int, vp, vp, vp]
+        L.orc_all_reduce_ef.restype = ctypes.c_int
+        L.orc_all_reduce_ef.argtypes = [ctypes.c_int, vp, vp, vp, c_size, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, vp]
         L.orc_fp8_encode_f32_array.restype = None
         L.orc_fp8_encode_f32_array.argtypes = [vp, c_size, ctypes.c_int, vp]
         L.orc_f32_to_bf16_array.restype = None
@@ -303,3 +308,38 @@ def bucket_plan(numels, elem_bytes: int, cap_bytes: int = 25 * 1024 * 1024, pad_
     if nb < 0:
         raise RuntimeError("bucket plan overflow")
     return bucket_of[:T], offset[:T], bucket_numel[:nb]
+
+
+# ------------------------------------------------------------ error feedback
+
+def encode_ef(s: np.ndarray, residual: np.ndarray, codec, block: int = 256):
+    """Encode s + residual; `residual` (float32, updated in place) becomes
+    (s + residual) - dec(codes).  Returns (codes, scales)."""
+    s = np.ascontiguousarray(s, dtype=np.float32)
+    assert residual.dtype == np.float32 and residual.flags.c_contiguous and residual.size == s.size
+    c = _codec_id(codec)
+    n = s.size
+    codes = np.empty(n, code_dtype(c))
+    nb = n_blocks(n, block) if c in (CODEC_E4M3, CODEC_E5M2) else 0
+    scales = np.empty(max(nb, 1), np.float32)
+    lib().orc_encode_ef(_ptr(s), n, c, block, _ptr(residual), _ptr(codes), _ptr(scales))
+    return codes, scales[:nb]
+
+
+def all_reduce_ef(ranks, island_sizes, residuals, op="sum", codec="none", block: int = 256):
+    """all_reduce with one error-feedback residual per island (float32 arrays
+    of n, updated in place).  Returns the outputs of every rank."""
+    ranks = [np.ascontiguousarray(r) for r in ranks]
+    sizes = np.asarray(island_sizes, dtype=np.int32)
+    assert len(residuals) == len(sizes)
+    for r in residuals:
+        assert r.dtype == np.float32 and r.flags.c_contiguous and r.size == ranks[0].size
+    outs = [np.empty_like(r) for r in ranks]
+    pi, _k1 = _ptr_array(ranks)
+    po, _k2 = _ptr_array(outs)
+    pr, _k3 = _ptr_array(residuals)
+    rc = lib().orc_all_reduce_ef(len(sizes), _ptr(sizes), pi, po, ranks[0].size, _dtype_id(ranks[0]),
+                                 _op_id(op), _codec_id(codec), block, pr)
+    if rc:
+        raise RuntimeError("oracle all_reduce_ef failed (%d)" % rc)
+    return outs

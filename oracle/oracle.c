@@ -474,3 +474,70 @@ void orc_f32_to_bf16_array(const float *x, size_t n, uint16_t *out)
     for (size_t j = 0; j < n; ++j)
         out[j] = orc_f32_to_bf16(x[j]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Error feedback (gpubridge README, "Bridge compression": each bridge      */
+/* member keeps an error-feedback residual per buffer, so rounding error    */
+/* carries into the next step instead of accumulating).                      */
+/* Reading: the leader encodes s' = s + r (float32) and keeps                */
+/* r <- s' - dec(enc(s')) (float32) for the next call on the same buffer.    */
+/* ------------------------------------------------------------------------ */
+
+void orc_encode_ef(const float *s, size_t n, int codec, int block, float *residual, void *codes,
+                   float *scales)
+{
+    float *sp = calloc(n ? n : 1, sizeof(float));
+    float *dec = calloc(n ? n : 1, sizeof(float));
+    if (!sp || !dec) {
+        free(sp);
+        free(dec);
+        return;
+    }
+    for (size_t j = 0; j < n; ++j)
+        sp[j] = s[j] + residual[j];
+    orc_encode(sp, n, codec, block, codes, scales);
+    orc_decode(codes, scales, n, codec, block, dec);
+    for (size_t j = 0; j < n; ++j)
+        residual[j] = sp[j] - dec[j];
+    free(sp);
+    free(dec);
+}
+
+/* all_reduce with error feedback: residuals[i] (n floats, in/out) belongs to
+ * island i's leader.  With one island there is no bridge and the residuals
+ * are left as they are. */
+int orc_all_reduce_ef(int I, const int *island_sizes, const void *const *in, void *const *out, size_t n,
+                      int dtype, int op, int codec, int block, float *const *residuals)
+{
+    int W = 0;
+    for (int i = 0; i < I; ++i)
+        W += island_sizes[i];
+    if (I == 1)
+        return orc_all_reduce(I, island_sizes, in, out, n, dtype, op, codec, block);
+    size_t nb = (codec == ORC_CODEC_E4M3 || codec == ORC_CODEC_E5M2) ? orc_n_blocks(n, block) : 0;
+    size_t cb = code_bytes(codec);
+    float *s = malloc((n ? n : 1) * sizeof(float));
+    uint8_t *codes = malloc((n ? n : 1) * cb * (size_t)I);
+    float *scales = malloc((nb ? nb : 1) * sizeof(float) * (size_t)I);
+    float *t = malloc((n ? n : 1) * sizeof(float));
+    const void **cptr = malloc(sizeof(void *) * (size_t)I);
+    const float **sptr = malloc(sizeof(float *) * (size_t)I);
+    if (!s || !codes || !scales || !t || !cptr || !sptr) {
+        free(s); free(codes); free(scales); free(t); free(cptr); free(sptr);
+        return -1;
+    }
+    int first = 0;
+    for (int i = 0; i < I; ++i) {
+        orc_island_sum(island_sizes[i], in + first, dtype, n, s);
+        orc_encode_ef(s, n, codec, block, residuals[i], codes + (size_t)i * n * cb, scales + (size_t)i * nb);
+        cptr[i] = codes + (size_t)i * n * cb;
+        sptr[i] = scales + (size_t)i * nb;
+        first += island_sizes[i];
+    }
+    orc_bridge_total(I, cptr, sptr, n, codec, block, op, W, t);
+    for (int r = 0; r < W; ++r)
+        for (size_t j = 0; j < n; ++j)
+            store_elem(out[r], dtype, j, t[j]);
+    free(s); free(codes); free(scales); free(t); free(cptr); free(sptr);
+    return 0;
+}

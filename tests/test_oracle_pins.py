@@ -474,3 +474,82 @@ def test_bucket_plan_small_cases_and_padding():
         pad = int(rng.choice([1, 2, 8, 256]))
         bo, off, bn = orc.bucket_plan(numels, 4, cap, pad)
         _check_greedy(numels, 4, cap, bo, off, bn, pad)
+
+
+# ------------------------------------------------------------- error feedback
+
+def _grid_data(rng, n, W):
+    """Values on a 2^-12 grid in [-1, 1]: every float32 operation of the
+    error-feedback step is then exact (dec values sit on a grid no coarser
+    than 2^-16, s + r spans fewer than 24 bits, and s' - dec(enc(s')) is
+    exact by Sterbenz's lemma or because dec is 0)."""
+    return [(rng.integers(-4096, 4097, n) / 4096.0).astype(np.float32) for _ in range(W)]
+
+
+@pytest.mark.parametrize("codec,block", [("e4m3", 256), ("e5m2", 128), ("bf16", 256)])
+def test_error_feedback_telescopes_exactly(codec, block):
+    """sum_t dec(p_t) = sum_t s_t + r_0 - r_T per element, exactly (the
+    residual carries every rounding error into the next step)."""
+    rng = np.random.default_rng(71)
+    n, T = 3 * block + 17, 6
+    r = np.zeros(n, np.float32)
+    r0 = r.copy()
+    sum_dec = np.zeros(n, dtype=object)
+    sum_s = np.zeros(n, dtype=object)
+    for _ in range(T):
+        s = _grid_data(rng, n, 1)[0] * np.float32(3.0)
+        codes, scales = orc.encode_ef(s, r, codec, block)
+        dec = orc.decode(codes, scales, codec, block)
+        sum_dec += np.array([Fraction(float(v)) for v in dec], dtype=object)
+        sum_s += np.array([Fraction(float(v)) for v in s], dtype=object)
+    rhs = sum_s + np.array([Fraction(float(v)) for v in r0], dtype=object) - \
+        np.array([Fraction(float(v)) for v in r], dtype=object)
+    assert all(a == b for a, b in zip(sum_dec, rhs))
+
+
+@pytest.mark.parametrize("codec,block,c", [("e4m3", 256, 2.0 ** -4), ("e5m2", 128, 2.0 ** -3)])
+def test_error_feedback_residual_bound(codec, block, c):
+    rng = np.random.default_rng(73)
+    n = 5 * block + 3
+    r = np.zeros(n, np.float32)
+    for _ in range(4):
+        s = (rng.standard_normal(n) * np.exp2(rng.integers(-20, 5, n))).astype(np.float32)
+        sp = (s + r).astype(np.float32)
+        orc.encode_ef(s, r, codec, block)
+        for b in range(orc.n_blocks(n, block)):
+            blk = slice(b * block, (b + 1) * block)
+            assert np.all(np.abs(r[blk].astype(np.float64)) <= c * np.max(np.abs(sp[blk].astype(np.float64))))
+
+
+def test_error_feedback_none_codec_is_plain_all_reduce():
+    rng = np.random.default_rng(79)
+    sizes = (2, 1, 1)
+    xs = [rng.standard_normal(1000).astype(np.float32) for _ in range(4)]
+    res = [np.zeros(1000, np.float32) for _ in range(3)]
+    outs = orc.all_reduce_ef(xs, sizes, res, "avg", "none")
+    want = orc.all_reduce(xs, sizes, "avg", "none")
+    for o, w_ in zip(outs, want):
+        assert np.array_equal(o.view(np.uint32), w_.view(np.uint32))
+    assert all(not np.any(r) for r in res)
+
+
+def test_error_feedback_error_does_not_accumulate():
+    """Over many steps the summed compressed totals stay within the final
+    residuals (plus float32 rounding) of the summed exact totals; without
+    error feedback the gap grows with the number of steps."""
+    rng = np.random.default_rng(83)
+    sizes, n, T = (1, 1), 512, 64
+    res = [np.zeros(n, np.float32) for _ in range(2)]
+    acc_ef = np.zeros(n)
+    acc_plain = np.zeros(n)
+    acc_exact = np.zeros(n)
+    base = rng.standard_normal(n).astype(np.float32)
+    for _ in range(T):
+        xs = [(base + rng.standard_normal(n).astype(np.float32) * np.float32(1e-3)) for _ in range(2)]
+        acc_exact += xs[0].astype(np.float64) + xs[1].astype(np.float64)
+        acc_ef += orc.all_reduce_ef(xs, sizes, res, "sum", "e4m3", 256)[0]
+        acc_plain += orc.all_reduce(xs, sizes, "sum", "e4m3", 256)[0]
+    gap_ef = np.abs(acc_ef - acc_exact)
+    bound = np.abs(res[0].astype(np.float64)) + np.abs(res[1].astype(np.float64)) + T * 4 * U * np.abs(acc_exact / T) * 4
+    assert np.all(gap_ef <= bound + 1e-6)
+    assert np.max(np.abs(acc_plain - acc_exact)) > 4 * np.max(gap_ef)

@@ -119,6 +119,16 @@ class Context:
         self._check(B.gb_all_reduce(self.handle, [t.data_ptr() for t in tensors], tensors[0].numel(), dt,
                                     _op(op), _codec(codec), block, _stream(stream)))
 
+    def all_reduce_ef(self, tensors, residuals, op="sum", codec="none", block=256, stream=None):
+        """all_reduce with error feedback; residuals: one float32 tensor of the
+        buffers' size per island, zero before the first step, kept across steps."""
+        dt = _dtype(tensors)
+        for r in residuals:
+            if r.dtype != torch.float32 or not r.is_contiguous() or r.numel() != tensors[0].numel():
+                raise GbError(B.GB_ERR_INVALID_ARG, "residuals: contiguous float32 of the buffers' size")
+        self._check(B.gb_all_reduce_ef(self.handle, [t.data_ptr() for t in tensors], [r.data_ptr() for r in residuals],
+                                       tensors[0].numel(), dt, _op(op), _codec(codec), block, _stream(stream)))
+
     def reduce_scatter(self, inputs, outputs, op="sum", codec="none", block=256, stream=None):
         dt = _dtype(list(inputs) + list(outputs))
         self._check(B.gb_reduce_scatter(self.handle, [t.data_ptr() for t in inputs],

@@ -62,6 +62,7 @@ SIGNATURES = {
     "gb_bridge_decompress_accumulate": (_i, [_vp, _vp, _sz, _i, _i, _vp, _i, _vp]),
     "gb_island_broadcast": (_i, [_vp, _i, _vp, _sz, _i, _P(_vp), _i, _vp]),
     "gb_all_reduce": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
+    "gb_all_reduce_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_reduce_scatter": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_all_gather": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _vp]),
     "gb_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _vp]),
@@ -188,6 +189,10 @@ def gb_island_broadcast(ctx, island, total, n, op, rank_bufs, dtype, stream=0):
 
 def gb_all_reduce(ctx, rank_bufs, n, dtype, op, codec, block, stream=0):
     return lib().gb_all_reduce(ctx, _ptrs(rank_bufs), n, dtype, op, codec, block, stream)
+
+
+def gb_all_reduce_ef(ctx, rank_bufs, residuals, n, dtype, op, codec, block, stream=0):
+    return lib().gb_all_reduce_ef(ctx, _ptrs(rank_bufs), _ptrs(residuals), n, dtype, op, codec, block, stream)
 
 
 def gb_reduce_scatter(ctx, inp, out, n_in, dtype, op, codec, block, stream=0):

@@ -26,6 +26,7 @@ constexpr int kMaxGraphs = 16;
 // Identity of a captured all_reduce (every value its graph bakes in).
 struct GraphKey {
     const void *in[GB_MAX_RANKS];
+    const void *res[GB_MAX_ISLANDS];
     uint64_t n, chunk;
     int dtype, op, codec, block, timed, pad;
     const void *d_stage, *h_stage;
@@ -107,7 +108,8 @@ gb_status fail(gb_ctx *c, gb_status s, const char *what, cudaError_t e = cudaSuc
 
 size_t elem_bytes(gb_dtype d) { return d == GB_F32 ? 4 : 2; }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+// The kernels move float32 data with 32-byte vector accesses.
+bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
 
 gb_status check_ctx(gb_ctx *c) {
     if (!c) return GB_ERR_INVALID_ARG;
@@ -150,14 +152,14 @@ gb_status check_dev_bufs(gb_ctx *c, const void *const *bufs, int count, const ch
     if (!bufs) return set_msg(c, GB_ERR_INVALID_ARG, "%s is NULL", name);
     for (int r = 0; r < count; ++r) {
         if (!bufs[r]) return set_msg(c, GB_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
-        if (!aligned16(bufs[r])) return set_msg(c, GB_ERR_MISALIGNED, "%s[%d] not 16-byte aligned", name, r);
+        if (!aligned32(bufs[r])) return set_msg(c, GB_ERR_MISALIGNED, "%s[%d] not 32-byte aligned", name, r);
     }
     return GB_OK;
 }
 
 gb_status check_dev_ptr(gb_ctx *c, const void *p, const char *name) {
     if (!p) return set_msg(c, GB_ERR_INVALID_ARG, "%s is NULL", name);
-    if (!aligned16(p)) return set_msg(c, GB_ERR_MISALIGNED, "%s not 16-byte aligned", name);
+    if (!aligned32(p)) return set_msg(c, GB_ERR_MISALIGNED, "%s not 32-byte aligned", name);
     return GB_OK;
 }
 
@@ -428,8 +430,8 @@ gb_status record(gb_ctx *c, cudaEvent_t ev, cudaStream_t s) {
 // decode overlap: chunk c's copies wait for its encode, and its decode waits
 // for its copies.  Staging (see Plan): own parts outbox(c, i), host slots
 // host(c, j), leader g's received parts inbox(g, c, j).
-gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *const *out, cudaStream_t s,
-                      int markmode, bool multi) {
+gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *const *out,
+                      float *const *res, cudaStream_t s, int markmode, bool multi) {
     const int I = p.I;
     auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
     // leader g's received copy of island j's part of chunk ch (j != g)
@@ -450,6 +452,7 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         memset(&ra, 0, sizeof ra);
         for (int r = 0; r < p.W; ++r) ra.src[r] = (const unsigned char *)in[r] + e0 * p.eb;
         for (int i = 0; i < I; ++i) ra.payload[i] = outbox(ch, i);
+        for (int i = 0; res && I > 1 && i < I; ++i) ra.residual[i] = res[i] + e0;  // no bridge: no feedback
         for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
         ra.n_islands = I;
         ra.n = m;
@@ -544,10 +547,11 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
 
 // Capture one pipelined all_reduce on the context's capture stream and
 // instantiate it.  The stand-in mark events become event-record nodes.
-gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, bool timed, GraphEntry *ge) {
+gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, float *const *res, bool timed,
+                      GraphEntry *ge) {
     cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
     if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
-    gb_status st = enqueue_rbb(c, p, in, (void *const *)in, c->scap, timed ? kMarkCapture : kMarkOff, true);
+    gb_status st = enqueue_rbb(c, p, in, (void *const *)in, res, c->scap, timed ? kMarkCapture : kMarkOff, true);
     cudaGraph_t g = nullptr;
     e = cudaStreamEndCapture(c->scap, &g);
     if (st != GB_OK) {
@@ -609,7 +613,7 @@ GraphEntry *new_graph_slot(gb_ctx *c) {
 // all_reduce runs as a CUDA graph captured on the second call with the same
 // buffers and shape (the first runs directly) and replayed afterwards.
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
-                  gb_op op, gb_codec codec, int block, cudaStream_t s, int rs) {
+                  gb_op op, gb_codec codec, int block, cudaStream_t s, int rs, float *const *res = nullptr) {
     const Plan p = make_plan(c, n, dtype, op, codec, block, rs);
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
     if (p.host_bytes) GB_TRY(grow_host(c, p.host_bytes));
@@ -617,13 +621,14 @@ gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, 
     const bool timed = c->tcap > 0;
     const bool graphable = !rs && p.C > 1 && c->use_graphs && (const void *)in == (const void *)out;
     if (!graphable) {
-        GB_TRY(enqueue_rbb(c, p, in, out, s, timed ? kMarkDirect : kMarkOff, p.C > 1));
+        GB_TRY(enqueue_rbb(c, p, in, out, res, s, timed ? kMarkDirect : kMarkOff, p.C > 1));
         commit_marks(c, p.C, p.I > 1);
         return end(c, s);
     }
     GraphKey k;
     memset(&k, 0, sizeof k);
     for (int r = 0; r < c->W; ++r) k.in[r] = in[r];
+    for (int i = 0; res && i < c->I; ++i) k.res[i] = res[i];
     k.n = n;
     k.chunk = p.chunk;
     k.dtype = dtype;
@@ -638,12 +643,12 @@ gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, 
         ge = new_graph_slot(c);
         ge->key = k;
         ge->last_use = ++c->clock;
-        GB_TRY(enqueue_rbb(c, p, in, out, s, timed ? kMarkDirect : kMarkOff, true));
+        GB_TRY(enqueue_rbb(c, p, in, out, res, s, timed ? kMarkDirect : kMarkOff, true));
         commit_marks(c, p.C, true);
         return end(c, s);
     }
     ge->last_use = ++c->clock;
-    if (!ge->exec) GB_TRY(capture_rbb(c, p, in, timed, ge));
+    if (!ge->exec) GB_TRY(capture_rbb(c, p, in, res, timed, ge));
     if (timed) {
         const long long slot = c->tcount % c->tcap;
         for (int idx = 0; idx < kMarks; ++idx) {
@@ -902,6 +907,18 @@ gb_status gb_all_reduce(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dt
     GB_TRY(bind(c));
     return run_rbb(c, (const void *const *)rank_bufs, rank_bufs, n, dtype, op, codec, block,
                    (cudaStream_t)stream, 0);
+}
+
+gb_status gb_all_reduce_ef(gb_ctx *c, void *const *rank_bufs, float *const *residuals, size_t n, gb_dtype dtype,
+                           gb_op op, gb_codec codec, int block, gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_collective(c, n, dtype, op, codec, block));
+    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_dev_bufs(c, (const void *const *)residuals, c->I, "residuals"));
+    if (n == 0) return GB_OK;
+    GB_TRY(bind(c));
+    return run_rbb(c, (const void *const *)rank_bufs, rank_bufs, n, dtype, op, codec, block, (cudaStream_t)stream,
+                   0, residuals);
 }
 
 gb_status gb_reduce_scatter(gb_ctx *c, const void *const *in, void *const *out, size_t n_in,

@@ -48,6 +48,16 @@ __device__ __forceinline__ U8x32 ld_v8(const void *p) {
         : "l"(p));
     return r;
 }
+// Coherent (read-write) 32-byte load, for buffers the kernel also writes.
+__device__ __forceinline__ U8x32 ld_rw_v8(const void *p) {
+    U8x32 r;
+    asm volatile("ld.global.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+                   "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
 __device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

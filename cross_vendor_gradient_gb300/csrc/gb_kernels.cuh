@@ -16,6 +16,7 @@ namespace gb {
 struct ReduceEncodeArgs {
     const void *src[GB_MAX_RANKS];
     void *payload[GB_MAX_ISLANDS];
+    float *residual[GB_MAX_ISLANDS];  // error feedback (all null: none)
     int first[GB_MAX_ISLANDS + 1];
     int n_islands;
     uint64_t n;

@@ -68,9 +68,11 @@ __device__ __forceinline__ float block_absmax(const float v[8]) {
 }
 
 // Encode this lane's 8 island-sum values into the payload at tile `tile`.
-template <int CODEC, int BLOCK>
+// With DEC, dec[] receives the decoded value of every code written (the
+// value the receiving leaders will add), for error feedback.
+template <int CODEC, int BLOCK, bool DEC>
 __device__ __forceinline__ void encode_store(unsigned char *payload, uint64_t scales_off, uint32_t tile,
-                                             int lane, uint64_t n, bool full, const float v[8]) {
+                                             int lane, uint64_t n, bool full, const float v[8], float dec[8]) {
     const uint64_t base = (uint64_t)tile * kTile;
     if constexpr (CODEC == GB_CODEC_NONE) {
         float *o = (float *)payload;
@@ -86,16 +88,28 @@ __device__ __forceinline__ void encode_store(unsigned char *payload, uint64_t sc
                 if (j < n) o[j] = v[k];
             }
         }
+        if constexpr (DEC) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) dec[k] = v[k];
+        }
     } else if constexpr (CODEC == GB_CODEC_BF16) {
         unsigned short *o = (unsigned short *)payload;
+        const uint32_t c[4] = {cvt_bf16x2(v[0], v[1]), cvt_bf16x2(v[2], v[3]), cvt_bf16x2(v[4], v[5]),
+                               cvt_bf16x2(v[6], v[7])};
         if (full) {
-            st_u4(o + base + 8 * lane, make_uint4(cvt_bf16x2(v[0], v[1]), cvt_bf16x2(v[2], v[3]),
-                                                  cvt_bf16x2(v[4], v[5]), cvt_bf16x2(v[6], v[7])));
+            st_u4(o + base + 8 * lane, make_uint4(c[0], c[1], c[2], c[3]));
         } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint64_t j = base + lane_elem(lane, k);
-                if (j < n) o[j] = (unsigned short)(cvt_bf16x2(v[k], 0.0f) & 0xFFFFu);
+                if (j < n) o[j] = (unsigned short)((k & 1) ? (c[k >> 1] >> 16) : (c[k >> 1] & 0xFFFFu));
+            }
+        }
+        if constexpr (DEC) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                dec[2 * i] = __uint_as_float(c[i] << 16);
+                dec[2 * i + 1] = __uint_as_float(c[i] & 0xFFFF0000u);
             }
         }
     } else {
@@ -104,16 +118,26 @@ __device__ __forceinline__ void encode_store(unsigned char *payload, uint64_t sc
         float y[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = __fmul_rn(v[k], inv);  // exact, or below fp8 half-ulp
+        const uint32_t p[4] = {cvt_fp8x2<CODEC>(y[0], y[1]), cvt_fp8x2<CODEC>(y[2], y[3]),
+                               cvt_fp8x2<CODEC>(y[4], y[5]), cvt_fp8x2<CODEC>(y[6], y[7])};
         unsigned char *o = payload;
         if (full) {
-            const uint32_t w0 = cvt_fp8x2<CODEC>(y[0], y[1]) | (cvt_fp8x2<CODEC>(y[2], y[3]) << 16);
-            const uint32_t w1 = cvt_fp8x2<CODEC>(y[4], y[5]) | (cvt_fp8x2<CODEC>(y[6], y[7]) << 16);
-            st_u2(o + base + 8 * lane, make_uint2(w0, w1));
+            st_u2(o + base + 8 * lane, make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16)));
         } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint64_t j = base + lane_elem(lane, k);
-                if (j < n) o[j] = (unsigned char)(cvt_fp8x2<CODEC>(y[k], 0.0f) & 0xFFu);
+                if (j < n) o[j] = (unsigned char)((k & 1) ? (p[k >> 1] >> 8) : (p[k >> 1] & 0xFFu));
+            }
+        }
+        if constexpr (DEC) {
+            const float sc = pow2f(kexp);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float lo, hi;
+                fp8x2_to_f32<CODEC>(p[i], lo, hi);
+                dec[2 * i] = __fmul_rn(lo, sc);  // exact
+                dec[2 * i + 1] = __fmul_rn(hi, sc);
             }
         }
         // one float32 scale 2^k per existing block of the tile
@@ -128,8 +152,43 @@ __device__ __forceinline__ void encode_store(unsigned char *payload, uint64_t sc
     }
 }
 
+// The island sum of this lane's 8 elements of the tile at `base` (ascending
+// rank order).  KT > 0: exactly KT ranks, all loads issued before the first
+// add; KT == 0: K ranks, four ranks' loads in flight at a time.
+template <typename T, int KT>
+__device__ __forceinline__ void island_sum(const ReduceEncodeArgs &a, int r0, int K, uint64_t base, int lane,
+                                           bool full, float v[8]) {
+    if constexpr (KT > 0) {
+        float w[KT][8];
+#pragma unroll
+        for (int q = 0; q < KT; ++q) load_rank<T>(a.src[r0 + q], base, lane, a.n, full, w[q]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = w[0][k];
+#pragma unroll
+        for (int q = 1; q < KT; ++q)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], w[q][k]);
+    } else {
+        load_rank<T>(a.src[r0], base, lane, a.n, full, v);
+        for (int q0 = 1; q0 < K; q0 += 4) {
+            float w[4][8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q0 + u < K) load_rank<T>(a.src[r0 + q0 + u], base, lane, a.n, full, w[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q0 + u < K) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], w[u][k]);
+                }
+        }
+    }
+}
+
 // KT > 0: every island has KT ranks (loads unrolled); KT == 0: any sizes.
-template <typename T, int CODEC, int BLOCK, int KT>
+// EF: error feedback -- encode s + r and keep r = (s + r) - dec(codes) in
+// the island's residual buffer (float32, n elements).
+template <typename T, int CODEC, int BLOCK, int KT, bool EF>
 __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ ReduceEncodeArgs a) {
     const int isl = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -143,58 +202,70 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
         const uint64_t base = (uint64_t)tile * kTile;
         const bool full = base + kTile <= n;
         float v[8];
-        if constexpr (KT > 0) {
-            float w[KT][8];
+        island_sum<T, KT>(a, r0, K, base, lane, full, v);
+        if constexpr (EF) {
+            float *res = a.residual[isl];
+            float r[8], dec[8];
+            if (full) {
+                const U8x32 x = ld_rw_v8(res + base + 8 * lane);
 #pragma unroll
-            for (int q = 0; q < KT; ++q) load_rank<T>(a.src[r0 + q], base, lane, n, full, w[q]);
+                for (int k = 0; k < 8; ++k) r[k] = __uint_as_float(x.w[k]);
+            } else {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = w[0][k];
-#pragma unroll
-            for (int q = 1; q < KT; ++q)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], w[q][k]);  // ascending rank order
-        } else {
-            load_rank<T>(a.src[r0], base, lane, n, full, v);
-            for (int q0 = 1; q0 < K; q0 += 4) {  // four ranks' loads in flight at a time
-                float w[4][8];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (q0 + u < K) load_rank<T>(a.src[r0 + q0 + u], base, lane, n, full, w[u]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (q0 + u < K) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], w[u][k]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t j = base + lane_elem(lane, k);
+                    r[k] = j < n ? res[j] : 0.0f;
+                }
             }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], r[k]);
+            encode_store<CODEC, BLOCK, true>(payload, a.scales_off, tile, lane, n, full, v, dec);
+            if (full) {
+                uint32_t w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__fsub_rn(v[k], dec[k]));
+                st_v8(res + base + 8 * lane, w);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t j = base + lane_elem(lane, k);
+                    if (j < n) res[j] = __fsub_rn(v[k], dec[k]);
+                }
+            }
+        } else {
+            encode_store<CODEC, BLOCK, false>(payload, a.scales_off, tile, lane, n, full, v, nullptr);
         }
-        encode_store<CODEC, BLOCK>(payload, a.scales_off, tile, lane, n, full, v);
     }
 }
 
-template <typename T, int CODEC, int BLOCK>
+template <typename T, int CODEC, int BLOCK, bool EF>
 static cudaError_t dispatch_k(const ReduceEncodeArgs &a, cudaStream_t s) {
     int K = a.first[1] - a.first[0];
     for (int i = 1; i < a.n_islands; ++i)
         if (a.first[i + 1] - a.first[i] != K) K = 0;
     const unsigned units = (unsigned)a.n_islands;
     switch (K) {
-    case 1: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 1>>(a.tiles, units, a, s);
-    case 2: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 2>>(a.tiles, units, a, s);
-    case 4: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 4>>(a.tiles, units, a, s);
-    default: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 0>>(a.tiles, units, a, s);
+    case 1: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 1, EF>>(a.tiles, units, a, s);
+    case 2: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 2, EF>>(a.tiles, units, a, s);
+    case 4: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 4, EF>>(a.tiles, units, a, s);
+    default: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 0, EF>>(a.tiles, units, a, s);
     }
+}
+
+template <typename T, int CODEC, int BLOCK>
+static cudaError_t dispatch_ef(const ReduceEncodeArgs &a, cudaStream_t s) {
+    return a.residual[0] ? dispatch_k<T, CODEC, BLOCK, true>(a, s) : dispatch_k<T, CODEC, BLOCK, false>(a, s);
 }
 
 template <typename T>
 static cudaError_t dispatch_codec(const ReduceEncodeArgs &a, int codec, int block, cudaStream_t s) {
     switch (codec) {
-    case GB_CODEC_NONE: return dispatch_k<T, GB_CODEC_NONE, 256>(a, s);
-    case GB_CODEC_BF16: return dispatch_k<T, GB_CODEC_BF16, 256>(a, s);
+    case GB_CODEC_NONE: return dispatch_ef<T, GB_CODEC_NONE, 256>(a, s);
+    case GB_CODEC_BF16: return dispatch_ef<T, GB_CODEC_BF16, 256>(a, s);
     case GB_CODEC_E4M3:
-        return block == 128 ? dispatch_k<T, GB_CODEC_E4M3, 128>(a, s) : dispatch_k<T, GB_CODEC_E4M3, 256>(a, s);
+        return block == 128 ? dispatch_ef<T, GB_CODEC_E4M3, 128>(a, s) : dispatch_ef<T, GB_CODEC_E4M3, 256>(a, s);
     case GB_CODEC_E5M2:
-        return block == 128 ? dispatch_k<T, GB_CODEC_E5M2, 128>(a, s) : dispatch_k<T, GB_CODEC_E5M2, 256>(a, s);
+        return block == 128 ? dispatch_ef<T, GB_CODEC_E5M2, 128>(a, s) : dispatch_ef<T, GB_CODEC_E5M2, 256>(a, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -61,7 +61,7 @@ size_t payload_bytes_of(int codec, int block, size_t n) {
     }
 }
 
-bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
 
 }  // namespace
 
@@ -78,7 +78,7 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
     if (!rank_bufs) return GB_ERR_INVALID_ARG;
     for (int r = 0; r < W; ++r) {
         if (!rank_bufs[r]) return GB_ERR_INVALID_ARG;
-        if (!aligned16(rank_bufs[r])) return GB_ERR_MISALIGNED;
+        if (!aligned32(rank_bufs[r])) return GB_ERR_MISALIGNED;
     }
     if (n == 0) return GB_OK;
     const int eff = I == 1 ? GB_CODEC_NONE : (int)codec;

@@ -19,8 +19,11 @@
  *
  * Conventions for every call below:
  *   - Pointers named *_bufs / rank_bufs / in / out are arrays of W (or K_i)
- *     DEVICE pointers, in global rank order, each 16-byte aligned
- *     (GB_ERR_MISALIGNED otherwise).  The caller owns them.
+ *     DEVICE pointers, in global rank order, each 32-byte aligned (the
+ *     kernels move float32 data with 32-byte vector accesses; cudaMalloc
+ *     and torch allocations are; GB_ERR_MISALIGNED otherwise).  Every other
+ *     device buffer argument must be 32-byte aligned too.  The caller owns
+ *     them.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call validates all of its arguments first and returns an error with
  *     nothing enqueued; otherwise it enqueues its work on `stream` and returns
@@ -60,7 +63,7 @@ typedef enum {
     GB_ERR_UNSUPPORTED_DTYPE = 2, /* dtype other than GB_F32 / GB_BF16                    */
     GB_ERR_UNSUPPORTED_OP = 3,    /* op other than GB_SUM / GB_AVG                        */
     GB_ERR_UNSUPPORTED_CODEC = 4, /* unknown codec, or fp8 block not 128 / 256            */
-    GB_ERR_MISALIGNED = 5,        /* a device buffer not 16-byte aligned                  */
+    GB_ERR_MISALIGNED = 5,        /* a device buffer not 32-byte aligned                  */
     GB_ERR_ALLOC = 6,             /* pinned or device staging allocation failed (sticky)  */
     GB_ERR_CUDA = 7,              /* a CUDA runtime call failed (sticky)                  */
     GB_ERR_BRIDGE = 8,            /* the bridge hop failed (sticky)                       */
@@ -173,12 +176,12 @@ size_t gb_payload_scales_offset(gb_codec codec, int block, size_t n);
 
 /* island_sum[j] = ((x_0[j] + x_1[j]) + ...) + x_{K-1}[j] in float32, over the
  * K = gb_island_size(ctx, island) buffers of `rank_bufs` (that island's
- * ranks, in rank order).  island_sum: n float32, device, 16-byte aligned,
+ * ranks, in rank order).  island_sum: n float32, device, 32-byte aligned,
  * must not overlap the inputs. */
 gb_status gb_island_reduce(gb_ctx *ctx, int island, const void *const *rank_bufs, size_t n,
                            gb_dtype dtype, float *island_sum, gb_stream stream);
 
-/* Encode n float32 values (device) into `payload` (device, 16-byte aligned,
+/* Encode n float32 values (device) into `payload` (device, 32-byte aligned,
  * gb_payload_bytes(codec, block, n) bytes, laid out as described above).
  * block is ignored for none / bf16. */
 gb_status gb_bridge_compress(gb_ctx *ctx, const float *island_sum, size_t n, gb_codec codec,
@@ -186,7 +189,7 @@ gb_status gb_bridge_compress(gb_ctx *ctx, const float *island_sum, size_t n, gb_
 
 /* accum[j] = dec(payload)[j] (accumulate == 0) or accum[j] + dec(payload)[j]
  * (accumulate != 0), float32, round to nearest even.  accum: n float32,
- * device, 16-byte aligned. */
+ * device, 32-byte aligned. */
 gb_status gb_bridge_decompress_accumulate(gb_ctx *ctx, const void *payload, size_t n,
                                           gb_codec codec, int block, float *accum, int accumulate,
                                           gb_stream stream);
@@ -204,6 +207,19 @@ gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_
  * Every rank buffer ends with the same bits. */
 gb_status gb_all_reduce(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype dtype, gb_op op,
                         gb_codec codec, int block, gb_stream stream);
+
+/* gb_all_reduce with error feedback (gpubridge README, "Bridge
+ * compression": each bridge member keeps an error-feedback residual per
+ * buffer, so rounding error carries into the next step instead of
+ * accumulating).  residuals: I device float32 arrays of n elements, one per
+ * island, owned by the caller, zero before the first call and kept (with
+ * the rank buffers' shape) from call to call of the same gradient buffer.
+ * Each leader encodes s_i + r_i and sets r_i = (s_i + r_i) - dec(payload_i)
+ * (float32); the rest is gb_all_reduce.  With one island there is no bridge
+ * and the residuals are left unchanged.  Saving and restoring the residual
+ * arrays checkpoints and resumes the feedback state. */
+gb_status gb_all_reduce_ef(gb_ctx *ctx, void *const *rank_bufs, float *const *residuals, size_t n,
+                           gb_dtype dtype, gb_op op, gb_codec codec, int block, gb_stream stream);
 
 /* reduce_scatter (API table, reduce_scatter_tensor row): out_r (n_in / W
  * elements) receives elements [r * n_in / W, (r + 1) * n_in / W) of what

@@ -120,6 +120,7 @@ def test_argument_errors_need_no_device():
         assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 5, 256) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_all_reduce(ctx, fake[:3] + [0], 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
         assert B.gb_all_reduce(ctx, fake[:3] + [0x10008], 10, 0, 0, 0, 256) == B.GB_ERR_MISALIGNED
+        assert B.gb_all_reduce(ctx, fake[:3] + [0x10010], 10, 1, 0, 0, 256) == B.GB_ERR_MISALIGNED
         assert B.gb_reduce_scatter(ctx, fake, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG  # 10 % 4
         assert B.gb_broadcast(ctx, fake, 10, 0, 4) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce(ctx, 2, fake, 10, 0, fake[0]) == B.GB_ERR_INVALID_ARG

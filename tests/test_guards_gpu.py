@@ -10,7 +10,7 @@ from cross_vendor_gradient_gb300 import Context, payload_bytes
 from cross_vendor_gradient_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
-GUARD = 512  # bytes on each side (keeps the buffer 16-byte aligned)
+GUARD = 512  # bytes on each side (keeps the buffer 32-byte aligned)
 SENTINEL = 0xA5
 
 

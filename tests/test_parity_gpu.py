@@ -151,7 +151,7 @@ def test_phase_blocks_match_oracle_and_compose_to_all_reduce(codec, block, dtype
 def test_reduce_scatter_and_all_gather(codec, block, sizes, dtype):
     W = sum(sizes)
     with Context(sizes) as ctx:
-        for m in (1, 5, 8, 300, 4096, 4099):  # slice lengths: 8 | m uses 16-byte accesses
+        for m in (1, 5, 8, 300, 4096, 4099):  # slice lengths: 8 | m uses vector accesses
             n = W * m
             xs = inputs(sizes, n, dtype, cid=m % 13)
             ins = [to_dev(x) for x in xs]
@@ -325,3 +325,31 @@ def test_pipelined_graph_replay_timing_and_streams():
             for r in range(4):
                 assert_bits_equal(to_host(bufs[r]), want[r], "call %d rank %d" % (call, r))
         assert len([ctx.phase_times(a) for a in range(4)]) == 4
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (2, 1, 3), (3,)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [0, 1024])
+def test_error_feedback_matches_oracle_over_steps(codec, block, sizes, dtype, chunk):
+    """gb_all_reduce_ef: outputs and residuals equal the oracle's bit for bit
+    over consecutive steps on the same buffers (direct, captured, replayed)."""
+    W, I = sum(sizes), len(sizes)
+    n = 256 * 23 + 9
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(chunk, True)
+        res_h = [np.zeros(n, np.float32) for _ in range(I)]
+        res_d = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in range(I)]
+        bufs = [torch.empty(n, dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device="cuda")
+                for _ in range(W)]
+        for step in range(4):
+            xs = inputs(sizes, n, dtype, cid=200 + step)
+            for b, x in zip(bufs, xs):
+                b.copy_(to_dev(x))
+            ctx.all_reduce_ef(bufs, res_d, "avg", codec, block)
+            want = orc.all_reduce_ef(xs, sizes, res_h, "avg", codec, block)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(bufs[r]), want[r], "EF step %d rank %d" % (step, r))
+            for i in range(I):
+                assert_bits_equal(to_host(res_d[i]), res_h[i], "EF step %d residual %d" % (step, i))

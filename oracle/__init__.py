@@ -16,12 +16,16 @@ import numpy as np
 
 from . import build as _build
 
-DT_F32, DT_BF16 = 0, 1
-OP_SUM, OP_AVG = 0, 1
+DT_F32, DT_BF16, DT_F16, DT_F64, DT_I8, DT_U8, DT_I32, DT_I64 = 0, 1, 2, 3, 4, 5, 6, 7
+OP_SUM, OP_AVG, OP_MAX, OP_MIN = 0, 1, 2, 3
 CODEC_NONE, CODEC_BF16, CODEC_E4M3, CODEC_E5M2 = 0, 1, 2, 3
 
 CODECS = {"none": CODEC_NONE, "bf16": CODEC_BF16, "e4m3": CODEC_E4M3, "e5m2": CODEC_E5M2}
-OPS = {"sum": OP_SUM, "avg": OP_AVG}
+OPS = {"sum": OP_SUM, "avg": OP_AVG, "max": OP_MAX, "min": OP_MIN}
+# numpy dtype of a rank buffer -> oracle dtype id (bf16 buffers are uint16 bit patterns)
+_NP_DT = {np.dtype(np.float32): DT_F32, np.dtype(np.uint16): DT_BF16, np.dtype(np.float16): DT_F16,
+          np.dtype(np.float64): DT_F64, np.dtype(np.int8): DT_I8, np.dtype(np.uint8): DT_U8,
+          np.dtype(np.int32): DT_I32, np.dtype(np.int64): DT_I64}
 
 _lib = None
 
@@ -78,6 +82,16 @@ def lib():
         L.orc_all_reduce_ef.restype = ctypes.c_int
         L.orc_all_reduce_ef.argtypes = [ctypes.c_int, vp, vp, vp, c_size, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, vp]
+        for name in ("orc_all_reduce_exact", "orc_reduce_scatter_exact"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.c_int, vp, vp, vp, c_size, ctypes.c_int, ctypes.c_int]
+        L.orc_f16_to_f32.restype = ctypes.c_float
+        L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.orc_f32_to_f16.restype = ctypes.c_uint16
+        L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+        L.orc_f32_to_f16_array.restype = None
+        L.orc_f32_to_f16_array.argtypes = [vp, c_size, vp]
         L.orc_fp8_encode_f32_array.restype = None
         L.orc_fp8_encode_f32_array.argtypes = [vp, c_size, ctypes.c_int, vp]
         L.orc_f32_to_bf16_array.restype = None
@@ -98,11 +112,9 @@ def _ptr_array(arrays):
 
 
 def _dtype_id(a: np.ndarray) -> int:
-    if a.dtype == np.float32:
-        return DT_F32
-    if a.dtype == np.uint16:
-        return DT_BF16
-    raise TypeError("rank buffers are float32 or uint16 (bf16 bit patterns), got %s" % a.dtype)
+    if a.dtype in _NP_DT:
+        return _NP_DT[a.dtype]
+    raise TypeError("unsupported rank buffer dtype %s" % a.dtype)
 
 
 def _codec_id(codec) -> int:
@@ -142,6 +154,18 @@ def f32_to_bf16_array(x: np.ndarray) -> np.ndarray:
 def bf16_bits_to_f32_array(h: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 patterns (a 16-bit shift)."""
     return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def f16_to_f32(h: int) -> float:
+    return lib().orc_f16_to_f32(int(h))
+
+
+def f32_to_f16_array(x: np.ndarray) -> np.ndarray:
+    """float16 bit patterns (uint16) of float32 inputs, nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().orc_f32_to_f16_array(_ptr(x), x.size, _ptr(out))
+    return out
 
 
 def fp8_max(codec) -> float:
@@ -246,9 +270,28 @@ def rbb_total(ranks, island_sizes, op="sum", codec="none", block: int = 256, int
     return t
 
 
+def _exact(ranks, op) -> bool:
+    """MAX / MIN and the float16, float64 and integer dtypes take the exact
+    path (no codec: it stays exact or is not offered)."""
+    return _op_id(op) in (OP_MAX, OP_MIN) or _dtype_id(ranks[0]) not in (DT_F32, DT_BF16)
+
+
+def _exact_call(name, ranks, island_sizes, op, out_elems):
+    sizes = np.asarray(island_sizes, dtype=np.int32)
+    outs = [np.empty(out_elems, ranks[0].dtype) for _ in ranks]
+    pi, _k1 = _ptr_array(ranks)
+    po, _k2 = _ptr_array(outs)
+    rc = getattr(lib(), name)(len(sizes), _ptr(sizes), pi, po, ranks[0].size, _dtype_id(ranks[0]), _op_id(op))
+    if rc:
+        raise ValueError("oracle %s refused (%d): AVG needs a float dtype, RS needs n %% W == 0" % (name, rc))
+    return outs
+
+
 def all_reduce(ranks, island_sizes, op="sum", codec="none", block: int = 256):
     """Outputs of every rank (new arrays, rank dtype)."""
     ranks = [np.ascontiguousarray(r) for r in ranks]
+    if _exact(ranks, op):
+        return _exact_call("orc_all_reduce_exact", ranks, island_sizes, op, ranks[0].size)
     sizes = np.asarray(island_sizes, dtype=np.int32)
     outs = [np.empty_like(r) for r in ranks]
     pi, _k1 = _ptr_array(ranks)
@@ -267,6 +310,8 @@ def reduce_scatter(ranks, island_sizes, op="sum", codec="none", block: int = 256
     n = ranks[0].size
     if n % W:
         raise ValueError("reduce_scatter needs n divisible by the world size")
+    if _exact(ranks, op):
+        return _exact_call("orc_reduce_scatter_exact", ranks, island_sizes, op, n // W)
     outs = [np.empty(n // W, ranks[0].dtype) for _ in ranks]
     pi, _k1 = _ptr_array(ranks)
     po, _k2 = _ptr_array(outs)

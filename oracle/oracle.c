@@ -541,3 +541,194 @@ int orc_all_reduce_ef(int I, const int *island_sizes, const void *const *in, voi
     free(s); free(codes); free(scales); free(t); free(cptr); free(sptr);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Exact path: MAX / MIN, and the float16, float64 and integer dtypes        */
+/* (gpubridge README, API table: SUM, AVG, MAX, MIN; supported dtypes        */
+/* float16, bfloat16, float32, float64, int8, uint8, int32, int64; "Bridge   */
+/* compression": MAX/MIN and integer dtypes stay exact).                     */
+/* Readings: integer SUM wraps modulo 2^bits (two's complement); float16    */
+/* and bfloat16 accumulate in float32 and round once; float64 in float64;   */
+/* MAX keeps the earlier value unless a later one is strictly greater (MIN: */
+/* strictly less), so among equal values (+0 / -0) the lower rank's wins.   */
+/* ------------------------------------------------------------------------ */
+
+enum { ORC_DT_F16 = 2, ORC_DT_F64 = 3, ORC_DT_I8 = 4, ORC_DT_U8 = 5, ORC_DT_I32 = 6, ORC_DT_I64 = 7 };
+enum { ORC_OP_MAX = 2, ORC_OP_MIN = 3 };
+
+/* IEEE binary16 value of a pattern (exact in float). */
+float orc_f16_to_f32(uint16_t h)
+{
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 31)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return (float)(s ? -v : v);
+}
+
+/* Round a float to binary16, to nearest, ties to even; beyond the largest
+ * finite value (65504) the IEEE result is an infinity. */
+uint16_t orc_f32_to_f16(float x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x))
+        return (uint16_t)(sign | 0x7E00);
+    double a = fabs((double)x);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    (void)frexp(a, &e2);
+    int ex = e2 - 1;
+    if (ex < -14)
+        ex = -14;                       /* subnormals share 2^-24 spacing */
+    double q = ldexp(1.0, ex - 10);
+    double v = nearbyint(a / q) * q;    /* exact quotient, half to even */
+    if (v >= 65520.0)                   /* rounds past 65504: infinity */
+        return (uint16_t)(sign | 0x7C00);
+    if (v == 0.0)
+        return sign;
+    (void)frexp(v, &e2);
+    int ev = e2 - 1;
+    if (ev < -14)
+        return (uint16_t)(sign | (int)ldexp(v, 24));
+    return (uint16_t)(sign | ((ev + 15) << 10) | ((int)ldexp(v, 10 - ev) - 1024));
+}
+
+static int is_float_dt(int dt) { return dt == ORC_DT_F32 || dt == ORC_DT_BF16 || dt == ORC_DT_F16 || dt == ORC_DT_F64; }
+
+size_t orc_dtype_bytes(int dt)
+{
+    switch (dt) {
+    case ORC_DT_F32: case ORC_DT_I32: return 4;
+    case ORC_DT_BF16: case ORC_DT_F16: return 2;
+    case ORC_DT_F64: case ORC_DT_I64: return 8;
+    default: return 1;
+    }
+}
+
+/* One element as the accumulator value: float widening for the floats
+ * (float64 stays double), the two's complement integer for the integers. */
+typedef struct { double f; int64_t i; } acc_t;
+
+static acc_t load_acc(const void *buf, int dt, size_t j)
+{
+    acc_t a = {0.0, 0};
+    switch (dt) {
+    case ORC_DT_F32: a.f = ((const float *)buf)[j]; break;
+    case ORC_DT_BF16: a.f = orc_bf16_to_f32(((const uint16_t *)buf)[j]); break;
+    case ORC_DT_F16: a.f = orc_f16_to_f32(((const uint16_t *)buf)[j]); break;
+    case ORC_DT_F64: a.f = ((const double *)buf)[j]; break;
+    case ORC_DT_I8: a.i = ((const int8_t *)buf)[j]; break;
+    case ORC_DT_U8: a.i = ((const uint8_t *)buf)[j]; break;
+    case ORC_DT_I32: a.i = ((const int32_t *)buf)[j]; break;
+    case ORC_DT_I64: a.i = ((const int64_t *)buf)[j]; break;
+    }
+    return a;
+}
+
+/* a (op) b in the dtype's accumulator arithmetic. */
+static acc_t combine(acc_t a, acc_t b, int dt, int op)
+{
+    acc_t r = a;
+    if (is_float_dt(dt)) {
+        if (op == ORC_OP_MAX) {
+            if (b.f > a.f) r = b;
+        } else if (op == ORC_OP_MIN) {
+            if (b.f < a.f) r = b;
+        } else if (dt == ORC_DT_F64) {
+            r.f = a.f + b.f;                       /* binary64 */
+        } else {
+            r.f = (double)((float)a.f + (float)b.f); /* binary32 */
+        }
+    } else {
+        if (op == ORC_OP_MAX) {
+            if (b.i > a.i) r = b;
+        } else if (op == ORC_OP_MIN) {
+            if (b.i < a.i) r = b;
+        } else {
+            r.i = (int64_t)((uint64_t)a.i + (uint64_t)b.i); /* wraps; truncated on store */
+        }
+    }
+    return r;
+}
+
+static void store_acc(void *buf, int dt, size_t j, acc_t a)
+{
+    switch (dt) {
+    case ORC_DT_F32: ((float *)buf)[j] = (float)a.f; break;
+    case ORC_DT_BF16: ((uint16_t *)buf)[j] = orc_f32_to_bf16((float)a.f); break;
+    case ORC_DT_F16: ((uint16_t *)buf)[j] = orc_f32_to_f16((float)a.f); break;
+    case ORC_DT_F64: ((double *)buf)[j] = a.f; break;
+    case ORC_DT_I8: ((int8_t *)buf)[j] = (int8_t)(uint8_t)(uint64_t)a.i; break;
+    case ORC_DT_U8: ((uint8_t *)buf)[j] = (uint8_t)(uint64_t)a.i; break;
+    case ORC_DT_I32: ((int32_t *)buf)[j] = (int32_t)(uint32_t)(uint64_t)a.i; break;
+    case ORC_DT_I64: ((int64_t *)buf)[j] = a.i; break;
+    }
+}
+
+/* Exact reduce-bridge-broadcast total of element j: island folds in rank
+ * order, then the fold over islands in island order, then AVG's division
+ * (float32 for the 16- and 32-bit floats, float64 for float64). */
+static acc_t exact_total(int I, const int *island_sizes, const void *const *in, int dt, int op, size_t j)
+{
+    int W = 0;
+    for (int i = 0; i < I; ++i)
+        W += island_sizes[i];
+    acc_t t = {0.0, 0};
+    int first = 0;
+    for (int i = 0; i < I; ++i) {
+        acc_t s = load_acc(in[first], dt, j);
+        for (int q = 1; q < island_sizes[i]; ++q)
+            s = combine(s, load_acc(in[first + q], dt, j), dt, op == ORC_OP_AVG ? ORC_OP_SUM : op);
+        t = (i == 0) ? s : combine(t, s, dt, op == ORC_OP_AVG ? ORC_OP_SUM : op);
+        first += island_sizes[i];
+    }
+    if (op == ORC_OP_AVG) {
+        if (dt == ORC_DT_F64)
+            t.f = t.f / (double)W;
+        else
+            t.f = (double)((float)t.f / (float)W);
+    }
+    return t;
+}
+
+int orc_all_reduce_exact(int I, const int *island_sizes, const void *const *in, void *const *out, size_t n,
+                         int dtype, int op)
+{
+    int W = 0;
+    for (int i = 0; i < I; ++i)
+        W += island_sizes[i];
+    if (op == ORC_OP_AVG && !is_float_dt(dtype))
+        return -2;
+    for (size_t j = 0; j < n; ++j) {
+        acc_t t = exact_total(I, island_sizes, in, dtype, op, j);
+        for (int r = 0; r < W; ++r)
+            store_acc(out[r], dtype, j, t);
+    }
+    return 0;
+}
+
+int orc_reduce_scatter_exact(int I, const int *island_sizes, const void *const *in, void *const *out,
+                             size_t n, int dtype, int op)
+{
+    int W = 0;
+    for (int i = 0; i < I; ++i)
+        W += island_sizes[i];
+    if (n % (size_t)W || (op == ORC_OP_AVG && !is_float_dt(dtype)))
+        return -2;
+    size_t m = n / (size_t)W;
+    for (int r = 0; r < W; ++r)
+        for (size_t j = 0; j < m; ++j)
+            store_acc(out[r], dtype, j, exact_total(I, island_sizes, in, dtype, op, (size_t)r * m + j));
+    return 0;
+}
+
+void orc_f32_to_f16_array(const float *x, size_t n, uint16_t *out)
+{
+    for (size_t j = 0; j < n; ++j)
+        out[j] = orc_f32_to_f16(x[j]);
+}

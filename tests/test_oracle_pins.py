@@ -553,3 +553,148 @@ def test_error_feedback_error_does_not_accumulate():
     bound = np.abs(res[0].astype(np.float64)) + np.abs(res[1].astype(np.float64)) + T * 4 * U * np.abs(acc_exact / T) * 4
     assert np.all(gap_ef <= bound + 1e-6)
     assert np.max(np.abs(acc_plain - acc_exact)) > 4 * np.max(gap_ef)
+
+
+# ------------------------------------------------ exact path: MAX/MIN, dtypes
+
+INT_DTS = [np.int8, np.uint8, np.int32, np.int64]
+
+
+def test_f16_conversions_match_numpy():
+    """float32 -> float16 rounding against numpy's correctly rounded cast
+    (strided sweep of all patterns plus every float16 midpoint and its
+    neighbours); float16 -> float32 widening over all 65536 patterns."""
+    bits = np.arange(0, 1 << 32, 8191, dtype=np.uint64).astype(np.uint32)
+    h = np.arange(0, 1 << 16, dtype=np.uint32)
+    f = h.astype(np.uint16).view(np.float16).astype(np.float32)
+    ok = np.isfinite(f)
+    mids = ((f[ok][:-1].astype(np.float64) + f[ok][1:].astype(np.float64)) / 2).astype(np.float32)
+    x = np.concatenate([bits.view(np.float32), mids, np.nextafter(mids, np.float32(np.inf)),
+                        np.nextafter(mids, np.float32(-np.inf))])
+    x = x[~np.isnan(x)]
+    ref = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(orc.f32_to_f16_array(x), ref)
+    for hv in range(0, 1 << 16, 7):
+        want = np.uint16(hv).view(np.float16).astype(np.float32)
+        got = orc.f16_to_f32(hv)
+        assert (np.isnan(want) and np.isnan(got)) or got == want
+
+
+@pytest.mark.parametrize("dt", INT_DTS)
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 3), (4, 4), (3,)])
+def test_integer_sum_wraps_modulo(dt, sizes):
+    rng = np.random.default_rng(101)
+    info = np.iinfo(dt)
+    W = sum(sizes)
+    xs = [rng.integers(info.min, info.max, 257, dtype=dt, endpoint=True) for _ in range(W)]
+    xs[0][:3] = [info.max, info.min, info.max]
+    bits = np.dtype(dt).itemsize * 8
+    exact = [sum(int(x[j]) for x in xs) for j in range(257)]
+    want = np.array([((v % (1 << bits)) if info.min == 0 else ((v + (1 << (bits - 1))) % (1 << bits) - (1 << (bits - 1))))
+                     for v in exact], dtype=dt)
+    for o in orc.all_reduce(xs, sizes, "sum"):
+        assert np.array_equal(o, want)
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64, np.float16, np.int8, np.uint8, np.int32, np.int64])
+@pytest.mark.parametrize("op,ref", [("max", np.max), ("min", np.min)])
+def test_max_min_match_numpy(dt, op, ref):
+    rng = np.random.default_rng(103)
+    W = 5
+    if np.issubdtype(dt, np.integer):
+        info = np.iinfo(dt)
+        xs = [rng.integers(info.min, info.max, 500, dtype=dt, endpoint=True) for _ in range(W)]
+    else:
+        xs = [(rng.standard_normal(500) * 100 + 1.0).astype(dt) for _ in range(W)]  # no zeros
+    want = ref(np.stack(xs), axis=0)
+    for sizes in ((2, 3), (5,), (1, 1, 1, 1, 1)):
+        for o in orc.all_reduce(xs, sizes, op):
+            assert np.array_equal(o, want)
+    bf = [wl.to_bf16_bits(x.astype(np.float32)) for x in xs] if not np.issubdtype(dt, np.integer) else None
+    if bf is not None and dt == np.float32:
+        want_bf = orc.bf16_bits_to_f32_array(np.stack(bf)).max(axis=0) if op == "max" else \
+            orc.bf16_bits_to_f32_array(np.stack(bf)).min(axis=0)
+        assert np.array_equal(orc.bf16_bits_to_f32_array(orc.all_reduce(bf, (2, 3), op)[0]), want_bf)
+
+
+def test_max_min_ties_keep_the_lower_rank():
+    a = np.array([-0.0, 0.0, -0.0], np.float32)
+    b = np.array([0.0, -0.0, -0.0], np.float32)
+    for op in ("max", "min"):
+        o = orc.all_reduce([a, b], (1, 1), op)[0]
+        assert np.array_equal(np.signbit(o), np.signbit(a))
+        o = orc.all_reduce([b, a], (2,), op)[0]
+        assert np.array_equal(np.signbit(o), np.signbit(b))
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float16])
+def test_float64_and_float16_sums(dt):
+    rng = np.random.default_rng(107)
+    sizes = (2, 2)
+    lim = 400 if dt == np.float16 else 2 ** 40
+    xs = [rng.integers(-lim, lim, 777).astype(dt) for _ in range(4)]
+    exact = np.sum([x.astype(np.int64) for x in xs], axis=0)
+    for o in orc.all_reduce(xs, sizes, "sum"):
+        assert np.array_equal(o.astype(np.int64), exact)
+    # AVG: the float32 (float16) or float64 quotient, rounded once to the dtype
+    xs = [rng.standard_normal(300).astype(dt) for _ in range(4)]
+    s = orc.all_reduce(xs, sizes, "sum")[0]
+    a = orc.all_reduce(xs, sizes, "avg")[0]
+    if dt == np.float64:
+        assert np.array_equal(a, s / 4.0)
+        ex = np.array([sum(Fraction(float(x[j])) for x in xs) for j in range(300)], dtype=object)
+        absx = np.sum([np.abs(x) for x in xs], axis=0)
+        assert all(abs(Fraction(float(s[j])) - ex[j]) <= 3 * 2.0 ** -53 * absx[j] for j in range(300))
+    else:
+        s32 = orc.island_sum([x.astype(np.float32) for x in xs[:2]]) + orc.island_sum(
+            [x.astype(np.float32) for x in xs[2:]])
+        assert np.array_equal(a, (s32 / np.float32(4)).astype(np.float16))
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float16, np.int32, np.uint8])
+@pytest.mark.parametrize("op", ["sum", "max", "min"])
+def test_exact_rs_then_ag_is_ar(dt, op):
+    rng = np.random.default_rng(109)
+    sizes = (2, 1, 1)
+    xs = [(rng.standard_normal(400) * 50).astype(dt) for _ in range(4)]
+    ag = orc.all_gather(orc.reduce_scatter(xs, sizes, op))
+    ar = orc.all_reduce(xs, sizes, op)
+    assert all(np.array_equal(g, r) for g, r in zip(ag, ar))
+
+
+def test_avg_refused_on_integers():
+    with pytest.raises(ValueError):
+        orc.all_reduce([np.zeros(4, np.int32)] * 2, (1, 1), "avg")
+
+
+def _f16_double_rounding_cases(rng, want, count=40):
+    """Random float16 triples (a, b, c) where float32 arithmetic followed by
+    one rounding to float16 differs from rounding the exact value once."""
+    found = []
+    while len(found) < count:
+        h = rng.integers(0, 1 << 16, (4096, 3)).astype(np.uint16)
+        v = h.view(np.float16).astype(np.float64)
+        ok = np.all(np.isfinite(v), axis=1)
+        for a, b, c in v[ok]:
+            exact = (a + b) + c  # exact in float64 for float16 inputs
+            f32 = (np.float32(a) + np.float32(b)) + np.float32(c)
+            if want == "sum" and np.float16(f32) != np.float16(exact) and np.isfinite(np.float16(f32)):
+                found.append((a, b, c))
+            if want == "avg":
+                q32 = np.float32(f32) / np.float32(3)
+                if np.float16(q32) != np.float16(exact / 3) and np.isfinite(np.float16(q32)):
+                    found.append((a, b, c))
+    return np.array(found[:count])
+
+
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_float16_accumulates_and_divides_in_float32(op):
+    """float16 buffers: the sum (and the AVG quotient) is formed in float32
+    and rounded once to float16, not formed exactly."""
+    rng = np.random.default_rng(113)
+    cases = _f16_double_rounding_cases(rng, op)
+    xs = [cases[:, q].astype(np.float16) for q in range(3)]
+    f32 = (xs[0].astype(np.float32) + xs[1].astype(np.float32)) + xs[2].astype(np.float32)
+    want = (f32 if op == "sum" else f32 / np.float32(3)).astype(np.float16)
+    for o in orc.all_reduce(xs, (3,), op):
+        assert np.array_equal(o.view(np.uint16), want.view(np.uint16))

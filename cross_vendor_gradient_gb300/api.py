@@ -9,10 +9,12 @@ import torch
 
 from . import binding as B
 
-_DTYPES = {torch.float32: B.GB_F32, torch.bfloat16: B.GB_BF16}
+_DTYPES = {torch.float32: B.GB_F32, torch.bfloat16: B.GB_BF16, torch.float16: B.GB_F16,
+           torch.float64: B.GB_F64, torch.int8: B.GB_I8, torch.uint8: B.GB_U8, torch.int32: B.GB_I32,
+           torch.int64: B.GB_I64}
 CODECS = {"none": B.GB_CODEC_NONE, "bf16": B.GB_CODEC_BF16, "e4m3": B.GB_CODEC_E4M3,
           "e5m2": B.GB_CODEC_E5M2}
-OPS = {"sum": B.GB_SUM, "avg": B.GB_AVG}
+OPS = {"sum": B.GB_SUM, "avg": B.GB_AVG, "max": B.GB_MAX, "min": B.GB_MIN}
 
 
 class GbError(RuntimeError):

@@ -25,8 +25,8 @@ GB_ERR_CONTEXT_FAILED = 9
 GB_ERR_NO_DEVICE = 10
 GB_ERR_TOO_LARGE = 11
 # gb_dtype / gb_op / gb_codec
-GB_F32, GB_BF16 = 0, 1
-GB_SUM, GB_AVG = 0, 1
+GB_F32, GB_BF16, GB_F16, GB_F64, GB_I8, GB_U8, GB_I32, GB_I64 = 0, 1, 2, 3, 4, 5, 6, 7
+GB_SUM, GB_AVG, GB_MAX, GB_MIN = 0, 1, 2, 3
 GB_CODEC_NONE, GB_CODEC_BF16, GB_CODEC_E4M3, GB_CODEC_E5M2 = 0, 1, 2, 3
 GB_MAX_RANKS = 64
 GB_MAX_ISLANDS = 8

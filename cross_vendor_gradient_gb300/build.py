@@ -15,7 +15,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgb.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_api.cu", "gb_noalloc.cu"]
+SOURCES = ["gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_kernels_exact.cu", "gb_api.cu", "gb_noalloc.cu"]
 HEADERS = [os.path.join(INCLUDE, "gb.h")] + [
     os.path.join(CSRC, f) for f in ("gb_device.cuh", "gb_kernels.cuh")]
 

@@ -106,7 +106,19 @@ gb_status fail(gb_ctx *c, gb_status s, const char *what, cudaError_t e = cudaSuc
     return s;
 }
 
-size_t elem_bytes(gb_dtype d) { return d == GB_F32 ? 4 : 2; }
+size_t elem_bytes(gb_dtype d) {
+    switch (d) {
+    case GB_F32: case GB_I32: return 4;
+    case GB_BF16: case GB_F16: return 2;
+    case GB_F64: case GB_I64: return 8;
+    default: return 1;
+    }
+}
+
+bool is_float_dtype(int d) { return d == GB_F32 || d == GB_BF16 || d == GB_F16 || d == GB_F64; }
+
+// MAX / MIN, and every dtype but float32 / bfloat16, take the exact path.
+bool is_exact(int dtype, int op) { return op == GB_MAX || op == GB_MIN || (dtype != GB_F32 && dtype != GB_BF16); }
 
 // The kernels move float32 data with 32-byte vector accesses.
 bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
@@ -118,12 +130,18 @@ gb_status check_ctx(gb_ctx *c) {
 }
 
 gb_status check_dtype(gb_ctx *c, int d) {
-    if (d != GB_F32 && d != GB_BF16) return set_msg(c, GB_ERR_UNSUPPORTED_DTYPE, "dtype %d", d);
+    if (d < GB_F32 || d > GB_I64) return set_msg(c, GB_ERR_UNSUPPORTED_DTYPE, "dtype %d", d);
+    return GB_OK;
+}
+
+// The codec path's phase-level calls take float32 / bfloat16 only.
+gb_status check_codec_dtype(gb_ctx *c, int d) {
+    if (d != GB_F32 && d != GB_BF16) return set_msg(c, GB_ERR_UNSUPPORTED_DTYPE, "dtype %d on the codec path", d);
     return GB_OK;
 }
 
 gb_status check_op(gb_ctx *c, int op) {
-    if (op != GB_SUM && op != GB_AVG) return set_msg(c, GB_ERR_UNSUPPORTED_OP, "op %d", op);
+    if (op < GB_SUM || op > GB_MIN) return set_msg(c, GB_ERR_UNSUPPORTED_OP, "op %d", op);
     return GB_OK;
 }
 
@@ -607,6 +625,86 @@ GraphEntry *new_graph_slot(gb_ctx *c) {
     return &g;
 }
 
+// The exact path: island fold -> payload (the dtype, or float32 sums of
+// 16-bit floats), one bridge hop on the caller's stream, fold of the
+// payloads in island order -> ranks.  Same staging layout as a one-chunk
+// Plan.
+gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype, gb_op op,
+                    cudaStream_t s, int rs) {
+    const int I = c->I, W = c->W;
+    const size_t P = n * gb::exact_payload_elem_bytes(dtype, op);
+    const size_t part = round_up(P, 256);
+    const int recv = I == 1 ? 0 : I == 2 ? 2 : I * I;
+    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(I + recv) * part));
+    if (I > 1) GB_TRY(grow_host(c, (size_t)I * part));
+    GB_TRY(begin(c, s));
+    const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
+    auto outbox = [&](int i) { return c->d_stage + (size_t)i * part; };
+    auto inbox = [&](int g, int j) {
+        unsigned char *base = c->d_stage + (size_t)I * part;
+        return I == 2 ? base + (size_t)j * part : base + ((size_t)g * I + j) * part;
+    };
+    GB_TRY(mark(c, mm, 0, s));
+    gb::ReduceEncodeArgs ra;
+    memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < W; ++r) ra.src[r] = in[r];
+    for (int i = 0; i < I; ++i) ra.payload[i] = outbox(i);
+    for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
+    ra.n_islands = I;
+    ra.n = n;
+    GB_TRY(check_launch(c, gb::launch_exact_reduce(ra, dtype, op, s), "island fold"));
+    GB_TRY(mark(c, mm, 1, s));
+    if (I > 1) {
+        if (c->inject == GB_INJECT_BRIDGE) {
+            c->inject = 0;
+            return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+        }
+        GB_TRY(mark(c, mm, 2, s));
+        GB_TRY(copy_async(c, c->h_stage, outbox(0), (size_t)(I - 1) * part + P, cudaMemcpyDeviceToHost, s));
+        if (I == 2) {
+            GB_TRY(copy_async(c, inbox(1, 0), c->h_stage, part + P, cudaMemcpyHostToDevice, s));
+        } else {
+            for (int g = 0; g < I; ++g) {
+                if (g > 0)
+                    GB_TRY(copy_async(c, inbox(g, 0), c->h_stage, (size_t)(g - 1) * part + P, cudaMemcpyHostToDevice, s));
+                if (g < I - 1)
+                    GB_TRY(copy_async(c, inbox(g, g + 1), c->h_stage + (size_t)(g + 1) * part,
+                                      (size_t)(I - g - 2) * part + P, cudaMemcpyHostToDevice, s));
+            }
+        }
+        GB_TRY(mark(c, mm, 3, s));
+    }
+    GB_TRY(mark(c, mm, 4, s));
+    gb::DecodeBcastArgs da;
+    memset(&da, 0, sizeof da);
+    for (int r = 0; r < W; ++r) {
+        da.dst[r] = out[r];
+        da.group_of_rank[r] = c->island_of[r];
+    }
+    for (int g = 0; g < I; ++g)
+        for (int j = 0; j < I; ++j)
+            da.payload[g][j] = (j == g) ? (const void *)outbox(j) : (const void *)inbox(g, j);
+    for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
+    da.n_groups = I;
+    da.n_src = I;
+    da.world = (float)W;
+    da.world_pow2 = (W & (W - 1)) == 0;
+    da.inv_world = 1.0f / (float)W;
+    da.n = n;
+    const uint64_t V = 16 / elem_bytes(dtype);
+    if (rs) {
+        da.rs = 1;
+        da.m = n / (uint64_t)W;
+        da.vec = (da.m % V) == 0;
+    } else {
+        da.vec = 1;
+    }
+    GB_TRY(check_launch(c, gb::launch_exact_combine(da, dtype, op, s), "fold + broadcast"));
+    GB_TRY(mark(c, mm, 5, s));
+    commit_marks(c, 1, I > 1);
+    return end(c, s);
+}
+
 // Reduce-bridge-broadcast over W rank buffers `in` (n elements).  rs == 0:
 // the total goes to out[r] (all n elements; out may equal in).  rs == 1:
 // out[r] receives slice r (n / W elements).  A pipelined in-place
@@ -614,6 +712,7 @@ GraphEntry *new_graph_slot(gb_ctx *c) {
 // buffers and shape (the first runs directly) and replayed afterwards.
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
                   gb_op op, gb_codec codec, int block, cudaStream_t s, int rs, float *const *res = nullptr) {
+    if (is_exact(dtype, op)) return run_exact(c, in, out, n, dtype, op, s, rs);
     const Plan p = make_plan(c, n, dtype, op, codec, block, rs);
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
     if (p.host_bytes) GB_TRY(grow_host(c, p.host_bytes));
@@ -671,6 +770,10 @@ gb_status check_collective(gb_ctx *c, size_t n, int dtype, int op, int codec, in
     GB_TRY(check_op(c, op));
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
+    if (op == GB_AVG && !is_float_dtype(dtype))
+        return set_msg(c, GB_ERR_UNSUPPORTED_OP, "AVG needs a floating dtype");
+    if ((dtype == GB_F16 || dtype == GB_F64) && (op == GB_SUM || op == GB_AVG) && codec != GB_CODEC_NONE)
+        return set_msg(c, GB_ERR_UNSUPPORTED_CODEC, "float16 / float64 are not compressed");
     return GB_OK;
 }
 
@@ -779,8 +882,12 @@ gb_status gb_reserve(gb_ctx *c, size_t n, gb_dtype dtype, gb_codec codec, int bl
     const Plan ar = make_plan(c, n, dtype, GB_SUM, codec, block, 0);
     const Plan rs = make_plan(c, n, dtype, GB_SUM, codec, block, 1);
     const size_t ag_host = (size_t)c->W * n * elem_bytes(dtype);
-    const size_t dev = ar.dev_bytes > rs.dev_bytes ? ar.dev_bytes : rs.dev_bytes;
+    size_t dev = ar.dev_bytes > rs.dev_bytes ? ar.dev_bytes : rs.dev_bytes;
     size_t host = ar.host_bytes > rs.host_bytes ? ar.host_bytes : rs.host_bytes;
+    const size_t ex_part = round_up(n * gb::exact_payload_elem_bytes(dtype, GB_SUM), 256);
+    const size_t ex_dev = (size_t)(c->I + (c->I == 1 ? 0 : c->I == 2 ? 2 : c->I * c->I)) * ex_part;
+    if (ex_dev > dev) dev = ex_dev;
+    if (c->I > 1 && (size_t)c->I * ex_part > host) host = (size_t)c->I * ex_part;
     if (ag_host > host) host = ag_host;
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, dev));
     GB_TRY(grow_host(c, host));
@@ -801,7 +908,7 @@ gb_status gb_island_reduce(gb_ctx *c, int island, const void *const *rank_bufs, 
     GB_TRY(check_ctx(c));
     if (island < 0 || island >= c->I) return set_msg(c, GB_ERR_INVALID_ARG, "island %d", island);
     const int K = c->size[island];
-    GB_TRY(check_dtype(c, dtype));
+    GB_TRY(check_codec_dtype(c, dtype));
     GB_TRY(check_n(c, n));
     GB_TRY(check_dev_bufs(c, rank_bufs, K, "rank_bufs"));
     GB_TRY(check_dev_ptr(c, island_sum, "island_sum"));
@@ -870,8 +977,8 @@ gb_status gb_island_broadcast(gb_ctx *c, int island, const float *total, size_t 
     GB_TRY(check_ctx(c));
     if (island < 0 || island >= c->I) return set_msg(c, GB_ERR_INVALID_ARG, "island %d", island);
     const int K = c->size[island];
-    GB_TRY(check_dtype(c, dtype));
-    GB_TRY(check_op(c, op));
+    GB_TRY(check_codec_dtype(c, dtype));
+    if (op != GB_SUM && op != GB_AVG) return set_msg(c, GB_ERR_UNSUPPORTED_OP, "island broadcast takes SUM / AVG");
     GB_TRY(check_n(c, n));
     GB_TRY(check_dev_ptr(c, total, "total"));
     GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, K, "rank_bufs"));

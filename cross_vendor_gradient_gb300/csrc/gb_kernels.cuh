@@ -87,6 +87,15 @@ cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, 
                                          cudaStream_t s);
 cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s);
 
+// The exact path (MAX / MIN, float16, float64, integers): island fold into
+// payload[i] (ReduceEncodeArgs: src, payload, first, n_islands, n), then the
+// fold of the payloads into the ranks (DecodeBcastArgs as for decode; vec:
+// 16-byte accesses allowed, i.e. for reduce_scatter m is a multiple of
+// 16 / sizeof(dtype)).
+cudaError_t launch_exact_reduce(const ReduceEncodeArgs &a, int dtype, int op, cudaStream_t s);
+cudaError_t launch_exact_combine(const DecodeBcastArgs &a, int dtype, int op, cudaStream_t s);
+size_t exact_payload_elem_bytes(int dtype, int op);
+
 uint64_t launches();
 void count_launch();
 int sm_count();

@@ -1,0 +1,285 @@
+// The exact path (sm_103a): MAX / MIN for every dtype, and SUM / AVG for the
+// float16, float64 and integer dtypes (gpubridge README, API table and
+// supported-dtype list; "Bridge compression": MAX/MIN and integer dtypes
+// stay exact).  Same reduce-bridge-broadcast shape as the codec path:
+//   k_exact_reduce   island fold (ascending rank) -> payload
+//   k_exact_combine  fold of the I payloads (island order), AVG, -> ranks
+// Arithmetic: float16 / bfloat16 / float32 fold in float32 (payload float32
+// for SUM / AVG, the dtype itself for MAX / MIN, whose result is always one
+// of the inputs); float64 in float64; integers wrap modulo 2^bits for SUM.
+// MAX keeps the earlier value unless a later one is strictly greater (MIN:
+// strictly less).  Each thread moves 16 bytes of rank data per step.
+#include <cstring>
+#include <type_traits>
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "gb_device.cuh"
+#include "gb_kernels.cuh"
+
+namespace gb {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------- dtype traits
+template <typename T> struct Ex;  // A: fold arithmetic type
+template <> struct Ex<float> {
+    using A = float;
+    __device__ static A widen(float x) { return x; }
+    __device__ static float narrow(A a) { return a; }
+};
+template <> struct Ex<bf16> {
+    using A = float;
+    __device__ static A widen(bf16 x) { return __bfloat162float(x); }
+    __device__ static bf16 narrow(A a) { return __float2bfloat16_rn(a); }
+};
+template <> struct Ex<__half> {
+    using A = float;
+    __device__ static A widen(__half x) { return __half2float(x); }
+    __device__ static __half narrow(A a) { return __float2half_rn(a); }
+};
+template <> struct Ex<double> {
+    using A = double;
+    __device__ static A widen(double x) { return x; }
+    __device__ static double narrow(A a) { return a; }
+};
+template <typename I> struct ExInt {
+    using A = I;
+    __device__ static A widen(I x) { return x; }
+    __device__ static I narrow(A a) { return a; }
+};
+template <> struct Ex<int8_t> : ExInt<int8_t> {};
+template <> struct Ex<uint8_t> : ExInt<uint8_t> {};
+template <> struct Ex<int32_t> : ExInt<int32_t> {};
+template <> struct Ex<int64_t> : ExInt<int64_t> {};
+
+template <typename A>
+__device__ __forceinline__ A add_(A a, A b) {
+    if constexpr (std::is_same<A, float>::value) return __fadd_rn(a, b);
+    else if constexpr (std::is_same<A, double>::value) return __dadd_rn(a, b);
+    else {  // integers: two's complement wrap-around
+        using U = typename std::make_unsigned<A>::type;
+        return (A)(U)((U)a + (U)b);
+    }
+}
+
+template <int OP, typename A>
+__device__ __forceinline__ A fold(A a, A b) {
+    if constexpr (OP == GB_MAX) return b > a ? b : a;
+    else if constexpr (OP == GB_MIN) return b < a ? b : a;
+    else return add_(a, b);
+}
+
+// Payload element: float32 island sums for 16-bit floats (SUM / AVG), the
+// dtype itself otherwise.
+template <typename T, int OP>
+using PayloadT = typename std::conditional<(OP == GB_SUM || OP == GB_AVG) && sizeof(T) == 2 &&
+                                               !std::is_integral<T>::value,
+                                           float, T>::type;
+
+template <typename T, int OP>
+__device__ __forceinline__ typename Ex<T>::A to_acc(PayloadT<T, OP> p) {
+    if constexpr (std::is_same<PayloadT<T, OP>, float>::value && !std::is_same<T, float>::value) return p;
+    else return Ex<T>::widen(p);
+}
+template <typename T, int OP>
+__device__ __forceinline__ PayloadT<T, OP> to_payload(typename Ex<T>::A a) {
+    if constexpr (std::is_same<PayloadT<T, OP>, float>::value && !std::is_same<T, float>::value) return a;
+    else return Ex<T>::narrow(a);
+}
+
+// 16 bytes of T per thread step.
+template <typename T> struct V16 {
+    static constexpr int N = 16 / sizeof(T);
+    T v[N];
+};
+
+template <typename T>
+__device__ __forceinline__ V16<T> load16(const T *p) {
+    const uint4 u = ld_u4(p);
+    V16<T> r;
+    memcpy(&r, &u, 16);
+    return r;
+}
+
+// --------------------------------------------------------------- kernels
+template <typename T, int OP>
+__global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ ReduceEncodeArgs a) {
+    using A = typename Ex<T>::A;
+    using P = PayloadT<T, OP>;
+    constexpr int N = V16<T>::N;
+    const int isl = blockIdx.y;
+    const int r0 = a.first[isl];
+    const int K = a.first[isl + 1] - r0;
+    P *out = (P *)a.payload[isl];
+    const uint64_t nvec = (a.n + N - 1) / N;
+    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; vi < nvec;
+         vi += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t j0 = vi * N;
+        const int cnt = (a.n - j0) < (uint64_t)N ? (int)(a.n - j0) : N;
+        A s[N];
+        if (cnt == N) {
+            const V16<T> x = load16((const T *)a.src[r0] + j0);
+#pragma unroll
+            for (int k = 0; k < N; ++k) s[k] = Ex<T>::widen(x.v[k]);
+            for (int q = 1; q < K; ++q) {
+                const V16<T> y = load16((const T *)a.src[r0 + q] + j0);
+#pragma unroll
+                for (int k = 0; k < N; ++k) s[k] = fold<OP>(s[k], Ex<T>::widen(y.v[k]));
+            }
+            P o[N];
+#pragma unroll
+            for (int k = 0; k < N; ++k) o[k] = to_payload<T, OP>(s[k]);
+            uint4 w[sizeof(P) * N / 16];
+            memcpy(w, o, sizeof o);
+#pragma unroll
+            for (int i = 0; i < (int)(sizeof(P) * N / 16); ++i) st_u4((unsigned char *)(out + j0) + 16 * i, w[i]);
+        } else {
+            for (int k = 0; k < cnt; ++k) {
+                A v = Ex<T>::widen(((const T *)a.src[r0])[j0 + k]);
+                for (int q = 1; q < K; ++q) v = fold<OP>(v, Ex<T>::widen(((const T *)a.src[r0 + q])[j0 + k]));
+                out[j0 + k] = to_payload<T, OP>(v);
+            }
+        }
+    }
+}
+
+template <typename T, int OP>
+__global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ DecodeBcastArgs a) {
+    using A = typename Ex<T>::A;
+    using P = PayloadT<T, OP>;
+    constexpr int N = V16<T>::N;
+    const int u = blockIdx.y;
+    int g, r_lo, r_hi;
+    uint64_t gofs, limit;
+    if (a.rs) {
+        g = a.group_of_rank[u];
+        r_lo = u;
+        r_hi = u + 1;
+        gofs = (uint64_t)u * a.m;
+        limit = a.m;
+    } else {
+        g = u;
+        r_lo = a.first[g];
+        r_hi = a.first[g + 1];
+        gofs = 0;
+        limit = a.n;
+    }
+    const uint64_t nvec = (limit + N - 1) / N;
+    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; vi < nvec;
+         vi += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t l0 = vi * N;
+        const int cnt = (limit - l0) < (uint64_t)N ? (int)(limit - l0) : N;
+        A t[N];
+        const bool full = a.vec && cnt == N;
+        for (int j = 0; j < a.n_src; ++j) {
+            const P *p = (const P *)a.payload[g][j] + gofs + l0;
+            P x[N];
+            if (full) {
+                uint4 w[sizeof(P) * N / 16];
+#pragma unroll
+                for (int i = 0; i < (int)(sizeof(P) * N / 16); ++i) w[i] = ld_u4((const unsigned char *)p + 16 * i);
+                memcpy(x, w, sizeof x);
+            } else {
+                for (int k = 0; k < cnt; ++k) x[k] = p[k];
+            }
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                const A v = to_acc<T, OP>(x[k]);
+                t[k] = (j == 0) ? v : fold<OP>(t[k], v);
+            }
+        }
+        if constexpr (OP == GB_AVG) {
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                if constexpr (sizeof(A) == 8)
+                    t[k] = __ddiv_rn(t[k], (double)a.world);
+                else
+                    t[k] = a.world_pow2 ? __fmul_rn(t[k], a.inv_world) : __fdiv_rn(t[k], a.world);
+            }
+        }
+        T o[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) o[k] = Ex<T>::narrow(t[k]);
+        for (int r = r_lo; r < r_hi; ++r) {
+            T *d = (T *)a.dst[r] + l0;
+            if (full) {
+                uint4 w;
+                memcpy(&w, o, 16);
+                st_stream_u4(d, w);
+            } else {
+                for (int k = 0; k < cnt; ++k) d[k] = o[k];
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launch
+template <auto Kern, typename Args>
+static cudaError_t launch_vec(uint64_t vec_items, unsigned units, const Args &a, cudaStream_t s) {
+    // launch_grid sizes in units of 8 warps per block: one vector per thread
+    return launch_grid<Kern>((vec_items + 31) / 32, units, a, s);
+}
+
+template <typename T, int OP>
+static cudaError_t launch_pair(bool combine, const void *args, cudaStream_t s) {
+    constexpr int N = V16<T>::N;
+    if (!combine) {
+        const ReduceEncodeArgs &a = *(const ReduceEncodeArgs *)args;
+        return launch_vec<k_exact_reduce<T, OP>>((a.n + N - 1) / N, (unsigned)a.n_islands, a, s);
+    }
+    const DecodeBcastArgs &a = *(const DecodeBcastArgs *)args;
+    const uint64_t limit = a.rs ? a.m : a.n;
+    const unsigned units = a.rs ? (unsigned)a.first[a.n_groups] : (unsigned)a.n_groups;
+    return launch_vec<k_exact_combine<T, OP>>((limit + N - 1) / N, units, a, s);
+}
+
+template <typename T>
+static cudaError_t by_op(int op, bool combine, const void *args, cudaStream_t s) {
+    switch (op) {
+    case GB_SUM: return launch_pair<T, GB_SUM>(combine, args, s);
+    case GB_MAX: return launch_pair<T, GB_MAX>(combine, args, s);
+    case GB_MIN: return launch_pair<T, GB_MIN>(combine, args, s);
+    case GB_AVG:
+        if constexpr (std::is_integral<T>::value) return cudaErrorInvalidValue;
+        else return launch_pair<T, GB_AVG>(combine, args, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+static cudaError_t by_dtype(int dtype, int op, bool combine, const void *args, cudaStream_t s) {
+    switch (dtype) {
+    case GB_F32: return by_op<float>(op, combine, args, s);
+    case GB_BF16: return by_op<bf16>(op, combine, args, s);
+    case GB_F16: return by_op<__half>(op, combine, args, s);
+    case GB_F64: return by_op<double>(op, combine, args, s);
+    case GB_I8: return by_op<int8_t>(op, combine, args, s);
+    case GB_U8: return by_op<uint8_t>(op, combine, args, s);
+    case GB_I32: return by_op<int32_t>(op, combine, args, s);
+    case GB_I64: return by_op<int64_t>(op, combine, args, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_exact_reduce(const ReduceEncodeArgs &a, int dtype, int op, cudaStream_t s) {
+    return by_dtype(dtype, op, false, &a, s);
+}
+
+cudaError_t launch_exact_combine(const DecodeBcastArgs &a, int dtype, int op, cudaStream_t s) {
+    return by_dtype(dtype, op, true, &a, s);
+}
+
+size_t exact_payload_elem_bytes(int dtype, int op) {
+    const bool small_float = dtype == GB_BF16 || dtype == GB_F16;
+    if (small_float && (op == GB_SUM || op == GB_AVG)) return 4;
+    switch (dtype) {
+    case GB_F32: case GB_I32: return 4;
+    case GB_BF16: case GB_F16: return 2;
+    case GB_F64: case GB_I64: return 8;
+    default: return 1;
+    }
+}
+
+}  // namespace gb

@@ -72,11 +72,32 @@ typedef enum {
     GB_ERR_TOO_LARGE = 11         /* exceeds the fixed buffers of gb_all_reduce_noalloc   */
 } gb_status;
 
-typedef enum { GB_F32 = 0, GB_BF16 = 1 } gb_dtype;
+/* Rank-buffer element types (gpubridge README: float16, bfloat16, float32,
+ * float64, int8, uint8, int32, int64; bool is excluded).  float32 and
+ * bfloat16 SUM / AVG take the codec path; everything else (MAX / MIN, and
+ * the other dtypes) takes the exact path: no compression, float16 /
+ * bfloat16 fold in float32 and round once, float64 folds in float64,
+ * integer SUM wraps modulo 2^bits. */
+typedef enum {
+    GB_F32 = 0,
+    GB_BF16 = 1,
+    GB_F16 = 2,
+    GB_F64 = 3,
+    GB_I8 = 4,
+    GB_U8 = 5,
+    GB_I32 = 6,
+    GB_I64 = 7
+} gb_dtype;
 
-/* gpubridge README, API table, all_reduce row: SUM, or AVG = the SUM divided
- * by the world size, identically on every rank (floating dtypes only). */
-typedef enum { GB_SUM = 0, GB_AVG = 1 } gb_op;
+/* gpubridge README, API table, all_reduce row: SUM; AVG = the SUM divided
+ * by the world size, identically on every rank (floating dtypes only,
+ * GB_ERR_UNSUPPORTED_OP otherwise); MAX and MIN (among equal values, +0 and
+ * -0, the lower rank's value is kept; NaN inputs are outside the contract).
+ * PRODUCT is not supported.  Compression applies to float32 / bfloat16 SUM
+ * and AVG only: MAX / MIN and integer dtypes stay exact whatever the codec
+ * argument (the README's rule), and float16 / float64 SUM / AVG accept
+ * GB_CODEC_NONE only (GB_ERR_UNSUPPORTED_CODEC otherwise). */
+typedef enum { GB_SUM = 0, GB_AVG = 1, GB_MAX = 2, GB_MIN = 3 } gb_op;
 
 /* gpubridge README, "Bridge compression".
  *   GB_CODEC_NONE: the payload is the float32 island sum (4n bytes).
@@ -183,7 +204,8 @@ gb_status gb_island_reduce(gb_ctx *ctx, int island, const void *const *rank_bufs
 
 /* Encode n float32 values (device) into `payload` (device, 32-byte aligned,
  * gb_payload_bytes(codec, block, n) bytes, laid out as described above).
- * block is ignored for none / bf16. */
+ * block is ignored for none / bf16.  The phase-level calls cover the codec
+ * path: float32 / bfloat16 rank buffers, SUM / AVG. */
 gb_status gb_bridge_compress(gb_ctx *ctx, const float *island_sum, size_t n, gb_codec codec,
                              int block, void *payload, gb_stream stream);
 
@@ -331,8 +353,9 @@ gb_status gb_debug_inject(gb_ctx *ctx, int what);
  * Limits: with I islands and P = gb_payload_bytes(codec, block, n) (the
  * float32 sum, 4n, when I == 1), I * I * round_up(P, 256) must fit the
  * device array and I * round_up(P, 256) the host array; larger calls return
- * GB_ERR_TOO_LARGE with nothing enqueued.  Other arguments are checked as in
- * gb_all_reduce.
+ * GB_ERR_TOO_LARGE with nothing enqueued.  It covers the codec path only
+ * (float32 / bfloat16 rank buffers, SUM / AVG); other arguments are checked
+ * as in gb_all_reduce.
  * Sharing: every call in the process uses the same two arrays, which keep
  * the last call's contents; nothing in them needs to start at zero (each
  * call reads only what it wrote).  Calls that overlap on the GPU -- from

@@ -10,9 +10,7 @@ def to_dev(x: np.ndarray, device="cuda") -> torch.Tensor:
         return torch.from_numpy(x.copy()).to(device)
     if x.dtype == np.uint16:
         return torch.from_numpy(x.view(np.int16).copy()).to(device).view(torch.bfloat16)
-    if x.dtype == np.uint8:
-        return torch.from_numpy(x.copy()).to(device)
-    raise TypeError(x.dtype)
+    return torch.from_numpy(x.copy()).to(device)
 
 
 def to_host(t: torch.Tensor) -> np.ndarray:
@@ -25,7 +23,7 @@ def to_host(t: torch.Tensor) -> np.ndarray:
 
 
 def bits(a: np.ndarray) -> np.ndarray:
-    return a.view({4: np.uint32, 2: np.uint16, 1: np.uint8}[a.itemsize])
+    return a.view({8: np.uint64, 4: np.uint32, 2: np.uint16, 1: np.uint8}[a.itemsize])
 
 
 def assert_bits_equal(got: np.ndarray, want: np.ndarray, what=""):

@@ -114,8 +114,12 @@ def test_argument_errors_need_no_device():
     fake = [0x10000 * (r + 1) for r in range(4)]
     try:
         assert B.gb_all_reduce(0, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
-        assert B.gb_all_reduce(ctx, fake, 10, 7, 0, 0, 256) == B.GB_ERR_UNSUPPORTED_DTYPE
-        assert B.gb_all_reduce(ctx, fake, 10, 0, 2, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_all_reduce(ctx, fake, 10, 9, 0, 0, 256) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert B.gb_all_reduce(ctx, fake, 10, 0, 5, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_all_reduce(ctx, fake, 10, B.GB_I32, B.GB_AVG, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_all_reduce(ctx, fake, 10, B.GB_F64, B.GB_SUM, 2, 256) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_island_reduce(ctx, 0, fake, 10, B.GB_F64, fake[0]) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert B.gb_island_broadcast(ctx, 0, fake[0], 10, B.GB_MAX, fake, B.GB_F32) == B.GB_ERR_UNSUPPORTED_OP
         assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 2, 64) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 5, 256) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_all_reduce(ctx, fake[:3] + [0], 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG

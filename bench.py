@@ -45,6 +45,8 @@ def parse():
     p.add_argument("--impl", choices=["gb", "reference"], default="gb")
     p.add_argument("--workload", default="c2")
     p.add_argument("--codec", default=None)
+    p.add_argument("--dtype", default=None, help="rank dtype override (f32 bf16 f16 f64 i8 u8 i32 i64)")
+    p.add_argument("--op", default=None, help="op override (sum avg max min)")
     p.add_argument("--n", type=int, default=None, help="override elements per rank")
     p.add_argument("--chunk-kib", type=int, default=None,
                    help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
@@ -181,6 +183,12 @@ def alg_bytes(W, I, n, b, P, I2=True):
     return W * n * b + I * P, I * I * P + W * n * b
 
 
+def dataclasses_replace_f32(w):
+    """The workload drawn as float32 (the draw's own type)."""
+    import dataclasses
+    return dataclasses.replace(w, dtype="f32")
+
+
 def run_gb(args, world, rank, local, pg):
     import torch
     from cross_vendor_gradient_gb300 import Context, kernel_launch_count, payload_bytes
@@ -191,17 +199,23 @@ def run_gb(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
-    codec = args.codec or w.codecs[0]
+    if args.dtype or args.op:
+        import dataclasses
+        w = dataclasses.replace(w, dtype=args.dtype or w.dtype, op=args.op or w.op)
+    exact = w.op in ("max", "min") or w.dtype not in ("f32", "bf16")
+    codec = "none" if exact else (args.codec or w.codecs[0])
     n = args.n or w.n
     W, I = w.world_size, len(w.island_sizes)
-    b = w.elem_bytes
-    xs = wl.host_rank_inputs(w, n=n)
-    tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    xs = wl.host_rank_inputs(dataclasses_replace_f32(w), n=n)
+    xs = [wl.as_dtype(x, w.dtype) for x in xs]
+    b = xs[0].itemsize
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "f64": torch.float64,
+           "i8": torch.int8, "u8": torch.uint8, "i32": torch.int32, "i64": torch.int64}[w.dtype]
 
     def dev_tensor(x):
-        if x.dtype == np.float32:
-            return torch.from_numpy(x).to(dev)
-        return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        if x.dtype == np.uint16:
+            return torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(x).to(dev)
 
     pristine = [dev_tensor(x) for x in xs]
     bufs = [p.clone() for p in pristine]
@@ -291,11 +305,17 @@ def run_gb(args, world, rank, local, pg):
     ctx.set_phase_timing(0)
     ctx.set_pipeline(chunk_bytes, not args.no_graphs)
 
-    P = payload_bytes(codec, w.block, n) if I > 1 else 4 * n
+    if exact:
+        pe = 4 if (w.dtype in ("bf16", "f16") and w.op in ("sum", "avg")) else b
+        P = pe * n
+        names = ("k_exact_reduce", "k_exact_combine")
+    else:
+        P = payload_bytes(codec, w.block, n) if I > 1 else 4 * n
+        names = ("k_reduce_encode", "k_decode_bcast")
     k1_ms, bridge_ms, k2_ms = (float(np.mean(phases[:, j])) for j in range(3))
     k1_bytes, k2_bytes = alg_bytes(W, I, n, b, P)
     peak, peak_kind = measured_peaks()
-    dom = ("k_reduce_encode", k1_bytes, k1_ms) if k1_ms >= k2_ms else ("k_decode_bcast", k2_bytes, k2_ms)
+    dom = (names[0], k1_bytes, k1_ms) if k1_ms >= k2_ms else (names[1], k2_bytes, k2_ms)
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
     link_bytes = I * P + I * (I - 1) * P
     link_peak = min(link["d2h_gbs"], link["h2d_gbs"])
@@ -340,11 +360,11 @@ def run_gb(args, world, rank, local, pg):
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "alg_bytes_per_launch": dom[1], "avg_launch_ms": dom[2], "traffic": None},
-        "kernels_ms": {"k_reduce_encode": k1_ms, "bridge_hop": bridge_ms, "k_decode_bcast": k2_ms,
+        "kernels_ms": {names[0]: k1_ms, "bridge_hop": bridge_ms, names[1]: k2_ms,
                        "region": "timed region 2: one bridge hop per call, CUDA events around each phase",
                        "step_ms_with_marks": plain_ms},
-        "kernels_hbm_frac": {"k_reduce_encode": k1_bytes / (k1_ms * 1e-3) / 1e9 / peak,
-                             "k_decode_bcast": k2_bytes / (k2_ms * 1e-3) / 1e9 / peak},
+        "kernels_hbm_frac": {names[0]: k1_bytes / (k1_ms * 1e-3) / 1e9 / peak,
+                             names[1]: k2_bytes / (k2_ms * 1e-3) / 1e9 / peak},
         "bridge": {"bytes_per_step": link_bytes, "ms": bridge_ms,
                    "achieved_gbs": link_bytes / (bridge_ms * 1e-3) / 1e9 if bridge_ms > 0 else None,
                    "pinned_copy_gbs": link, "frac": (link_bytes / (bridge_ms * 1e-3) / 1e9) / link_peak

@@ -22,9 +22,9 @@ class Workload:
     key: str                 # short name
     cid: int                 # seed base: rank r uses seed 1000 * cid + r
     island_sizes: tuple      # contiguous islands of simulated ranks
-    dtype: str               # "f32" or "bf16": rank-buffer element type
+    dtype: str               # rank-buffer element type: f32 bf16 f16 f64 i8 u8 i32 i64
     dist: str                # value distribution, see draw_host / draw_device
-    op: str                  # "sum" or "avg"
+    op: str                  # "sum", "avg", "max" or "min"
     codecs: tuple            # bridge codecs exercised
     block: int = 256         # fp8 scale block
     n: int = 0               # elements per rank buffer (single-buffer workloads)
@@ -36,7 +36,7 @@ class Workload:
 
     @property
     def elem_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        return {"f32": 4, "bf16": 2, "f16": 2, "f64": 8, "i8": 1, "u8": 1, "i32": 4, "i64": 8}[self.dtype]
 
 
 def gpt2_small_shapes():
@@ -177,3 +177,23 @@ def draw_device(dist: str, n: int, seed: int, device, dtype):
     else:
         raise ValueError("unknown distribution %r" % dist)
     return x.to(dtype)
+
+
+DTYPE_NAMES = ("f32", "bf16", "f16", "f64", "i8", "u8", "i32", "i64")
+
+
+def as_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Input preparation only: float32 draws as another rank dtype
+    (bf16 patterns via torch's cast; integers: x * 1000 rounded and clipped
+    to the type's range)."""
+    if dtype == "f32":
+        return x
+    if dtype == "bf16":
+        return to_bf16_bits(x)
+    if dtype == "f16":
+        return x.astype(np.float16)
+    if dtype == "f64":
+        return x.astype(np.float64)
+    npdt = {"i8": np.int8, "u8": np.uint8, "i32": np.int32, "i64": np.int64}[dtype]
+    info = np.iinfo(npdt)
+    return np.clip(np.round(x.astype(np.float64) * 1000.0), info.min, info.max).astype(npdt)

@@ -26,6 +26,7 @@ constexpr int kMaxGraphs = 16;
 // Identity of a captured all_reduce (every value its graph bakes in).
 struct GraphKey {
     const void *in[GB_MAX_RANKS];
+    const void *host[GB_MAX_RANKS];  // gb_all_reduce_host: the host rank buffers
     const void *res[GB_MAX_ISLANDS];
     uint64_t n, chunk;
     int dtype, op, codec, block, timed, pad;
@@ -69,6 +70,7 @@ struct gb_ctx {
     int use_graphs = 1;
     cudaStream_t sd = nullptr, sh = nullptr, scap = nullptr;
     cudaEvent_t ev_k1[kMaxChunks] = {}, ev_d2h[kMaxChunks] = {}, ev_h2d[kMaxChunks] = {};
+    cudaEvent_t ev_in[kMaxChunks] = {}, ev_k2[kMaxChunks] = {};  // host-buffer pipeline
     cudaEvent_t ev_join_d = nullptr, ev_join_h = nullptr;
     cudaEvent_t cap_mark[kMarks] = {};  // stand-ins recorded while capturing
     GraphEntry graphs[kMaxGraphs];
@@ -204,7 +206,7 @@ gb_status bind(gb_ctx *c) {
             if ((e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking)) != cudaSuccess)
                 return fail(c, GB_ERR_CUDA, "cudaStreamCreate", e);
         for (int i = 0; i < kMaxChunks; ++i) {
-            cudaEvent_t *evs[3] = {&c->ev_k1[i], &c->ev_d2h[i], &c->ev_h2d[i]};
+            cudaEvent_t *evs[5] = {&c->ev_k1[i], &c->ev_d2h[i], &c->ev_h2d[i], &c->ev_in[i], &c->ev_k2[i]};
             for (cudaEvent_t *ev : evs)
                 if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess)
                     return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
@@ -563,6 +565,125 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
     return GB_OK;
 }
 
+// gb_all_reduce_host, pipelined: chunk c of every host rank buffer goes to
+// the device (copy stream H), is encoded (s), its payload crosses the
+// bridge (D, then H), is decoded into the device rank chunks (s) and copied
+// back to the host buffers (D).  Issued one chunk ahead so that both copy
+// directions stay busy: H carries in(0), in(1), bridge-in(0), in(2), ...; D
+// carries bridge-out(0), bridge-out(1), out(0), bridge-out(2), out(1), ...
+gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, cudaStream_t s) {
+    const int I = p.I, W = p.W;
+    auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
+    auto inbox = [&](int g, int ch, int j) {
+        unsigned char *base = c->d_stage + (size_t)I * p.C * p.part;
+        if (I == 2) return base + ((size_t)ch * I + j) * p.part;
+        return base + (((size_t)g * p.C + ch) * I + j) * p.part;
+    };
+    auto hslot = [&](int ch, int j) { return c->h_stage + ((size_t)ch * I + j) * p.part; };
+    auto range = [&](int ch, uint64_t *e0, uint64_t *m) {
+        *e0 = (uint64_t)ch * p.chunk;
+        *m = (p.n - *e0) < p.chunk ? (p.n - *e0) : p.chunk;
+    };
+    cudaStream_t D = c->sd, H = c->sh;
+    if (c->inject == GB_INJECT_BRIDGE) {
+        c->inject = 0;
+        return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+    }
+    GB_TRY(record(c, c->ev_join_d, s));  // the copy streams start after the caller's prior work
+    GB_TRY(wait_on(c, H, c->ev_join_d));
+    GB_TRY(wait_on(c, D, c->ev_join_d));
+    auto issue_front = [&](int ch) -> gb_status {  // in(ch), encode(ch), bridge-out(ch)
+        uint64_t e0, m;
+        range(ch, &e0, &m);
+        for (int r = 0; r < W; ++r) {
+            cudaError_t e = cudaMemcpyAsync((unsigned char *)dev[r] + e0 * p.eb, (const unsigned char *)host[r] + e0 * p.eb,
+                                            m * p.eb, cudaMemcpyHostToDevice, H);
+            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "host -> device staging", e);
+        }
+        GB_TRY(record(c, c->ev_in[ch], H));
+        GB_TRY(wait_on(c, s, c->ev_in[ch]));
+        gb::ReduceEncodeArgs ra;
+        memset(&ra, 0, sizeof ra);
+        for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)dev[r] + e0 * p.eb;
+        for (int i = 0; i < I; ++i) ra.payload[i] = outbox(ch, i);
+        for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
+        ra.n_islands = I;
+        ra.n = m;
+        ra.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
+        ra.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
+        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        GB_TRY(record(c, c->ev_k1[ch], s));
+        if (I > 1) {
+            GB_TRY(wait_on(c, D, c->ev_k1[ch]));
+            GB_TRY(copy_async(c, hslot(ch, 0), outbox(ch, 0), (size_t)(I - 1) * p.part + part_bytes(p, m),
+                              cudaMemcpyDeviceToHost, D));
+            GB_TRY(record(c, c->ev_d2h[ch], D));
+        }
+        return GB_OK;
+    };
+    auto issue_back = [&](int ch) -> gb_status {  // bridge-in(ch), decode(ch), out(ch)
+        uint64_t e0, m;
+        range(ch, &e0, &m);
+        const size_t pb = part_bytes(p, m);
+        if (I > 1) {
+            GB_TRY(wait_on(c, H, c->ev_d2h[ch]));
+            if (I == 2) {
+                GB_TRY(copy_async(c, inbox(1, ch, 0), hslot(ch, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+            } else {
+                for (int g = 0; g < I; ++g) {
+                    if (g > 0)
+                        GB_TRY(copy_async(c, inbox(g, ch, 0), hslot(ch, 0), (size_t)(g - 1) * p.part + pb,
+                                          cudaMemcpyHostToDevice, H));
+                    if (g < I - 1)
+                        GB_TRY(copy_async(c, inbox(g, ch, g + 1), hslot(ch, g + 1), (size_t)(I - g - 2) * p.part + pb,
+                                          cudaMemcpyHostToDevice, H));
+                }
+            }
+            GB_TRY(record(c, c->ev_h2d[ch], H));
+            GB_TRY(wait_on(c, s, c->ev_h2d[ch]));
+        }
+        gb::DecodeBcastArgs da;
+        memset(&da, 0, sizeof da);
+        for (int r = 0; r < W; ++r) {
+            da.dst[r] = (unsigned char *)dev[r] + e0 * p.eb;
+            da.group_of_rank[r] = c->island_of[r];
+        }
+        for (int g = 0; g < I; ++g)
+            for (int j = 0; j < I; ++j)
+                da.payload[g][j] = (j == g) ? (const void *)outbox(ch, j) : (const void *)inbox(g, ch, j);
+        for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
+        da.n_groups = I;
+        da.n_src = I;
+        da.avg = p.op == GB_AVG;
+        da.world = (float)W;
+        da.world_pow2 = (W & (W - 1)) == 0;
+        da.inv_world = 1.0f / (float)W;
+        da.n = m;
+        da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
+        da.vec = 1;
+        da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
+        GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        GB_TRY(record(c, c->ev_k2[ch], s));
+        GB_TRY(wait_on(c, D, c->ev_k2[ch]));
+        for (int r = 0; r < W; ++r) {
+            cudaError_t e = cudaMemcpyAsync((unsigned char *)host[r] + e0 * p.eb, (const unsigned char *)dev[r] + e0 * p.eb,
+                                            m * p.eb, cudaMemcpyDeviceToHost, D);
+            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "device -> host copy back", e);
+        }
+        return GB_OK;
+    };
+    GB_TRY(issue_front(0));
+    for (int ch = 0; ch < p.C; ++ch) {
+        if (ch + 1 < p.C) GB_TRY(issue_front(ch + 1));
+        GB_TRY(issue_back(ch));
+    }
+    GB_TRY(record(c, c->ev_join_d, D));
+    GB_TRY(record(c, c->ev_join_h, H));
+    GB_TRY(wait_on(c, s, c->ev_join_d));
+    GB_TRY(wait_on(c, s, c->ev_join_h));
+    return GB_OK;
+}
+
 // Capture one pipelined all_reduce on the context's capture stream and
 // instantiate it.  The stand-in mark events become event-record nodes.
 gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, float *const *res, bool timed,
@@ -822,7 +943,7 @@ gb_status gb_destroy(gb_ctx *c) {
         for (cudaStream_t st : streams)
             if (st) cudaStreamDestroy(st);
         for (int i = 0; i < kMaxChunks; ++i) {
-            cudaEvent_t evs[3] = {c->ev_k1[i], c->ev_d2h[i], c->ev_h2d[i]};
+            cudaEvent_t evs[5] = {c->ev_k1[i], c->ev_d2h[i], c->ev_h2d[i], c->ev_in[i], c->ev_k2[i]};
             for (cudaEvent_t ev : evs)
                 if (ev) cudaEventDestroy(ev);
         }
@@ -1166,10 +1287,67 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
     const size_t nb = n * elem_bytes(dtype);
     const size_t stride = round_up(nb, 256);
     GB_TRY(grow_device(c, &c->d_ranks, &c->d_ranks_bytes, (size_t)c->W * stride));
-    GB_TRY(begin(c, s));
     void *dev[GB_MAX_RANKS];
+    for (int r = 0; r < c->W; ++r) dev[r] = c->d_ranks + (size_t)r * stride;
+    const Plan p = make_plan(c, n, dtype, op, codec, block, 0);
+    if (!is_exact(dtype, op) && p.C > 1 && c->tcap == 0) {
+        // pipelined: staging in, bridge and copy-back overlap chunk by chunk
+        GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
+        GB_TRY(grow_host(c, p.host_bytes));
+        GB_TRY(begin(c, s));
+        if (!c->use_graphs) {
+            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, s));
+            return end(c, s);
+        }
+        GraphKey k;
+        memset(&k, 0, sizeof k);
+        for (int r = 0; r < c->W; ++r) {
+            k.in[r] = dev[r];
+            k.host[r] = host_bufs[r];
+        }
+        k.n = n;
+        k.chunk = p.chunk;
+        k.dtype = dtype;
+        k.op = op;
+        k.codec = p.eff;
+        k.block = p.blk;
+        k.d_stage = c->d_stage;
+        k.h_stage = c->h_stage;
+        GraphEntry *ge = find_graph(c, k);
+        if (!ge) {  // first time: run directly, remember the shape
+            ge = new_graph_slot(c);
+            ge->key = k;
+            ge->last_use = ++c->clock;
+            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, s));
+            return end(c, s);
+        }
+        ge->last_use = ++c->clock;
+        if (!ge->exec) {
+            cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
+            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
+            gb_status st = enqueue_host_pipeline(c, p, host_bufs, dev, c->scap);
+            cudaGraph_t g = nullptr;
+            e = cudaStreamEndCapture(c->scap, &g);
+            if (st != GB_OK) {
+                if (g) cudaGraphDestroy(g);
+                return st;
+            }
+            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamEndCapture", e);
+            cudaGraphExec_t x = nullptr;
+            if ((e = cudaGraphInstantiate(&x, g, 0)) != cudaSuccess) {
+                cudaGraphDestroy(g);
+                return fail(c, GB_ERR_CUDA, "cudaGraphInstantiate", e);
+            }
+            ge->graph = g;
+            ge->exec = x;
+        }
+        cudaError_t e = cudaGraphLaunch(ge->exec, s);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphLaunch", e);
+        for (int k2 = 0; k2 < 2 * p.C; ++k2) gb::count_launch();
+        return end(c, s);
+    }
+    GB_TRY(begin(c, s));
     for (int r = 0; r < c->W; ++r) {
-        dev[r] = c->d_ranks + (size_t)r * stride;
         cudaError_t e = cudaMemcpyAsync(dev[r], host_bufs[r], nb, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "host -> device staging", e);
     }

@@ -353,3 +353,32 @@ def test_error_feedback_matches_oracle_over_steps(codec, block, sizes, dtype, ch
                 assert_bits_equal(to_host(bufs[r]), want[r], "EF step %d rank %d" % (step, r))
             for i in range(I):
                 assert_bits_equal(to_host(res_d[i]), res_h[i], "EF step %d residual %d" % (step, i))
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (2, 1, 3)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_all_reduce_host_pipelined(codec, block, sizes, dtype):
+    """gb_all_reduce_host under the pipelined policy (staging, bridge and
+    copy-back chunk by chunk): the oracle's bits on three calls with the same
+    host buffers (direct, captured, replayed)."""
+    W = sum(sizes)
+    n = 256 * 97 + 5
+    xs = inputs(sizes, n, dtype, cid=61)
+    want = orc.all_reduce(xs, sizes, "avg", codec, block)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(2048, True)
+        host = [torch.from_numpy(x.view(np.int16) if dtype == "bf16" else x).clone().pin_memory() for x in xs]
+        if dtype == "bf16":
+            host = [h.view(torch.bfloat16) for h in host]
+        for call in range(3):
+            for h, x in zip(host, xs):
+                h.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) if dtype == "bf16"
+                        else torch.from_numpy(x))
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                ctx.all_reduce_host(host, "avg", codec, block)
+            s.synchronize()
+            for r in range(W):
+                got = host[r].view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else host[r].numpy()
+                assert_bits_equal(got, want[r], "host pipelined call %d rank %d" % (call, r))

@@ -409,6 +409,116 @@ def traffic_from_profiles(kernel):
     return None
 
 
+def run_buckets_bench(args, world, rank, local, pg):
+    """Bucketed workloads (c4: GPT-2 small, c5: 1.1B Llama-style): one step is
+    the all_reduce of the whole bf16 gradient set, fused into 25 MiB DDP
+    buckets, through gb_all_reduce_buckets (one pipeline, one graph)."""
+    import torch
+    from cross_vendor_gradient_gb300 import Context, bucket_plan, kernel_launch_count, payload_bytes
+    from cross_vendor_gradient_gb300 import workloads as wl
+    from cross_vendor_gradient_gb300 import build as gbuild
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    codec = args.codec or w.codecs[0]
+    W, I = w.world_size, len(w.island_sizes)
+    numels = [wl.numel(sh) for sh in w.tensors]
+    _, _, bn = bucket_plan(numels, w.elem_bytes, wl.BUCKET_CAP_BYTES, 1)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    pristine = [[wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 1000 * bi, dev, tdt) for r in range(W)]
+                for bi, nb in enumerate(bn)]
+    bufs = [[x.clone() for x in row] for row in pristine]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    K, Wm = args.steps, max(3, args.warmup)
+    ctx = Context(w.island_sizes)
+    chunk_bytes = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
+    ctx.set_pipeline(chunk_bytes, not args.no_graphs)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def step(i, timed, per_bucket=False):
+        for row_p, row_b in zip(pristine, bufs):
+            for x, y in zip(row_p, row_b):
+                y.copy_(x, non_blocking=True)
+        flush.zero_()
+        clean.amax()
+        if timed:
+            ev0[i].record(stream)
+        if per_bucket:
+            for row in bufs:
+                ctx.all_reduce(row, w.op, codec, w.block, stream=stream)
+        else:
+            ctx.all_reduce_buckets(bufs, w.op, codec, w.block, stream=stream)
+        if timed:
+            ev1[i].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i, False)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    l0 = kernel_launch_count()
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            step(i, True)
+    torch.cuda.synchronize()
+    barrier(pg)
+    launches = kernel_launch_count() - l0
+    clk = clocks.stop()
+    ms = max_over_ranks(pg, float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(K)])),
+                        dev if pg is not None else None)
+    # roofline region: one hop per bucket, phase marks around every kernel
+    Kr = max(2, min(K, 5))
+    ctx.set_pipeline(0, False)
+    ctx.set_phase_timing(Kr * len(bn))
+    with torch.cuda.stream(stream):
+        step(0, False, per_bucket=True)
+        torch.cuda.synchronize()
+        for i in range(Kr):
+            step(i, True, per_bucket=True)
+    torch.cuda.synchronize()
+    ph = np.array([ctx.phase_times(a) for a in range(Kr * len(bn))])  # newest first
+    ctx.close()
+    b = w.elem_bytes
+    per_rank = sum(bn) * b
+    bytes1 = bytes2 = 0
+    for nb in bn:
+        P = payload_bytes(codec, w.block, nb)
+        x1, x2 = alg_bytes(W, I, nb, b, P)
+        bytes1 += x1
+        bytes2 += x2
+    t1 = float(np.sum(ph[:, 0])) / Kr
+    t2 = float(np.sum(ph[:, 2])) / Kr
+    peak, peak_kind = measured_peaks()
+    dom = ("k_reduce_encode", bytes1, t1) if t1 >= t2 else ("k_decode_bcast", bytes2, t2)
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    return {
+        "metric": METRIC, "value": world * per_rank / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded torch generators on the device)",
+        "config": {"workload": "%s: %d simulated ranks as islands %s, %d-tensor %s gradient set (%d values) in %d "
+                               "buckets of <= 25 MiB, %s, op %s, codec %s block %d" % (
+                                   w.key, W, list(w.island_sizes), len(numels), w.dtype, sum(numels), len(bn),
+                                   w.dist, w.op, codec, w.block),
+                   "buckets": len(bn), "values_per_rank": sum(bn),
+                   "policy": "one pipeline over all buckets (%d KiB payload chunks), one CUDA graph per step" % (
+                       chunk_bytes >> 10),
+                   "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_step": dom[1],
+                     "kernel_ms_per_step": dom[2], "traffic": None,
+                     "region": "one hop per bucket, CUDA events around each kernel"},
+        "gpu_launches": int(launches), "clocks": clk,
+    }
+
+
 def run_sweep(args, local):
     """Payload sweep (workload c3): 4 KiB .. 256 MiB of float32 per rank at
     2 islands x 2 ranks, codecs none / bf16 / e4m3; one JSON line per row.
@@ -540,6 +650,14 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args, local)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    from cross_vendor_gradient_gb300 import workloads as _wl
+    if _wl.WORKLOADS[args.workload].tensors:
+        line = run_buckets_bench(args, world, rank, local, pg)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         if pg is not None:
             pg.destroy_process_group()
         return

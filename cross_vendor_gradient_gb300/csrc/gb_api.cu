@@ -6,6 +6,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -76,6 +77,15 @@ struct gb_ctx {
     GraphEntry graphs[kMaxGraphs];
     int n_graphs = 0;
     uint64_t clock = 0;
+    // gb_all_reduce_buckets: whole gradient sets captured as one graph each
+    struct BucketGraph {
+        std::vector<uint64_t> key;
+        cudaGraph_t graph = nullptr;
+        cudaGraphExec_t exec = nullptr;  // null: seen once
+        uint64_t last_use = 0;
+        int kernels = 0;
+    };
+    std::vector<BucketGraph> bucket_graphs;
     // phase timing (observer marks): a ring of `tcap` records of kMarks events
     int tcap = 0;
     cudaEvent_t *tev = nullptr;
@@ -302,6 +312,11 @@ void drop_graphs(gb_ctx *c) {
         c->graphs[i] = GraphEntry();
     }
     c->n_graphs = 0;
+    for (auto &bg : c->bucket_graphs) {
+        if (bg.exec) cudaGraphExecDestroy(bg.exec);
+        if (bg.graph) cudaGraphDestroy(bg.graph);
+    }
+    c->bucket_graphs.clear();
 }
 
 gb_status grow_device(gb_ctx *c, unsigned char **buf, size_t *have, size_t need) {
@@ -682,6 +697,178 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
     GB_TRY(wait_on(c, s, c->ev_join_d));
     GB_TRY(wait_on(c, s, c->ev_join_h));
     return GB_OK;
+}
+
+// gb_all_reduce_buckets as one pipeline over every bucket's chunks: chunk
+// i's encode, bridge hop and decode use staging slot i % 2 (a two-slot
+// ring), and chunks are issued one ahead (encode + device -> host of chunk
+// i+1 before host -> device + decode of chunk i), so the bridge of one
+// bucket overlaps the kernels of the next and never idles between buckets.
+// The ring is safe because on the kernel stream encode(i+1) follows
+// decode(i-1), which waited for every copy of chunk i-1.
+struct WorkChunk {
+    int b;
+    uint64_t e0, m;
+};
+
+gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, void *const *bufs,
+                          cudaStream_t s) {
+    const int I = p.I, W = p.W;
+    constexpr int R = 2;
+    auto outbox = [&](int slot, int i) { return c->d_stage + ((size_t)slot * I + i) * p.part; };
+    auto inbox = [&](int g, int slot, int j) {
+        unsigned char *base = c->d_stage + (size_t)I * R * p.part;
+        if (I == 2) return base + ((size_t)slot * I + j) * p.part;
+        return base + (((size_t)g * R + slot) * I + j) * p.part;
+    };
+    auto hslot = [&](int slot, int j) { return c->h_stage + ((size_t)slot * I + j) * p.part; };
+    if (c->inject == GB_INJECT_BRIDGE) {
+        c->inject = 0;
+        return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+    }
+    cudaStream_t D = c->sd, H = c->sh;
+    const int N = (int)work.size();
+    auto front = [&](int i) -> gb_status {
+        const WorkChunk &w = work[i];
+        const int slot = i % R, ev = i % kMaxChunks;
+        gb::ReduceEncodeArgs ra;
+        memset(&ra, 0, sizeof ra);
+        for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)bufs[(size_t)w.b * W + r] + w.e0 * p.eb;
+        for (int q = 0; q < I; ++q) ra.payload[q] = outbox(slot, q);
+        for (int q = 0; q <= I; ++q) ra.first[q] = c->first[q];
+        ra.n_islands = I;
+        ra.n = w.m;
+        ra.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
+        ra.scales_off = is_fp8(p.eff) ? round_up(w.m * p.cb, 16) : 0;
+        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        GB_TRY(record(c, c->ev_k1[ev], s));
+        GB_TRY(wait_on(c, D, c->ev_k1[ev]));
+        GB_TRY(copy_async(c, hslot(slot, 0), outbox(slot, 0), (size_t)(I - 1) * p.part + part_bytes(p, w.m),
+                          cudaMemcpyDeviceToHost, D));
+        GB_TRY(record(c, c->ev_d2h[ev], D));
+        return GB_OK;
+    };
+    auto back = [&](int i) -> gb_status {
+        const WorkChunk &w = work[i];
+        const int slot = i % R, ev = i % kMaxChunks;
+        const size_t pb = part_bytes(p, w.m);
+        GB_TRY(wait_on(c, H, c->ev_d2h[ev]));
+        if (I == 2) {
+            GB_TRY(copy_async(c, inbox(1, slot, 0), hslot(slot, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+        } else {
+            for (int g = 0; g < I; ++g) {
+                if (g > 0)
+                    GB_TRY(copy_async(c, inbox(g, slot, 0), hslot(slot, 0), (size_t)(g - 1) * p.part + pb,
+                                      cudaMemcpyHostToDevice, H));
+                if (g < I - 1)
+                    GB_TRY(copy_async(c, inbox(g, slot, g + 1), hslot(slot, g + 1), (size_t)(I - g - 2) * p.part + pb,
+                                      cudaMemcpyHostToDevice, H));
+            }
+        }
+        GB_TRY(record(c, c->ev_h2d[ev], H));
+        GB_TRY(wait_on(c, s, c->ev_h2d[ev]));
+        gb::DecodeBcastArgs da;
+        memset(&da, 0, sizeof da);
+        for (int r = 0; r < W; ++r) {
+            da.dst[r] = (unsigned char *)bufs[(size_t)w.b * W + r] + w.e0 * p.eb;
+            da.group_of_rank[r] = c->island_of[r];
+        }
+        for (int g = 0; g < I; ++g)
+            for (int j = 0; j < I; ++j)
+                da.payload[g][j] = (j == g) ? (const void *)outbox(slot, j) : (const void *)inbox(g, slot, j);
+        for (int q = 0; q <= I; ++q) da.first[q] = c->first[q];
+        da.n_groups = I;
+        da.n_src = I;
+        da.avg = p.op == GB_AVG;
+        da.world = (float)W;
+        da.world_pow2 = (W & (W - 1)) == 0;
+        da.inv_world = 1.0f / (float)W;
+        da.n = w.m;
+        da.scales_off = is_fp8(p.eff) ? round_up(w.m * p.cb, 16) : 0;
+        da.vec = 1;
+        da.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
+        GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        return GB_OK;
+    };
+    GB_TRY(front(0));
+    for (int i = 0; i < N; ++i) {
+        if (i + 1 < N) GB_TRY(front(i + 1));
+        GB_TRY(back(i));
+    }
+    GB_TRY(record(c, c->ev_join_d, D));
+    GB_TRY(record(c, c->ev_join_h, H));
+    GB_TRY(wait_on(c, s, c->ev_join_d));
+    GB_TRY(wait_on(c, s, c->ev_join_h));
+    return GB_OK;
+}
+
+gb_status run_buckets(gb_ctx *c, int nb, void *const *bufs, const size_t *numel, gb_dtype dtype, gb_op op,
+                      gb_codec codec, int block, cudaStream_t s) {
+    // the chunk shape of the largest bucket fixes the slot size
+    size_t nmax = 0;
+    for (int b = 0; b < nb; ++b) nmax = numel[b] > nmax ? numel[b] : nmax;
+    Plan p = make_plan(c, nmax, dtype, op, codec, block, 0);
+    std::vector<WorkChunk> work;
+    for (int b = 0; b < nb; ++b)
+        for (uint64_t e0 = 0; e0 < numel[b]; e0 += p.chunk)
+            work.push_back({b, e0, (numel[b] - e0) < p.chunk ? (numel[b] - e0) : p.chunk});
+    const size_t recv = c->I == 2 ? 2 : (size_t)c->I * c->I;
+    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(c->I + recv) * 2 * p.part));
+    GB_TRY(grow_host(c, (size_t)c->I * 2 * p.part));
+    GB_TRY(begin(c, s));
+    if (!c->use_graphs) {
+        GB_TRY(enqueue_buckets(c, p, work, bufs, s));
+        return end(c, s);
+    }
+    std::vector<uint64_t> key = {(uint64_t)nb, (uint64_t)dtype, (uint64_t)op, (uint64_t)p.eff, (uint64_t)p.blk,
+                                 (uint64_t)p.chunk, (uint64_t)(uintptr_t)c->d_stage, (uint64_t)(uintptr_t)c->h_stage};
+    for (int b = 0; b < nb; ++b) {
+        key.push_back(numel[b]);
+        for (int r = 0; r < c->W; ++r) key.push_back((uint64_t)(uintptr_t)bufs[(size_t)b * c->W + r]);
+    }
+    gb_ctx::BucketGraph *bg = nullptr;
+    for (auto &g : c->bucket_graphs)
+        if (g.key == key) bg = &g;
+    if (!bg) {  // first time: run directly, remember the shape
+        if (c->bucket_graphs.size() >= 8) {
+            size_t lru = 0;
+            for (size_t i = 1; i < c->bucket_graphs.size(); ++i)
+                if (c->bucket_graphs[i].last_use < c->bucket_graphs[lru].last_use) lru = i;
+            if (c->bucket_graphs[lru].exec) cudaGraphExecDestroy(c->bucket_graphs[lru].exec);
+            if (c->bucket_graphs[lru].graph) cudaGraphDestroy(c->bucket_graphs[lru].graph);
+            c->bucket_graphs.erase(c->bucket_graphs.begin() + lru);
+        }
+        c->bucket_graphs.emplace_back();
+        c->bucket_graphs.back().key = key;
+        c->bucket_graphs.back().last_use = ++c->clock;
+        GB_TRY(enqueue_buckets(c, p, work, bufs, s));
+        return end(c, s);
+    }
+    bg->last_use = ++c->clock;
+    if (!bg->exec) {
+        cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
+        gb_status st = enqueue_buckets(c, p, work, bufs, c->scap);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(c->scap, &g);
+        if (st != GB_OK) {
+            if (g) cudaGraphDestroy(g);
+            return st;
+        }
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamEndCapture", e);
+        cudaGraphExec_t x = nullptr;
+        if ((e = cudaGraphInstantiate(&x, g, 0)) != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return fail(c, GB_ERR_CUDA, "cudaGraphInstantiate", e);
+        }
+        bg->graph = g;
+        bg->exec = x;
+        bg->kernels = 2 * (int)work.size();
+    }
+    cudaError_t e = cudaGraphLaunch(bg->exec, s);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphLaunch", e);
+    for (int k = 0; k < bg->kernels; ++k) gb::count_launch();
+    return end(c, s);
 }
 
 // Capture one pipelined all_reduce on the context's capture stream and
@@ -1394,11 +1581,20 @@ gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bu
     GB_TRY(check_collective(c, 0, dtype, op, codec, block));
     for (int b = 0; b < n_buckets; ++b) {
         GB_TRY(check_n(c, bucket_numel[b]));
-        GB_TRY(check_dev_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
+        if (bucket_numel[b] > 0)  // an empty bucket's pointers are never used
+            GB_TRY(check_dev_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
+    }
+    size_t total = 0;
+    for (int b = 0; b < n_buckets; ++b) total += bucket_numel[b];
+    if (total == 0) return GB_OK;
+    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
+        GB_TRY(bind(c));
+        return run_buckets(c, n_buckets, bucket_bufs, bucket_numel, dtype, op, codec, block, (cudaStream_t)stream);
     }
     for (int b = 0; b < n_buckets; ++b)
-        GB_TRY(gb_all_reduce(c, bucket_bufs + (size_t)b * c->W, bucket_numel[b], dtype, op, codec, block,
-                             stream));
+        if (bucket_numel[b] > 0)
+            GB_TRY(gb_all_reduce(c, bucket_bufs + (size_t)b * c->W, bucket_numel[b], dtype, op, codec, block,
+                                 stream));
     return GB_OK;
 }
 

@@ -294,10 +294,17 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, 
                          size_t pad_elems, int *bucket_of, size_t *offset, size_t *bucket_numel,
                          int max_buckets, int *n_buckets);
 
-/* One gb_all_reduce per bucket, in bucket order.  bucket_bufs holds
- * n_buckets * W device pointers, bucket-major (bucket b, rank r at
- * [b * W + r]); bucket b has bucket_numel[b] elements.  The tensors of the
- * plan are views into these flat buffers, so nothing is copied in or out. */
+/* All_reduce of every bucket, in bucket order: each bucket gets the bits
+ * gb_all_reduce would give it.  bucket_bufs holds n_buckets * W device
+ * pointers, bucket-major (bucket b, rank r at [b * W + r]); bucket b has
+ * bucket_numel[b] elements.  The tensors of the plan are views into these
+ * flat buffers, so nothing is copied in or out.  Under the pipelined policy
+ * (float32 / bfloat16 SUM / AVG, two or more islands, no phase marks kept)
+ * the buckets run as one pipeline of chunks on a two-slot staging ring, the
+ * bridge of one bucket overlapping the kernels of the next, captured as one
+ * CUDA graph for the whole set from the second call with the same buffers
+ * (one launch per gradient sync); otherwise one gb_all_reduce per bucket.
+ * Empty buckets are allowed (nothing to do; their pointers may be NULL). */
 gb_status gb_all_reduce_buckets(gb_ctx *ctx, int n_buckets, void *const *bucket_bufs,
                                 const size_t *bucket_numel, gb_dtype dtype, gb_op op,
                                 gb_codec codec, int block, gb_stream stream);

@@ -382,3 +382,30 @@ def test_all_reduce_host_pipelined(codec, block, sizes, dtype):
             for r in range(W):
                 got = host[r].view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else host[r].numpy()
                 assert_bits_equal(got, want[r], "host pipelined call %d rank %d" % (call, r))
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (4, 4), (2, 1, 3)])
+def test_bucket_pipeline_matches_oracle(codec, block, sizes):
+    """gb_all_reduce_buckets as one pipeline over all buckets' chunks (two-slot
+    staging ring, one CUDA graph for the set): every bucket gets the
+    oracle's bits, on three calls with the same buffers."""
+    W = sum(sizes)
+    numels = [5000, 0, 257, 40_000, 1, 9000, 31_337]
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(4096, True)  # several chunks per bucket
+        hosts = [inputs(sizes, n, "bf16", cid=300 + b) if n else [np.zeros(0, np.uint16)] * W
+                 for b, n in enumerate(numels)]
+        bufs = [[torch.empty(max(n, 1), dtype=torch.bfloat16, device="cuda")[:n] for _ in range(W)] for n in numels]
+        wants = [orc.all_reduce(h, sizes, "sum", codec, block) if n else None for h, n in zip(hosts, numels)]
+        for call in range(3):
+            for b, n in enumerate(numels):
+                for r in range(W):
+                    if n:
+                        bufs[b][r].copy_(to_dev(hosts[b][r]))
+            ctx.all_reduce_buckets(bufs, "sum", codec, block)
+            torch.cuda.synchronize()
+            for b, n in enumerate(numels):
+                for r in range(W):
+                    if n:
+                        assert_bits_equal(to_host(bufs[b][r]), wants[b][r], "call %d bucket %d rank %d" % (call, b, r))

@@ -1,5 +1,9 @@
 """Benchmark of the reduce-bridge-broadcast gradient all_reduce on one GB300.
 
+Bucketed workloads (--workload c4, c5): a step is the all_reduce of a whole
+GPT-2 small or 1.1B Llama-style bf16 gradient set in 25 MiB buckets through
+gb_all_reduce_buckets; c5 adds reduce_scatter then all_gather of every bucket.
+
 Default workload: 4 simulated ranks as 2 islands of 2, one 25 MiB float32
 DDP bucket per rank (n = 6,553,600), values N(0, 1e-3) with 1% of them x100,
 op AVG, bridge codec fp8 E4M3 with a power-of-two scale per 256 values.
@@ -12,8 +16,11 @@ buffer and then reading a separate 256 MiB one (so no dirty line is left to
 be written back during the step); neither is inside the step's CUDA events.
 
 Reported: algorithm GB/s (bytes of one rank buffer / step time, summed over
-replicas), the dominant kernel's HBM roofline fraction from its live CUDA
-event durations, the bridge hop against measured pinned copy bandwidth, the
+replicas), the dominant kernel's HBM roofline fraction from live CUDA event
+durations (each kernel launched back to back over input sets cycled so that
+none is in L2; the per-kernel durations inside a step, with a CUDA event
+around every phase, are reported beside it), the bridge hop against measured
+pinned copy bandwidth, the
 same metric end to end through gb_all_reduce_host with pinned host buffers,
 and the oracle timed on the host cores (``--impl reference`` times only the
 oracle).  Multi-GPU: one independent replica per GPU (the path has no
@@ -35,6 +42,7 @@ if ROOT not in sys.path:
 
 METRIC = "all_reduce algorithm GB/s and % of GB300 HBM roofline vs payload size, per codec"
 FLUSH_BYTES = 512 << 20
+L2_BYTES = 129 << 20  # GB300 L2 (nominal 129 MB)
 
 
 def parse():
@@ -315,7 +323,57 @@ def run_gb(args, world, rank, local, pg):
     k1_ms, bridge_ms, k2_ms = (float(np.mean(phases[:, j])) for j in range(3))
     k1_bytes, k2_bytes = alg_bytes(W, I, n, b, P)
     peak, peak_kind = measured_peaks()
-    dom = (names[0], k1_bytes, k1_ms) if k1_ms >= k2_ms else (names[1], k2_bytes, k2_ms)
+
+    # ---- timed region 3: each kernel back to back, as the fused halves of
+    # the path (gb_island_reduce_compress, gb_decompress_island_broadcast).
+    # S input sets, outputs and payloads, together several times L2, are
+    # cycled so that no launch finds its inputs in L2.  A batch starts from a
+    # clean L2 (256 MiB read); its first launch of each kernel is untimed, and
+    # CUDA events on the launching stream bracket the other S - 1, so that
+    # every timed launch also writes back what its predecessor left dirty in
+    # L2: the steady state of a stream of buckets.
+    ks = None
+    if not exact and I > 1:
+        set_bytes = W * n * b + I * P
+        S = max(5, min(-(-(4 * L2_BYTES) // set_bytes), (8 << 30) // set_bytes))
+        ins = [[p.clone() for p in pristine] for _ in range(S)]
+        outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
+        pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
+        Kk = max(3, min(Kr, 50))
+        ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kk)]
+        with torch.cuda.stream(stream):
+            for it in range(Wm + Kk):
+                e = ea[it - Wm] if it >= Wm else None
+                clean.amax()
+                # hold the stream ~0.4 ms so that the host has queued the whole
+                # batch before its first event: the batch then runs GPU-bound
+                torch.cuda._sleep(800_000)
+                for q in range(S):
+                    ctx.island_reduce_compress(ins[q], codec, w.block, pays[q], stream=stream)
+                    if e and q == 0:
+                        e[0].record(stream)
+                if e:
+                    e[1].record(stream)
+                for q in range(S):
+                    ctx.decompress_island_broadcast(pays[q], w.op, codec, w.block, outs[q], stream=stream)
+                    if e and q == 0:
+                        e[2].record(stream)
+                if e:
+                    e[3].record(stream)
+        torch.cuda.synchronize()
+        ks = {"sets": S, "timed_launches_per_batch": S - 1, "batches": Kk, "set_bytes": set_bytes,
+              names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
+              names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
+        del ins, outs, pays
+    if ks:
+        r1, r2 = ks[names[0]], ks[names[1]]
+        region = ("timed region 3: each kernel launched back to back over %d input sets (%.0f MB each, "
+                  "cycled so that none is in L2); CUDA events around the last %d launches of each batch"
+                  % (S, set_bytes / 1e6, S - 1))
+    else:
+        r1, r2 = k1_ms, k2_ms
+        region = "timed region 2: one bridge hop per call, CUDA events around each phase"
+    dom = (names[0], k1_bytes, r1) if r1 >= r2 else (names[1], k2_bytes, r2)
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
     link_bytes = I * P + I * (I - 1) * P
     link_peak = min(link["d2h_gbs"], link["h2d_gbs"])
@@ -359,7 +417,12 @@ def run_gb(args, world, rank, local, pg):
                    "parallelism": "replicas x%d" % world},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "alg_bytes_per_launch": dom[1], "avg_launch_ms": dom[2], "traffic": None},
+                     "alg_bytes_per_launch": dom[1], "avg_launch_ms": dom[2], "traffic": None,
+                     "region": region},
+        **({"kernels_stream_ms": ks,
+            "kernels_stream_hbm_frac": {names[0]: k1_bytes / (ks[names[0]] * 1e-3) / 1e9 / peak,
+                                        names[1]: k2_bytes / (ks[names[1]] * 1e-3) / 1e9 / peak}}
+           if ks else {}),
         "kernels_ms": {names[0]: k1_ms, "bridge_hop": bridge_ms, names[1]: k2_ms,
                        "region": "timed region 2: one bridge hop per call, CUDA events around each phase",
                        "step_ms_with_marks": plain_ms},
@@ -425,7 +488,9 @@ def run_buckets_bench(args, world, rank, local, pg):
     codec = args.codec or w.codecs[0]
     W, I = w.world_size, len(w.island_sizes)
     numels = [wl.numel(sh) for sh in w.tensors]
-    _, _, bn = bucket_plan(numels, w.elem_bytes, wl.BUCKET_CAP_BYTES, 1)
+    rs_ag = args.workload == "c5"  # this set is also reduce_scattered then all_gathered
+    # reduce_scatter slices of whole 8-element vectors: buckets padded to 8 * W elements
+    _, _, bn = bucket_plan(numels, w.elem_bytes, wl.BUCKET_CAP_BYTES, 8 * W if rs_ag else 1)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     pristine = [[wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 1000 * bi, dev, tdt) for r in range(W)]
                 for bi, nb in enumerate(bn)]
@@ -474,6 +539,36 @@ def run_buckets_bench(args, world, rank, local, pg):
     clk = clocks.stop()
     ms = max_over_ranks(pg, float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(K)])),
                         dev if pg is not None else None)
+    rs_line = None
+    if rs_ag:
+        # reduce_scatter then all_gather of every bucket, same ranks, same buffers
+        slices = [[torch.empty(nb // W, dtype=tdt, device=dev) for _ in range(W)] for nb in bn]
+        Ks = max(2, min(K, 5))
+
+        def step_rs(i, timed):
+            for row_p, row_b in zip(pristine, bufs):
+                for x, y in zip(row_p, row_b):
+                    y.copy_(x, non_blocking=True)
+            flush.zero_()
+            clean.amax()
+            if timed:
+                ev0[i].record(stream)
+            for row, sl in zip(bufs, slices):
+                ctx.reduce_scatter(row, sl, w.op, codec, w.block, stream=stream)
+                ctx.all_gather(sl, row, stream=stream)
+            if timed:
+                ev1[i].record(stream)
+
+        with torch.cuda.stream(stream):
+            step_rs(0, False)
+            for i in range(Ks):
+                step_rs(i, True)
+        torch.cuda.synchronize()
+        ms_rs = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Ks)]))
+        per = sum(bn) * w.elem_bytes
+        rs_line = {"what": "reduce_scatter then all_gather of every bucket, one bridge hop per call",
+                   "ms_per_step": ms_rs, "value": per / (ms_rs * 1e-3) / 1e9, "unit": "GB/s", "steps": Ks}
+        del slices
     # roofline region: one hop per bucket, phase marks around every kernel
     Kr = max(2, min(K, 5))
     ctx.set_pipeline(0, False)
@@ -516,6 +611,7 @@ def run_buckets_bench(args, world, rank, local, pg):
                      "kernel_ms_per_step": dom[2], "traffic": None,
                      "region": "one hop per bucket, CUDA events around each kernel"},
         "gpu_launches": int(launches), "clocks": clk,
+        **({"rs_ag": rs_line} if rs_line else {}),
     }
 
 

@@ -182,6 +182,23 @@ class Context:
         self._check(B.gb_island_broadcast(self.handle, island, total.data_ptr(), total.numel(), _op(op),
                                           [t.data_ptr() for t in tensors], dt, _stream(stream)))
 
+    def island_reduce_compress(self, tensors, codec, block, payloads, stream=None):
+        """Fused island reduce + encode of every island: payloads[i] (uint8
+        device tensors of payload_bytes(codec, block, n) bytes) receive the
+        encoded island sums."""
+        dt = _dtype(tensors)
+        self._check(B.gb_island_reduce_compress(self.handle, [t.data_ptr() for t in tensors],
+                                                tensors[0].numel(), dt, _codec(codec), block,
+                                                [p.data_ptr() for p in payloads], _stream(stream)))
+
+    def decompress_island_broadcast(self, payloads, op, codec, block, tensors, stream=None):
+        """Fused decode of every island's payload + accumulate + broadcast
+        into all rank tensors."""
+        dt = _dtype(tensors)
+        self._check(B.gb_decompress_island_broadcast(self.handle, [p.data_ptr() for p in payloads],
+                                                     tensors[0].numel(), dt, _op(op), _codec(codec), block,
+                                                     [t.data_ptr() for t in tensors], _stream(stream)))
+
     # -------------------------------------------------------------- timing
     def set_phase_timing(self, capacity):
         """capacity > 0: keep the phase marks of the last `capacity` calls."""

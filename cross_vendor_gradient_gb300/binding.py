@@ -61,6 +61,8 @@ SIGNATURES = {
     "gb_bridge_compress": (_i, [_vp, _vp, _sz, _i, _i, _vp, _vp]),
     "gb_bridge_decompress_accumulate": (_i, [_vp, _vp, _sz, _i, _i, _vp, _i, _vp]),
     "gb_island_broadcast": (_i, [_vp, _i, _vp, _sz, _i, _P(_vp), _i, _vp]),
+    "gb_island_reduce_compress": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
+    "gb_decompress_island_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
     "gb_all_reduce": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_all_reduce_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_reduce_scatter": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
@@ -185,6 +187,16 @@ def gb_bridge_decompress_accumulate(ctx, payload, n, codec, block, accum, accumu
 
 def gb_island_broadcast(ctx, island, total, n, op, rank_bufs, dtype, stream=0):
     return lib().gb_island_broadcast(ctx, island, total, n, op, _ptrs(rank_bufs), dtype, stream)
+
+
+def gb_island_reduce_compress(ctx, rank_bufs, n, dtype, codec, block, payloads, stream=0):
+    return lib().gb_island_reduce_compress(ctx, _ptrs(rank_bufs), n, dtype, codec, block, _ptrs(payloads),
+                                           stream)
+
+
+def gb_decompress_island_broadcast(ctx, payloads, n, dtype, op, codec, block, rank_bufs, stream=0):
+    return lib().gb_decompress_island_broadcast(ctx, _ptrs(payloads), n, dtype, op, codec, block,
+                                                _ptrs(rank_bufs), stream)
 
 
 def gb_all_reduce(ctx, rank_bufs, n, dtype, op, codec, block, stream=0):

@@ -1313,6 +1313,68 @@ gb_status gb_island_broadcast(gb_ctx *c, int island, const float *total, size_t 
                         "island broadcast");
 }
 
+gb_status gb_island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                    gb_codec codec, int block, void *const *payloads, gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_codec_dtype(c, dtype));
+    GB_TRY(check_codec(c, codec, block));
+    GB_TRY(check_n(c, n));
+    GB_TRY(check_dev_bufs(c, rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_dev_bufs(c, (const void *const *)payloads, c->I, "payloads"));
+    if (n == 0) return GB_OK;
+    GB_TRY(bind(c));
+    const int blk = is_fp8(codec) ? block : 256;
+    gb::ReduceEncodeArgs ra;
+    memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < c->W; ++r) ra.src[r] = rank_bufs[r];
+    for (int i = 0; i < c->I; ++i) ra.payload[i] = payloads[i];
+    for (int i = 0; i <= c->I; ++i) ra.first[i] = c->first[i];
+    ra.n_islands = c->I;
+    ra.n = n;
+    ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
+    ra.scales_off = scales_offset(codec, n);
+    return check_launch(c, gb::launch_reduce_encode(ra, dtype, codec, blk, (cudaStream_t)stream),
+                        "island reduce + compress");
+}
+
+gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype,
+                                         gb_op op, gb_codec codec, int block, void *const *rank_bufs,
+                                         gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_codec_dtype(c, dtype));
+    if (op != GB_SUM && op != GB_AVG)
+        return set_msg(c, GB_ERR_UNSUPPORTED_OP, "decompress + island broadcast takes SUM / AVG");
+    GB_TRY(check_codec(c, codec, block));
+    GB_TRY(check_n(c, n));
+    GB_TRY(check_dev_bufs(c, payloads, c->I, "payloads"));
+    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    if (n == 0) return GB_OK;
+    GB_TRY(bind(c));
+    const int blk = is_fp8(codec) ? block : 256;
+    gb::DecodeBcastArgs da;
+    memset(&da, 0, sizeof da);
+    for (int r = 0; r < c->W; ++r) {
+        da.dst[r] = rank_bufs[r];
+        da.group_of_rank[r] = c->island_of[r];
+    }
+    for (int g = 0; g < c->I; ++g)
+        for (int j = 0; j < c->I; ++j) da.payload[g][j] = payloads[j];
+    for (int i = 0; i <= c->I; ++i) da.first[i] = c->first[i];
+    da.n_groups = c->I;
+    da.n_src = c->I;
+    da.avg = op == GB_AVG;
+    da.world = (float)c->W;
+    da.world_pow2 = (c->W & (c->W - 1)) == 0;
+    da.inv_world = 1.0f / (float)c->W;
+    da.n = n;
+    da.scales_off = scales_offset(codec, n);
+    da.rs = 0;
+    da.vec = 1;
+    da.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
+    return check_launch(c, gb::launch_decode_bcast(da, dtype, codec, blk, (cudaStream_t)stream),
+                        "decompress + island broadcast");
+}
+
 gb_status gb_all_reduce(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dtype, gb_op op,
                         gb_codec codec, int block, gb_stream stream) {
     GB_TRY(check_ctx(c));

@@ -36,6 +36,55 @@ int sm_count() {
     return count;
 }
 
+// The raw payload bits of one lane's 8 elements of a full tile: the codes
+// and, for fp8, the block scale.  Loading them is split from decoding them
+// so that a warp can have the next tile's loads in flight while it decodes
+// and stores the current one.
+template <int CODEC> struct RawLane;
+template <> struct RawLane<GB_CODEC_NONE> { U8x32 x; };
+template <> struct RawLane<GB_CODEC_BF16> { uint4 x; };
+template <> struct RawLane<GB_CODEC_E4M3> { uint2 x; float s; };
+template <> struct RawLane<GB_CODEC_E5M2> { uint2 x; float s; };
+
+template <int CODEC, int BLOCK>
+__device__ __forceinline__ void load_raw(const void *payload, uint64_t scales_off, uint64_t gbase, int lane,
+                                         RawLane<CODEC> &r) {
+    if constexpr (CODEC == GB_CODEC_NONE) {
+        r.x = ld_v8((const float *)payload + gbase + 8 * lane);
+    } else if constexpr (CODEC == GB_CODEC_BF16) {
+        r.x = ld_u4((const unsigned short *)payload + gbase + 8 * lane);
+    } else {
+        const uint64_t j0 = gbase + 8 * lane;
+        r.x = ld_u2((const unsigned char *)payload + j0);
+        r.s = __ldg((const float *)((const unsigned char *)payload + scales_off) + j0 / BLOCK);
+    }
+}
+
+template <int CODEC>
+__device__ __forceinline__ void decode_raw(const RawLane<CODEC> &r, float d[8]) {
+    if constexpr (CODEC == GB_CODEC_NONE) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = __uint_as_float(r.x.w[k]);
+    } else if constexpr (CODEC == GB_CODEC_BF16) {
+        const uint32_t w[4] = {r.x.x, r.x.y, r.x.z, r.x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            d[2 * i] = __uint_as_float(w[i] << 16);
+            d[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    } else {
+        float c[8];
+        fp8x2_to_f32<CODEC>(r.x.x & 0xFFFFu, c[0], c[1]);
+        fp8x2_to_f32<CODEC>(r.x.x >> 16, c[2], c[3]);
+        fp8x2_to_f32<CODEC>(r.x.y & 0xFFFFu, c[4], c[5]);
+        fp8x2_to_f32<CODEC>(r.x.y >> 16, c[6], c[7]);
+        // code value * 2^k is exact in float32: k >= -126 keeps every
+        // product on or above the subnormal grid
+#pragma unroll
+        for (int k = 0; k < 8; ++k) d[k] = __fmul_rn(c[k], r.s);
+    }
+}
+
 // Decode this lane's 8 elements of a payload.  `gbase` is the index, in the
 // full buffer, of the tile's first element; in the element-wise path only
 // elements whose index within the output unit (lbase + offset) is below
@@ -44,32 +93,9 @@ template <int CODEC, int BLOCK>
 __device__ __forceinline__ void decode_lane(const void *payload, uint64_t scales_off, uint64_t gbase,
                                             uint64_t lbase, uint64_t limit, int lane, bool full, float d[8]) {
     if (full) {
-        if constexpr (CODEC == GB_CODEC_NONE) {
-            const U8x32 x = ld_v8((const float *)payload + gbase + 8 * lane);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) d[k] = __uint_as_float(x.w[k]);
-        } else if constexpr (CODEC == GB_CODEC_BF16) {
-            const uint4 x = ld_u4((const unsigned short *)payload + gbase + 8 * lane);
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                d[2 * i] = __uint_as_float(w[i] << 16);
-                d[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
-        } else {
-            const uint64_t j0 = gbase + 8 * lane;
-            const uint2 x = ld_u2((const unsigned char *)payload + j0);
-            const float s = __ldg((const float *)((const unsigned char *)payload + scales_off) + j0 / BLOCK);
-            float c[8];
-            fp8x2_to_f32<CODEC>(x.x & 0xFFFFu, c[0], c[1]);
-            fp8x2_to_f32<CODEC>(x.x >> 16, c[2], c[3]);
-            fp8x2_to_f32<CODEC>(x.y & 0xFFFFu, c[4], c[5]);
-            fp8x2_to_f32<CODEC>(x.y >> 16, c[6], c[7]);
-            // code value * 2^k is exact in float32: k >= -126 keeps every
-            // product on or above the subnormal grid
-#pragma unroll
-            for (int k = 0; k < 8; ++k) d[k] = __fmul_rn(c[k], s);
-        }
+        RawLane<CODEC> r;
+        load_raw<CODEC, BLOCK>(payload, scales_off, gbase, lane, r);
+        decode_raw<CODEC>(r, d);
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -126,6 +152,24 @@ __device__ __forceinline__ void store_rank(void *p, uint64_t lbase, int lane, ui
     }
 }
 
+// AVG and the stores of one tile's totals to ranks r_lo .. r_hi - 1.
+template <typename T>
+__device__ __forceinline__ void finish_tile(const DecodeBcastArgs &a, int r_lo, int r_hi, uint64_t lbase, int lane,
+                                            uint64_t limit, bool full, float t[8]) {
+    if (a.avg) {
+        // t / W; for W = 2^e the product with 2^-e is the same correctly
+        // rounded quotient (one rounding of the same real number)
+        if (a.world_pow2) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(t[k], a.inv_world);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) t[k] = __fdiv_rn(t[k], a.world);
+        }
+    }
+    for (int r = r_lo; r < r_hi; ++r) store_rank<T>(a.dst[r], lbase, lane, limit, full, t);
+}
+
 // NS > 0: exactly NS payloads (loads unrolled); NS == 0: a.n_src of them.
 template <typename T, int CODEC, int BLOCK, int NS>
 __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ DecodeBcastArgs a) {
@@ -149,51 +193,64 @@ __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ De
     const int nsrc = NS > 0 ? NS : a.n_src;
     const uint32_t wpb = blockDim.x >> 5;
     const uint32_t stride = gridDim.x * wpb;
-    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < a.tiles; tile += stride) {
+    uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5);
+    if constexpr (NS > 0) {
+        // Full tiles (vector path), software-pipelined: the payload loads of
+        // the warp's next tile are in flight while the current one is decoded
+        // and stored.  tiles < 2^31 (n < 2^39), so tile + stride never wraps.
+        const uint32_t nfull = a.vec ? (uint32_t)(limit / kTile) : 0u;
+        RawLane<CODEC> cur[NS];
+        if (tile < nfull) {
+#pragma unroll
+            for (int q = 0; q < NS; ++q)
+                load_raw<CODEC, BLOCK>(a.payload[g][q], a.scales_off, gofs + (uint64_t)tile * kTile, lane, cur[q]);
+        }
+        while (tile < nfull) {
+            const uint32_t nxt = tile + stride;
+            RawLane<CODEC> nx[NS];
+            if (nxt < nfull) {
+#pragma unroll
+                for (int q = 0; q < NS; ++q)
+                    load_raw<CODEC, BLOCK>(a.payload[g][q], a.scales_off, gofs + (uint64_t)nxt * kTile, lane, nx[q]);
+            }
+            float t[8];
+            decode_raw<CODEC>(cur[0], t);
+#pragma unroll
+            for (int q = 1; q < NS; ++q) {
+                float d[8];
+                decode_raw<CODEC>(cur[q], d);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[k]);  // island order
+            }
+            finish_tile<T>(a, r_lo, r_hi, (uint64_t)tile * kTile, lane, limit, true, t);
+#pragma unroll
+            for (int q = 0; q < NS; ++q) cur[q] = nx[q];
+            tile = nxt;
+        }
+    }
+    // the rest: every tile when NS == 0, else the ragged last tile (or all
+    // tiles when vector accesses are off), element by element
+    for (; tile < a.tiles; tile += stride) {
         const uint64_t lbase = (uint64_t)tile * kTile;
         const uint64_t gbase = gofs + lbase;
         const bool full = a.vec && lbase + kTile <= limit;
         float t[8];
-        if constexpr (NS > 0) {
-            float d[NS][8];
+        decode_lane<CODEC, BLOCK>(a.payload[g][0], a.scales_off, gbase, lbase, limit, lane, full, t);
+        for (int j0 = 1; j0 < nsrc; j0 += 2) {  // two payloads in flight at a time
+            float d[2][8];
 #pragma unroll
-            for (int q = 0; q < NS; ++q)
-                decode_lane<CODEC, BLOCK>(a.payload[g][q], a.scales_off, gbase, lbase, limit, lane, full, d[q]);
+            for (int q = 0; q < 2; ++q)
+                if (j0 + q < nsrc)
+                    decode_lane<CODEC, BLOCK>(a.payload[g][j0 + q], a.scales_off, gbase, lbase, limit, lane, full,
+                                              d[q]);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) t[k] = d[0][k];
+            for (int q = 0; q < 2; ++q)
+                if (j0 + q < nsrc) {
 #pragma unroll
-            for (int q = 1; q < NS; ++q)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);  // island order
-        } else {
-            decode_lane<CODEC, BLOCK>(a.payload[g][0], a.scales_off, gbase, lbase, limit, lane, full, t);
-            for (int j0 = 1; j0 < nsrc; j0 += 2) {  // two payloads in flight at a time
-                float d[2][8];
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    if (j0 + q < nsrc)
-                        decode_lane<CODEC, BLOCK>(a.payload[g][j0 + q], a.scales_off, gbase, lbase, limit, lane,
-                                                  full, d[q]);
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-                    if (j0 + q < nsrc) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);
-                    }
-            }
+                    for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);
+                }
         }
-        if (a.avg) {
-            // t / W; for W = 2^e the product with 2^-e is the same correctly
-            // rounded quotient (one rounding of the same real number)
-            if (a.world_pow2) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) t[k] = __fmul_rn(t[k], a.inv_world);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) t[k] = __fdiv_rn(t[k], a.world);
-            }
-        }
-        for (int r = r_lo; r < r_hi; ++r) store_rank<T>(a.dst[r], lbase, lane, limit, full, t);
+        finish_tile<T>(a, r_lo, r_hi, lbase, lane, limit, full, t);
     }
 }
 

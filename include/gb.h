@@ -222,6 +222,36 @@ gb_status gb_bridge_decompress_accumulate(gb_ctx *ctx, const void *payload, size
 gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_t n, gb_op op,
                               void *const *rank_bufs, gb_dtype dtype, gb_stream stream);
 
+/* The two fused halves of reduce-bridge-broadcast, for a caller that moves
+ * the payloads over a bridge of its own (gpubridge README, "all_reduce uses
+ * reduce-bridge-broadcast": island reduce, the leaders' bridge step, island
+ * broadcast; "Bridge compression": leaders compress before the bridge and
+ * decompress after it).
+ *
+ * gb_island_reduce_compress: for every island i, payloads[i] receives the
+ * encoding of s_i, the float32 sum of the island's ranks in ascending order,
+ * with `codec` and `block`, in the layout of gb_payload_bytes (codes, then
+ * the fp8 scales at gb_payload_scales_offset).  The codec is applied as
+ * given, with one island too (gb_all_reduce skips it there: no bridge).
+ * rank_bufs: W device buffers of n elements, 32-byte aligned, read only.
+ * payloads: I device buffers of gb_payload_bytes(codec, block, n) bytes,
+ * 32-byte aligned, owned by the caller.  dtype F32 or BF16.  One kernel
+ * launch for all islands, stream-ordered on `stream`.
+ *
+ * gb_decompress_island_broadcast: every rank buffer receives
+ * t = dec(payloads[0]) + ... + dec(payloads[I - 1]) in float32, island
+ * order, divided by W for AVG (float32 division), rounded to dtype (nearest
+ * even for bf16).  With the payloads of gb_island_reduce_compress, carried
+ * bit for bit, this is what gb_all_reduce writes.  op SUM or AVG.  One
+ * kernel launch.
+ *
+ * Errors as for gb_all_reduce; n == 0 is a no-op.  Neither call allocates. */
+gb_status gb_island_reduce_compress(gb_ctx *ctx, const void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                    gb_codec codec, int block, void *const *payloads, gb_stream stream);
+gb_status gb_decompress_island_broadcast(gb_ctx *ctx, const void *const *payloads, size_t n, gb_dtype dtype,
+                                         gb_op op, gb_codec codec, int block, void *const *rank_bufs,
+                                         gb_stream stream);
+
 /* ------------------------------------------------------------ collectives */
 
 /* In-place all_reduce of W rank buffers of n elements (gpubridge README, API

@@ -409,3 +409,47 @@ def test_bucket_pipeline_matches_oracle(codec, block, sizes):
                 for r in range(W):
                     if n:
                         assert_bits_equal(to_host(bufs[b][r]), wants[b][r], "call %d bucket %d rank %d" % (call, b, r))
+
+
+@pytest.mark.parametrize("codec,block", CODECS)
+@pytest.mark.parametrize("sizes", [(1,), (3,), (1, 1), (2, 2), (2, 1, 3), (1, 1, 1, 1, 1, 1, 1, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_halves_match_oracle(codec, block, sizes, dtype):
+    """island_reduce_compress writes every island's payload as the oracle
+    encodes its island sum (codes and scales bit for bit); after a plain copy
+    of the payloads, decompress_island_broadcast writes the oracle's total to
+    every rank, which for two or more islands is the fused all_reduce."""
+    W, I = sum(sizes), len(sizes)
+    first = np.concatenate([[0], np.cumsum(sizes)]).astype(int)
+    with Context(sizes) as ctx:
+        for n in (1, 255, 256 * 9 + 17, 40000):
+            for op in ("sum", "avg"):
+                xs = inputs(sizes, n, dtype, cid=31 + n % 13)
+                bufs = [to_dev(x) for x in xs]
+                P = payload_bytes(codec, block, n)
+                pay = [torch.empty(P, dtype=torch.uint8, device="cuda") for _ in range(I)]
+                ctx.island_reduce_compress(bufs, codec, block, pay)
+                moved = [p.clone() for p in pay]  # the caller's own bridge
+                ctx.decompress_island_broadcast(moved, op, codec, block, bufs)
+                torch.cuda.synchronize()
+                cd = orc.code_dtype(codec)
+                cb = np.dtype(cd).itemsize
+                enc = []
+                for i in range(I):
+                    s = orc.island_sum(xs[first[i]:first[i + 1]])
+                    codes, scales = orc.encode(s, codec, block)
+                    ph = to_host(pay[i])
+                    assert_bits_equal(ph[:n * cb].view(cd), codes, "codes island %d n=%d" % (i, n))
+                    if scales.size:
+                        off = payload_scales_offset(codec, block, n)
+                        assert_bits_equal(ph[off:off + 4 * scales.size].view(np.float32), scales,
+                                          "scales island %d n=%d" % (i, n))
+                    enc.append((codes, scales))
+                t = orc.bridge_total(enc, codec, block, op, W)
+                want = t if dtype == "f32" else orc.f32_to_bf16_array(t)
+                for r in range(W):
+                    assert_bits_equal(to_host(bufs[r]), want, "%s %s n=%d %s rank %d" % (
+                        codec, sizes, n, op, r))
+                if I > 1:
+                    ref = orc.all_reduce(xs, sizes, op, codec, block)
+                    assert_bits_equal(to_host(bufs[0]), ref[0], "equals all_reduce n=%d" % n)

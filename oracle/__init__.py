@@ -86,6 +86,9 @@ def lib():
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.c_int, vp, vp, vp, c_size, ctypes.c_int, ctypes.c_int]
+        L.orc_all_reduce_sharded.restype = ctypes.c_int
+        L.orc_all_reduce_sharded.argtypes = [ctypes.c_int, vp, vp, vp, c_size, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, vp]
         L.orc_f16_to_f32.restype = ctypes.c_float
         L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_f32_to_f16.restype = ctypes.c_uint16
@@ -388,3 +391,23 @@ def all_reduce_ef(ranks, island_sizes, residuals, op="sum", codec="none", block:
     if rc:
         raise RuntimeError("oracle all_reduce_ef failed (%d)" % rc)
     return outs
+
+
+# ------------------------------------------------------------ sharded bridge
+
+def all_reduce_sharded(ranks, island_sizes, op="sum", codec="none", block: int = 256, with_segment=False):
+    """all_reduce under the sharded-bridge policy: k = smallest island size
+    segments of ceil(n / k) rounded up to 256 elements, each all_reduced over
+    its own link, then all_gathered.  Returns the outputs of every rank (and
+    the segment length with with_segment)."""
+    ranks = [np.ascontiguousarray(r) for r in ranks]
+    sizes = np.asarray(island_sizes, dtype=np.int32)
+    outs = [np.empty_like(r) for r in ranks]
+    pi, _k1 = _ptr_array(ranks)
+    po, _k2 = _ptr_array(outs)
+    seg = np.zeros(1, np.uint64)
+    rc = lib().orc_all_reduce_sharded(len(sizes), _ptr(sizes), pi, po, ranks[0].size, _dtype_id(ranks[0]),
+                                      _op_id(op), _codec_id(codec), block, _ptr(seg))
+    if rc:
+        raise RuntimeError("oracle all_reduce_sharded failed (%d)" % rc)
+    return (outs, int(seg[0])) if with_segment else outs

@@ -732,3 +732,70 @@ void orc_f32_to_f16_array(const float *x, size_t n, uint16_t *out)
     for (size_t j = 0; j < n; ++j)
         out[j] = orc_f32_to_f16(x[j]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* sharded-bridge                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* all_reduce under the sharded-bridge policy (gpubridge README, policy table,
+ * sharded-bridge row).  k is the size of the smallest island.  Each island
+ * reduce_scatters its sum onto its first k ranks, so that rank j of the
+ * island holds the island sum of segment j; rank j of every island then
+ * all_reduces segment j over its own bridge link (encode, exchange, decode
+ * and add in island order, AVG); each island finally all_gathers the
+ * segments to all its ranks.  With one island, or an island of one rank
+ * (k == 1), it is reduce-bridge-broadcast.
+ *
+ * Reading (the page does not say where the tensor is cut): segment j is
+ * [j * seg, (j + 1) * seg) with seg = ceil(n / k) rounded up to a multiple of
+ * 256 elements, so that every codec block lies inside one segment; trailing
+ * segments may be short or empty.  The codec blocks of a segment count from
+ * its first element.  *seg_out (if not NULL) receives seg (n for k == 1).
+ * dtype float32 or bf16. */
+int orc_all_reduce_sharded(int I, const int *island_sizes, const void *const *in, void *const *out,
+                           size_t n, int dtype, int op, int codec, int block, size_t *seg_out)
+{
+    int W = 0, k = island_sizes[0];
+    for (int i = 0; i < I; ++i) {
+        W += island_sizes[i];
+        if (island_sizes[i] < k)
+            k = island_sizes[i];
+    }
+    if (I == 1 || k == 1) {
+        if (seg_out)
+            *seg_out = n;
+        return orc_all_reduce(I, island_sizes, in, out, n, dtype, op, codec, block);
+    }
+    size_t seg = (n + (size_t)k - 1) / (size_t)k;
+    seg = (seg + 255) / 256 * 256;
+    if (seg_out)
+        *seg_out = seg;
+    const size_t eb = orc_dtype_bytes(dtype);
+    float *t = malloc((n ? n : 1) * sizeof(float));
+    const void **part = malloc(sizeof(void *) * (size_t)W);
+    if (!t || !part) {
+        free(t); free(part);
+        return -1;
+    }
+    for (int j = 0; j < k; ++j) {
+        const size_t e0 = (size_t)j * seg;
+        if (e0 >= n)
+            break;
+        const size_t m = (n - e0) < seg ? (n - e0) : seg;
+        for (int r = 0; r < W; ++r)
+            part[r] = (const uint8_t *)in[r] + e0 * eb;
+        /* rank j of each island: the island sum of segment j (the island
+         * reduce_scatter), encoded, exchanged over link j, decoded and added
+         * in island order */
+        if (orc_rbb_total(I, island_sizes, part, m, dtype, op, codec, block, t + e0, NULL, NULL, NULL)) {
+            free(t); free(part);
+            return -1;
+        }
+    }
+    /* island all_gather: every rank receives every segment */
+    for (int r = 0; r < W; ++r)
+        for (size_t j = 0; j < n; ++j)
+            store_elem(out[r], dtype, j, t[j]);
+    free(t); free(part);
+    return 0;
+}

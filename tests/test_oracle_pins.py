@@ -698,3 +698,54 @@ def test_float16_accumulates_and_divides_in_float32(op):
     want = (f32 if op == "sum" else f32 / np.float32(3)).astype(np.float16)
     for o in orc.all_reduce(xs, (3,), op):
         assert np.array_equal(o.view(np.uint16), want.view(np.uint16))
+
+
+# ------------------------------------------------------------ sharded bridge
+# gpubridge README, policy table, sharded-bridge row: k = smallest island size;
+# island reduce_scatter onto k ranks, rank j of every island all_reduces
+# segment j over its own link, island all_gather.
+
+@pytest.mark.parametrize("sizes,n,seg", [((2, 2), 1000, 512), ((4, 4), 6_553_600, 1_638_400),
+                                         ((3, 5), 1, 256), ((2, 3, 4), 513, 512), ((4, 2), 4097, 2304),
+                                         ((1, 3), 700, 700), ((4,), 900, 900)])
+def test_sharded_segment_length_is_the_reading(sizes, n, seg):
+    xs = [np.zeros(n, np.float32) for _ in range(sum(sizes))]
+    _, got = orc.all_reduce_sharded(xs, sizes, with_segment=True)
+    assert got == seg
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e4m3", 128),
+                                         ("e5m2", 128), ("e5m2", 256)])
+@pytest.mark.parametrize("sizes", [(2, 2), (3, 2), (4, 4), (2, 3, 4), (1, 3), (5,)])
+def test_sharded_equals_reduce_bridge_broadcast(codec, block, sizes):
+    """Codec blocks are local and every segment starts on a block boundary,
+    so cutting the tensor into segments changes no bit: the sharded result
+    equals reduce-bridge-broadcast for every codec, op, dtype and length,
+    short and empty trailing segments included."""
+    W = sum(sizes)
+    for n in (1, 255, 256, 257, 600, 3 * 256 + 5, 5000):
+        for dtype in ("f32", "bf16"):
+            w = wl.Workload("t", 40 + n % 7, tuple(sizes), dtype, "normal_1e-3_outliers", "sum", ())
+            xs = wl.host_rank_inputs(w, n=n)
+            for op in ("sum", "avg"):
+                got = orc.all_reduce_sharded(xs, sizes, op, codec, block)
+                want = orc.all_reduce(xs, sizes, op, codec, block)
+                for r in range(W):
+                    assert np.array_equal(got[r].view(np.uint8), want[r].view(np.uint8)), (n, dtype, op, r)
+
+
+@pytest.mark.parametrize("sizes", [(2, 2), (3, 4), (2, 2, 2)])
+@pytest.mark.parametrize("op", ["sum", "avg"])
+def test_sharded_integer_sums_are_exact(sizes, op):
+    """Integer-valued float32 inputs below 2^24 in magnitude: every segment's
+    uncompressed sum is the exact integer sum, and AVG its one correctly
+    rounded quotient by W, independent of where the segments fall."""
+    W = sum(sizes)
+    rng = np.random.default_rng(77)
+    n = 2000
+    xs = [rng.integers(-1000, 1001, n).astype(np.float32) for _ in range(W)]
+    exact = np.sum(np.stack(xs).astype(np.float64), axis=0)
+    want = exact if op == "sum" else exact / W
+    got = orc.all_reduce_sharded(xs, sizes, op, "none", 256)
+    for r in range(W):
+        assert np.array_equal(got[r], want.astype(np.float32)), r

@@ -59,6 +59,7 @@ def parse():
     p.add_argument("--chunk-kib", type=int, default=None,
                    help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
     p.add_argument("--no-graphs", action="store_true")
+    p.add_argument("--sharded", action="store_true", help="sharded-bridge policy for the timed step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--roofline-only", action="store_true",
                    help="only the per-kernel timed region (one bridge hop per call); for profiling")
@@ -272,6 +273,7 @@ def run_gb(args, world, rank, local, pg):
     launches, clk, t_wall, ms = 0, None, 0.0, None
     if not args.roofline_only:
         ctx.set_pipeline(chunk_bytes, not args.no_graphs)
+        ctx.set_sharded_bridge(args.sharded)
         with torch.cuda.stream(stream):
             for i in range(Wm):
                 step(i, False)
@@ -298,6 +300,7 @@ def run_gb(args, world, rank, local, pg):
     # around every phase on the launching stream.
     Kr = args.steps if args.roofline_only else min(K, 500)
     ctx.set_pipeline(0, False)
+    ctx.set_sharded_bridge(False)
     ctx.set_phase_timing(Kr)
     with torch.cuda.stream(stream):
         for i in range(Wm):
@@ -408,8 +411,11 @@ def run_gb(args, world, rank, local, pg):
                                    w.op, codec, w.block),
                    "ranks": W, "islands": list(w.island_sizes), "n": n, "codec": codec, "block": w.block,
                    "op": w.op,
-                   "policy": ("pipelined-reduce-bridge-broadcast, %d KiB payload chunks%s" % (
-                       chunk_bytes >> 10, ", CUDA graph replay" if not args.no_graphs else "")
+                   "policy": (("sharded-bridge, %d links%s" % (
+                       min(w.island_sizes), ", CUDA graph replay" if not args.no_graphs else ""))
+                              if args.sharded and min(w.island_sizes) > 1 else
+                              ("pipelined-reduce-bridge-broadcast, %d KiB payload chunks%s" % (
+                                  chunk_bytes >> 10, ", CUDA graph replay" if not args.no_graphs else ""))
                               if chunk_bytes else "reduce-bridge-broadcast"),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB "
                                      "read so that no dirty line is left); inputs restored from a device "

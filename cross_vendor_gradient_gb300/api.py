@@ -108,9 +108,14 @@ class Context:
         return B.gb_context_status(self.handle)
 
     def set_pipeline(self, chunk_bytes, use_graphs=True):
-        """chunk_bytes > 0: pipelined bridge in chunks of that many rank-buffer
-        bytes (default 4 MiB); 0: one bridge hop per call."""
+        """chunk_bytes > 0: pipelined bridge in chunks of about that many bytes
+        of one island's payload (default 2 MiB); 0: one bridge hop per call."""
         self._check(B.gb_set_pipeline(self.handle, chunk_bytes, use_graphs))
+
+    def set_sharded_bridge(self, on=True):
+        """Sharded-bridge policy for all_reduce: k = smallest island size
+        segments, each over its own bridge link (same bits)."""
+        self._check(B.gb_set_sharded_bridge(self.handle, on))
 
     def reserve(self, n, dtype=torch.float32, codec="none", block=256):
         self._check(B.gb_reserve(self.handle, n, _DTYPES[dtype], _codec(codec), block))

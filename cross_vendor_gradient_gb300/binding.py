@@ -61,6 +61,7 @@ SIGNATURES = {
     "gb_bridge_compress": (_i, [_vp, _vp, _sz, _i, _i, _vp, _vp]),
     "gb_bridge_decompress_accumulate": (_i, [_vp, _vp, _sz, _i, _i, _vp, _i, _vp]),
     "gb_island_broadcast": (_i, [_vp, _i, _vp, _sz, _i, _P(_vp), _i, _vp]),
+    "gb_set_sharded_bridge": (_i, [_vp, _i]),
     "gb_island_reduce_compress": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
     "gb_decompress_island_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
     "gb_all_reduce": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
@@ -187,6 +188,10 @@ def gb_bridge_decompress_accumulate(ctx, payload, n, codec, block, accum, accumu
 
 def gb_island_broadcast(ctx, island, total, n, op, rank_bufs, dtype, stream=0):
     return lib().gb_island_broadcast(ctx, island, total, n, op, _ptrs(rank_bufs), dtype, stream)
+
+
+def gb_set_sharded_bridge(ctx, on):
+    return lib().gb_set_sharded_bridge(ctx, 1 if on else 0)
 
 
 def gb_island_reduce_compress(ctx, rank_bufs, n, dtype, codec, block, payloads, stream=0):

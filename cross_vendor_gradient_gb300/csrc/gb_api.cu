@@ -22,6 +22,8 @@ constexpr int kMaxChunks = 32;
 // 2 bridge start, 3 bridge end, then decode start / end per chunk
 constexpr int kMarks = 4 + 2 * kMaxChunks;
 constexpr int kMaxGraphs = 16;
+// sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
+constexpr int kMaxLinks = 8;
 }  // namespace
 
 // Identity of a captured all_reduce (every value its graph bakes in).
@@ -30,7 +32,7 @@ struct GraphKey {
     const void *host[GB_MAX_RANKS];  // gb_all_reduce_host: the host rank buffers
     const void *res[GB_MAX_ISLANDS];
     uint64_t n, chunk;
-    int dtype, op, codec, block, timed, pad;
+    int dtype, op, codec, block, timed, links;
     const void *d_stage, *h_stage;
 };
 
@@ -73,6 +75,11 @@ struct gb_ctx {
     cudaEvent_t ev_k1[kMaxChunks] = {}, ev_d2h[kMaxChunks] = {}, ev_h2d[kMaxChunks] = {};
     cudaEvent_t ev_in[kMaxChunks] = {}, ev_k2[kMaxChunks] = {};  // host-buffer pipeline
     cudaEvent_t ev_join_d = nullptr, ev_join_h = nullptr;
+    // sharded-bridge policy: links 1 .. kMaxLinks - 1 (link 0 is sd / sh),
+    // created on first use, with their join events
+    int sharded = 0;
+    cudaStream_t lsd[kMaxLinks] = {}, lsh[kMaxLinks] = {};
+    cudaEvent_t ev_ljd[kMaxLinks] = {}, ev_ljh[kMaxLinks] = {};
     cudaEvent_t cap_mark[kMarks] = {};  // stand-ins recorded while capturing
     GraphEntry graphs[kMaxGraphs];
     int n_graphs = 0;
@@ -389,6 +396,7 @@ struct Plan {
     size_t eb = 4, cb = 4;
     uint64_t chunk = 0;
     int C = 1;
+    int links = 1;  // copy stream pairs the chunks' bridge copies are spread over
     size_t part = 0;
     size_t dev_bytes = 0, host_bytes = 0;
 };
@@ -401,7 +409,8 @@ size_t part_bytes(const Plan &p, uint64_t m) {
     return b;
 }
 
-Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs) {
+Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
+               bool sharded_ok = false) {
     Plan p;
     p.I = c->I;
     p.W = c->W;
@@ -414,7 +423,15 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
     p.eb = elem_bytes(dtype);
     p.cb = p.eff == GB_CODEC_NONE ? 4 : p.eff == GB_CODEC_BF16 ? 2 : 1;
     p.chunk = n;
-    if (!rs && c->I > 1 && c->chunk_bytes > 0) {
+    int k = c->I > 1 ? c->size[0] : 1;  // sharded-bridge: k = the smallest island's size
+    for (int i = 1; i < c->I; ++i)
+        if (c->size[i] < k) k = c->size[i];
+    if (sharded_ok && !rs && c->sharded && c->I > 1 && k > 1) {
+        // k segments of ceil(n / k) elements rounded up to whole tiles (so
+        // whole codec blocks), one per bridge link
+        const uint64_t seg = round_up((n + (uint64_t)k - 1) / (uint64_t)k, gb::kTile);
+        if (seg < n) p.chunk = seg;
+    } else if (!rs && c->I > 1 && c->chunk_bytes > 0) {
         // chunk_bytes of one island's payload per chunk
         const double per_elem = (double)p.cb + (is_fp8(p.eff) ? 4.0 / p.blk : 0.0);
         uint64_t ch = (uint64_t)((double)c->chunk_bytes / per_elem) / gb::kTile * gb::kTile;
@@ -424,6 +441,7 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         if (ch < n) p.chunk = ch;
     }
     p.C = (int)((n + p.chunk - 1) / p.chunk);
+    if (sharded_ok && !rs && c->sharded && c->I > 1 && k > 1) p.links = p.C < kMaxLinks ? p.C : kMaxLinks;
     p.part = round_up(part_bytes(p, p.chunk), 256);
     // received parts: two islands share one mirror of the host slots (leader
     // 1 holds island 0's part, leader 0 island 1's); more islands keep one
@@ -504,11 +522,19 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
             c->inject = 0;
             return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
         }
-        cudaStream_t D = multi ? c->sd : s, H = multi ? c->sh : s;
+        // chunk ch's copies run on link ch % links (sharded-bridge: one
+        // segment per link; otherwise one link for every chunk)
+        auto link_d = [&](int ch) { const int l = ch % p.links; return l ? c->lsd[l] : c->sd; };
+        auto link_h = [&](int ch) { const int l = ch % p.links; return l ? c->lsh[l] : c->sh; };
+        cudaStream_t D = s, H = s;
         for (int ch = 0; ch < p.C; ++ch) {
             const uint64_t e0 = (uint64_t)ch * p.chunk;
             const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
             const size_t pb = part_bytes(p, m);
+            if (multi) {
+                D = link_d(ch);
+                H = link_h(ch);
+            }
             if (multi) GB_TRY(wait_on(c, D, c->ev_k1[ch]));
             if (ch == 0) GB_TRY(mark(c, markmode, 2, D));
             GB_TRY(copy_async(c, host(ch, 0), outbox(ch, 0), (size_t)(I - 1) * p.part + pb, cudaMemcpyDeviceToHost, D));
@@ -529,6 +555,14 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
                 }
             }
             if (multi) GB_TRY(record(c, c->ev_h2d[ch], H));
+        }
+        if (multi && p.links > 1 && markmode != kMarkOff) {
+            // the bridge ends when every link's last copy has landed
+            H = link_h(0);
+            for (int l = 1; l < p.links && l < p.C; ++l) {
+                const int last = l + (p.C - 1 - l) / p.links * p.links;
+                GB_TRY(wait_on(c, H, c->ev_h2d[last]));
+            }
         }
         GB_TRY(mark(c, markmode, 3, H));
     }
@@ -576,6 +610,27 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         GB_TRY(record(c, c->ev_join_h, c->sh));
         GB_TRY(wait_on(c, s, c->ev_join_d));
         GB_TRY(wait_on(c, s, c->ev_join_h));
+        for (int l = 1; l < p.links; ++l) {
+            GB_TRY(record(c, c->ev_ljd[l], c->lsd[l]));
+            GB_TRY(record(c, c->ev_ljh[l], c->lsh[l]));
+            GB_TRY(wait_on(c, s, c->ev_ljd[l]));
+            GB_TRY(wait_on(c, s, c->ev_ljh[l]));
+        }
+    }
+    return GB_OK;
+}
+
+// Copy stream pairs 1 .. L - 1 of the sharded-bridge policy, created on
+// first use (link 0 is the pipelined policy's pair).
+gb_status ensure_links(gb_ctx *c, int L) {
+    for (int l = 1; l < L && l < kMaxLinks; ++l) {
+        if (c->lsd[l]) continue;
+        cudaError_t e;
+        if ((e = cudaStreamCreateWithFlags(&c->lsd[l], cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&c->lsh[l], cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->ev_ljd[l], cudaEventDisableTiming)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&c->ev_ljh[l], cudaEventDisableTiming)) != cudaSuccess)
+            return fail(c, GB_ERR_CUDA, "bridge link streams", e);
     }
     return GB_OK;
 }
@@ -1021,7 +1076,8 @@ gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
                   gb_op op, gb_codec codec, int block, cudaStream_t s, int rs, float *const *res = nullptr) {
     if (is_exact(dtype, op)) return run_exact(c, in, out, n, dtype, op, s, rs);
-    const Plan p = make_plan(c, n, dtype, op, codec, block, rs);
+    const Plan p = make_plan(c, n, dtype, op, codec, block, rs, true);
+    GB_TRY(ensure_links(c, p.links));
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
     if (p.host_bytes) GB_TRY(grow_host(c, p.host_bytes));
     GB_TRY(begin(c, s));
@@ -1043,6 +1099,7 @@ gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, 
     k.codec = p.eff;
     k.block = p.blk;
     k.timed = timed;
+    k.links = p.links;
     k.d_stage = c->d_stage;
     k.h_stage = c->h_stage;
     GraphEntry *ge = find_graph(c, k);
@@ -1136,6 +1193,12 @@ gb_status gb_destroy(gb_ctx *c) {
         }
         if (c->ev_join_d) cudaEventDestroy(c->ev_join_d);
         if (c->ev_join_h) cudaEventDestroy(c->ev_join_h);
+        for (int l = 1; l < kMaxLinks; ++l) {
+            if (c->lsd[l]) cudaStreamDestroy(c->lsd[l]);
+            if (c->lsh[l]) cudaStreamDestroy(c->lsh[l]);
+            if (c->ev_ljd[l]) cudaEventDestroy(c->ev_ljd[l]);
+            if (c->ev_ljh[l]) cudaEventDestroy(c->ev_ljh[l]);
+        }
         for (int i = 0; i < kMarks; ++i)
             if (c->cap_mark[i]) cudaEventDestroy(c->cap_mark[i]);
         if (cur >= 0 && cur != c->device) cudaSetDevice(cur);
@@ -1187,7 +1250,7 @@ gb_status gb_reserve(gb_ctx *c, size_t n, gb_dtype dtype, gb_codec codec, int bl
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
     GB_TRY(bind(c));
-    const Plan ar = make_plan(c, n, dtype, GB_SUM, codec, block, 0);
+    const Plan ar = make_plan(c, n, dtype, GB_SUM, codec, block, 0, true);
     const Plan rs = make_plan(c, n, dtype, GB_SUM, codec, block, 1);
     const size_t ag_host = (size_t)c->W * n * elem_bytes(dtype);
     size_t dev = ar.dev_bytes > rs.dev_bytes ? ar.dev_bytes : rs.dev_bytes;
@@ -1208,6 +1271,14 @@ gb_status gb_set_pipeline(gb_ctx *c, size_t chunk_bytes, int use_graphs) {
     drop_graphs(c);
     c->chunk_bytes = chunk_bytes;
     c->use_graphs = use_graphs ? 1 : 0;
+    return GB_OK;
+}
+
+gb_status gb_set_sharded_bridge(gb_ctx *c, int on) {
+    if (!c) return GB_ERR_INVALID_ARG;
+    if (c->device >= 0 && c->done_recorded) cudaEventSynchronize(c->done);
+    drop_graphs(c);
+    c->sharded = on ? 1 : 0;
     return GB_OK;
 }
 
@@ -1649,7 +1720,7 @@ gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bu
     size_t total = 0;
     for (int b = 0; b < n_buckets; ++b) total += bucket_numel[b];
     if (total == 0) return GB_OK;
-    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
+    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0 && !c->sharded) {
         GB_TRY(bind(c));
         return run_buckets(c, n_buckets, bucket_bufs, bucket_numel, dtype, op, codec, block, (cudaStream_t)stream);
     }

@@ -172,6 +172,22 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  * the context's outstanding work. */
 gb_status gb_set_pipeline(gb_ctx *ctx, size_t chunk_bytes, int use_graphs);
 
+/* The sharded-bridge policy of gb_all_reduce and gb_all_reduce_ef (gpubridge
+ * README, policy table, sharded-bridge row), on (on != 0) or off (default).
+ * k = the size of the smallest island.  Each island's sum is cut into k
+ * segments of ceil(n / k) elements rounded up to whole 256-element tiles
+ * (whole codec blocks; trailing segments may be short or absent); rank j of
+ * every island encodes segment j of its island sum, all_reduces it with the
+ * other islands over its own bridge link (a pinned host slot and a pair of
+ * copy streams; segment j uses link j mod 8), and every island gathers the
+ * segments into all its ranks.  The result is the same bits as
+ * reduce-bridge-broadcast.  With one island, or an island of one rank
+ * (k == 1), the call falls back to the gb_set_pipeline policy.  use_graphs of
+ * gb_set_pipeline applies.  gb_all_reduce_host, gb_reduce_scatter and, while
+ * this policy is on, gb_all_reduce_buckets bucket by bucket keep one link.
+ * Waits for the context's outstanding work. */
+gb_status gb_set_sharded_bridge(gb_ctx *ctx, int on);
+
 /* The context's sticky status (GB_OK until a call fails after enqueueing)
  * and a one-line description of the last error on this context. */
 gb_status gb_context_status(const gb_ctx *ctx);

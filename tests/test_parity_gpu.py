@@ -453,3 +453,91 @@ def test_fused_halves_match_oracle(codec, block, sizes, dtype):
                 if I > 1:
                     ref = orc.all_reduce(xs, sizes, op, codec, block)
                     assert_bits_equal(to_host(bufs[0]), ref[0], "equals all_reduce n=%d" % n)
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e4m3", 128),
+                                         ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(2, 2), (4, 4), (3, 5), (2, 3, 4), (8, 8), (1, 3), (6,)])
+@pytest.mark.parametrize("graphs", [True, False])
+def test_sharded_bridge_matches_oracle(codec, block, sizes, graphs):
+    """sharded-bridge policy: k = smallest island size segments, each over its
+    own link; bit-identical to the oracle's sharded all_reduce (and so to
+    reduce-bridge-broadcast), direct, captured and replayed."""
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(2 << 20, graphs)
+        ctx.set_sharded_bridge(True)
+        for n in (1, 255, 257, 5000, 40000):
+            for dtype in ("f32", "bf16"):
+                for op in ("sum", "avg"):
+                    xs = inputs(sizes, n, dtype, cid=50 + n % 11)
+                    want = orc.all_reduce_sharded(xs, sizes, op, codec, block)
+                    bufs = [to_dev(x) for x in xs]
+                    pristine = [b.clone() for b in bufs]
+                    for call in range(3):  # direct, then captured, then replayed
+                        for b, p in zip(bufs, pristine):
+                            b.copy_(p)
+                        ctx.all_reduce(bufs, op, codec, block)
+                        torch.cuda.synchronize()
+                        for r in range(W):
+                            assert_bits_equal(to_host(bufs[r]), want[r], "%s %s n=%d %s %s call %d rank %d" % (
+                                codec, sizes, n, dtype, op, call, r))
+
+
+def test_sharded_bridge_timing_ef_and_other_calls():
+    """Phase marks span every link; error feedback and the calls that keep
+    one link (reduce_scatter, host buffers, buckets) stay bit-exact."""
+    sizes, codec, block, n = (4, 4), "e4m3", 256, 70000
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        ctx.set_sharded_bridge(True)
+        ctx.set_phase_timing(4)
+        xs = inputs(sizes, n, "f32", cid=61)
+        for _ in range(2):
+            bufs = [to_dev(x) for x in xs]
+            ctx.all_reduce(bufs, "sum", codec, block)
+        torch.cuda.synchronize()
+        k1, br, k2 = ctx.phase_times(0)
+        assert k1 > 0 and br > 0 and k2 > 0
+        want = orc.all_reduce(xs, sizes, "sum", codec, block)
+        for r in range(W):
+            assert_bits_equal(to_host(bufs[r]), want[r], "timed rank %d" % r)
+        ctx.set_phase_timing(0)
+        # error feedback over three steps
+        res_h = [np.zeros(n, np.float32) for _ in sizes]
+        res_d = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in sizes]
+        for step in range(3):
+            xs = inputs(sizes, n, "f32", cid=70 + step)
+            bufs = [to_dev(x) for x in xs]
+            ctx.all_reduce_ef(bufs, res_d, "avg", codec, block)
+            want = orc.all_reduce_ef(xs, sizes, res_h, "avg", codec, block)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(bufs[r]), want[r], "ef step %d rank %d" % (step, r))
+            for i in range(len(sizes)):
+                assert_bits_equal(to_host(res_d[i]), res_h[i], "ef residual %d" % i)
+        # reduce_scatter and host buffers
+        nr = 8 * 1000
+        xs = inputs(sizes, nr, "f32", cid=81)
+        outs = [torch.empty(nr // W, dtype=torch.float32, device="cuda") for _ in range(W)]
+        ctx.reduce_scatter([to_dev(x) for x in xs], outs, "sum", codec, block)
+        want = orc.reduce_scatter(xs, sizes, "sum", codec, block)
+        host = [torch.from_numpy(x.copy()).pin_memory() for x in xs]
+        ctx.all_reduce_host(host, "sum", codec, block)
+        torch.cuda.synchronize()
+        want_ar = orc.all_reduce(xs, sizes, "sum", codec, block)
+        for r in range(W):
+            assert_bits_equal(to_host(outs[r]), want[r], "rs rank %d" % r)
+            assert_bits_equal(host[r].numpy(), want_ar[r], "host rank %d" % r)
+        # bucketed, bucket by bucket under this policy
+        numels = [5000, 0, 257, 40000]
+        sets = [inputs(sizes, max(m, 1), "f32", cid=90 + b)[:W] for b, m in enumerate(numels)]
+        buckets = [[to_dev(x[:m]) for x in xs_b] for xs_b, m in zip(sets, numels)]
+        ctx.all_reduce_buckets(buckets, "sum", codec, block)
+        torch.cuda.synchronize()
+        for b, m in enumerate(numels):
+            if m == 0:
+                continue
+            want = orc.all_reduce([x[:m] for x in sets[b]], sizes, "sum", codec, block)
+            for r in range(W):
+                assert_bits_equal(to_host(buckets[b][r]), want[r], "bucket %d rank %d" % (b, r))

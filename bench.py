@@ -342,6 +342,11 @@ def run_gb(args, world, rank, local, pg):
         ins = [[p.clone() for p in pristine] for _ in range(S)]
         outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
         pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
+        # every leader decodes the same I payloads: in a step the received
+        # parts were written by the host -> device copy just before the
+        # decode and are still in L2, so only one read of each part comes
+        # from DRAM there too
+        rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
         Kk = max(3, min(Kr, 50))
         ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kk)]
         with torch.cuda.stream(stream):
@@ -358,7 +363,7 @@ def run_gb(args, world, rank, local, pg):
                 if e:
                     e[1].record(stream)
                 for q in range(S):
-                    ctx.decompress_island_broadcast(pays[q], w.op, codec, w.block, outs[q], stream=stream)
+                    ctx.decompress_island_broadcast(rows[q], w.op, codec, w.block, outs[q], stream=stream)
                     if e and q == 0:
                         e[2].record(stream)
                 if e:
@@ -367,7 +372,7 @@ def run_gb(args, world, rank, local, pg):
         ks = {"sets": S, "timed_launches_per_batch": S - 1, "batches": Kk, "set_bytes": set_bytes,
               names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
               names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
-        del ins, outs, pays
+        del ins, outs, pays, rows
     if ks:
         r1, r2 = ks[names[0]], ks[names[1]]
         region = ("timed region 3: each kernel launched back to back over %d input sets (%.0f MB each, "

@@ -198,8 +198,12 @@ class Context:
 
     def decompress_island_broadcast(self, payloads, op, codec, block, tensors, stream=None):
         """Fused decode of every island's payload + accumulate + broadcast
-        into all rank tensors."""
+        into all rank tensors.  payloads: I tensors (every leader holds the
+        same ones) or I * I (row g: what leader g holds, island order)."""
         dt = _dtype(tensors)
+        I = len(self.island_sizes)
+        if len(payloads) == I and I > 1:  # one shared set: every leader's row
+            payloads = [p for _ in range(I) for p in payloads]
         self._check(B.gb_decompress_island_broadcast(self.handle, [p.data_ptr() for p in payloads],
                                                      tensors[0].numel(), dt, _op(op), _codec(codec), block,
                                                      [t.data_ptr() for t in tensors], _stream(stream)))

@@ -1417,7 +1417,7 @@ gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads,
         return set_msg(c, GB_ERR_UNSUPPORTED_OP, "decompress + island broadcast takes SUM / AVG");
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
-    GB_TRY(check_dev_bufs(c, payloads, c->I, "payloads"));
+    GB_TRY(check_dev_bufs(c, payloads, c->I * c->I, "payloads"));
     GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
@@ -1429,7 +1429,7 @@ gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads,
         da.group_of_rank[r] = c->island_of[r];
     }
     for (int g = 0; g < c->I; ++g)
-        for (int j = 0; j < c->I; ++j) da.payload[g][j] = payloads[j];
+        for (int j = 0; j < c->I; ++j) da.payload[g][j] = payloads[g * c->I + j];
     for (int i = 0; i <= c->I; ++i) da.first[i] = c->first[i];
     da.n_groups = c->I;
     da.n_src = c->I;

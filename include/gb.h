@@ -254,12 +254,15 @@ gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_
  * 32-byte aligned, owned by the caller.  dtype F32 or BF16.  One kernel
  * launch for all islands, stream-ordered on `stream`.
  *
- * gb_decompress_island_broadcast: every rank buffer receives
- * t = dec(payloads[0]) + ... + dec(payloads[I - 1]) in float32, island
- * order, divided by W for AVG (float32 division), rounded to dtype (nearest
- * even for bf16).  With the payloads of gb_island_reduce_compress, carried
- * bit for bit, this is what gb_all_reduce writes.  op SUM or AVG.  One
- * kernel launch.
+ * gb_decompress_island_broadcast: payloads holds I * I device pointers,
+ * row g being what leader g holds after the bridge: payloads[g * I + j] is
+ * island j's payload (its own for j == g), and the same pointer may appear
+ * in several rows.  Every rank of island g receives
+ * t = dec(payloads[g * I + 0]) + ... + dec(payloads[g * I + I - 1]) in
+ * float32, island order, divided by W for AVG (float32 division), rounded to
+ * dtype (nearest even for bf16).  With the payloads of
+ * gb_island_reduce_compress, carried bit for bit, this is what gb_all_reduce
+ * writes.  op SUM or AVG.  One kernel launch.
  *
  * Errors as for gb_all_reduce; n == 0 is a no-op.  Neither call allocates. */
 gb_status gb_island_reduce_compress(gb_ctx *ctx, const void *const *rank_bufs, size_t n, gb_dtype dtype,

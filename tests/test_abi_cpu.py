@@ -136,11 +136,13 @@ def test_argument_errors_need_no_device():
         assert B.gb_island_reduce_compress(ctx, fake, 10, 0, 2, 64, pl) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_island_reduce_compress(ctx, fake, 10, 0, 2, 256, [pl[0], 0]) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce_compress(ctx, fake, 10, 0, 2, 256, [pl[0], pl[1] + 16]) == B.GB_ERR_MISALIGNED
-        assert B.gb_decompress_island_broadcast(ctx, pl, 10, 0, B.GB_MAX, 2, 256, fake) == B.GB_ERR_UNSUPPORTED_OP
-        assert B.gb_decompress_island_broadcast(ctx, pl, 10, 0, 0, 7, 256, fake) == B.GB_ERR_UNSUPPORTED_CODEC
-        assert B.gb_decompress_island_broadcast(ctx, pl, 10, 0, 0, 2, 256, fake[:3] + [0]) == B.GB_ERR_INVALID_ARG
+        pl4 = pl + pl[::-1]  # every leader's row
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, B.GB_MAX, 2, 256, fake) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, 0, 7, 256, fake) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, 0, 2, 256, fake[:3] + [0]) == B.GB_ERR_INVALID_ARG
+        assert B.gb_decompress_island_broadcast(ctx, pl4[:3] + [0], 10, 0, 0, 2, 256, fake) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce_compress(ctx, fake, 0, 0, 2, 256, pl) == B.GB_OK
-        assert B.gb_decompress_island_broadcast(ctx, pl, 0, 1, 1, 3, 128, fake) == B.GB_OK
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 0, 1, 1, 3, 128, fake) == B.GB_OK
         # n == 0 is a valid no-op, answered without a device
         assert B.gb_all_reduce(ctx, fake, 0, 0, 0, 2, 256) == B.GB_OK
         assert B.gb_all_gather(ctx, fake, fake, 0, 1) == B.GB_OK

@@ -429,8 +429,11 @@ def test_fused_halves_match_oracle(codec, block, sizes, dtype):
                 P = payload_bytes(codec, block, n)
                 pay = [torch.empty(P, dtype=torch.uint8, device="cuda") for _ in range(I)]
                 ctx.island_reduce_compress(bufs, codec, block, pay)
-                moved = [p.clone() for p in pay]  # the caller's own bridge
-                ctx.decompress_island_broadcast(moved, op, codec, block, bufs)
+                # the caller's own bridge: every leader receives its own copy
+                # of every other island's payload (row g, island order)
+                rows = [pay[j] if j == g else pay[j].clone() for g in range(I) for j in range(I)]
+                # (the shared-set form, I payloads, for AVG)
+                ctx.decompress_island_broadcast(rows if op == "sum" else pay, op, codec, block, bufs)
                 torch.cuda.synchronize()
                 cd = orc.code_dtype(codec)
                 cb = np.dtype(cd).itemsize

@@ -577,7 +577,8 @@ def run_buckets_bench(args, world, rank, local, pg):
         torch.cuda.synchronize()
         ms_rs = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Ks)]))
         per = sum(bn) * w.elem_bytes
-        rs_line = {"what": "reduce_scatter then all_gather of every bucket, one bridge hop per call",
+        rs_line = {"what": "reduce_scatter then all_gather of every bucket, pipelined policy (%d KiB payload "
+                           "chunks; all_gather in groups of whole rank blocks)" % (chunk_bytes >> 10),
                    "ms_per_step": ms_rs, "value": per / (ms_rs * 1e-3) / 1e9, "unit": "GB/s", "steps": Ks}
         del slices
     # roofline region: one hop per bucket, phase marks around every kernel

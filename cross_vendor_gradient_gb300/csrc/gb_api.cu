@@ -75,6 +75,7 @@ struct gb_ctx {
     cudaEvent_t ev_k1[kMaxChunks] = {}, ev_d2h[kMaxChunks] = {}, ev_h2d[kMaxChunks] = {};
     cudaEvent_t ev_in[kMaxChunks] = {}, ev_k2[kMaxChunks] = {};  // host-buffer pipeline
     cudaEvent_t ev_join_d = nullptr, ev_join_h = nullptr;
+    cudaEvent_t ev_ag[GB_MAX_RANKS] = {};  // all_gather: one per group of rank blocks
     // sharded-bridge policy: links 1 .. kMaxLinks - 1 (link 0 is sd / sh),
     // created on first use, with their join events
     int sharded = 0;
@@ -231,6 +232,9 @@ gb_status bind(gb_ctx *c) {
         if ((e = cudaEventCreateWithFlags(&c->ev_join_d, cudaEventDisableTiming)) != cudaSuccess ||
             (e = cudaEventCreateWithFlags(&c->ev_join_h, cudaEventDisableTiming)) != cudaSuccess)
             return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+        for (int i = 0; i < GB_MAX_RANKS; ++i)
+            if ((e = cudaEventCreateWithFlags(&c->ev_ag[i], cudaEventDisableTiming)) != cudaSuccess)
+                return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
         for (int i = 0; i < kMarks; ++i)
             if ((e = cudaEventCreate(&c->cap_mark[i])) != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
         c->device = dev;
@@ -431,7 +435,7 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         // whole codec blocks), one per bridge link
         const uint64_t seg = round_up((n + (uint64_t)k - 1) / (uint64_t)k, gb::kTile);
         if (seg < n) p.chunk = seg;
-    } else if (!rs && c->I > 1 && c->chunk_bytes > 0) {
+    } else if (c->I > 1 && c->chunk_bytes > 0) {
         // chunk_bytes of one island's payload per chunk
         const double per_elem = (double)p.cb + (is_fp8(p.eff) ? 4.0 / p.blk : 0.0);
         uint64_t ch = (uint64_t)((double)c->chunk_bytes / per_elem) / gb::kTile * gb::kTile;
@@ -579,6 +583,21 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
             da.dst[r] = (unsigned char *)out[r] + (p.rs ? 0 : e0 * p.eb);
             da.group_of_rank[r] = c->island_of[r];
         }
+        uint64_t rs_max = 0;
+        if (p.rs) {  // the parts of the slices that fall inside this chunk
+            const uint64_t ms = p.n / (uint64_t)p.W;
+            for (int r = 0; r < p.W; ++r) {
+                const uint64_t s0 = (uint64_t)r * ms;
+                const uint64_t lo = e0 > s0 ? e0 : s0;
+                const uint64_t hi = (e0 + m) < (s0 + ms) ? (e0 + m) : (s0 + ms);
+                if (hi > lo) {
+                    da.rs_src[r] = lo - e0;
+                    da.rs_len[r] = hi - lo;
+                    da.dst[r] = (unsigned char *)out[r] + (lo - s0) * p.eb;
+                    if (hi - lo > rs_max) rs_max = hi - lo;
+                }
+            }
+        }
         for (int g = 0; g < I; ++g)
             for (int j = 0; j < I; ++j)
                 da.payload[g][j] = (j == g) ? (const void *)outbox(ch, j) : (const void *)inbox(g, ch, j);
@@ -591,11 +610,10 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         da.inv_world = 1.0f / (float)p.W;
         da.n = m;
         da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
-        if (p.rs) {  // one chunk: slices of the full range
+        if (p.rs) {
             da.rs = 1;
-            da.m = p.n / (uint64_t)p.W;
-            da.vec = (da.m % 8) == 0;
-            da.tiles = (uint32_t)((da.m + gb::kTile - 1) / gb::kTile);
+            da.vec = ((p.n / (uint64_t)p.W) % 8) == 0;
+            da.tiles = (uint32_t)((rs_max + gb::kTile - 1) / gb::kTile);
         } else {
             da.rs = 0;
             da.vec = 1;
@@ -1056,9 +1074,13 @@ gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n
     da.n = n;
     const uint64_t V = 16 / elem_bytes(dtype);
     if (rs) {
+        const uint64_t m = n / (uint64_t)W;
         da.rs = 1;
-        da.m = n / (uint64_t)W;
-        da.vec = (da.m % V) == 0;
+        for (int r = 0; r < W; ++r) {
+            da.rs_src[r] = (uint64_t)r * m;
+            da.rs_len[r] = m;
+        }
+        da.vec = (m % V) == 0;
     } else {
         da.vec = 1;
     }
@@ -1193,6 +1215,8 @@ gb_status gb_destroy(gb_ctx *c) {
         }
         if (c->ev_join_d) cudaEventDestroy(c->ev_join_d);
         if (c->ev_join_h) cudaEventDestroy(c->ev_join_h);
+        for (int i = 0; i < GB_MAX_RANKS; ++i)
+            if (c->ev_ag[i]) cudaEventDestroy(c->ev_ag[i]);
         for (int l = 1; l < kMaxLinks; ++l) {
             if (c->lsd[l]) cudaStreamDestroy(c->lsd[l]);
             if (c->lsh[l]) cudaStreamDestroy(c->lsh[l]);
@@ -1505,15 +1529,48 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
             return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
         }
         GB_TRY(mark(c, mm, 2, s));
-        // every rank's block goes to the host slots ...
-        for (int q = 0; q < W; ++q)
-            GB_TRY(copy_async(c, c->h_stage + (size_t)q * mb, in[q], mb, cudaMemcpyDeviceToHost, s));
-        // ... and each leader receives the other islands' blocks in place
-        for (int i = 0; i < I; ++i) {
-            unsigned char *lead = (unsigned char *)out[c->first[i]];
-            const size_t lo = (size_t)c->first[i] * mb, hi = (size_t)c->first[i + 1] * mb;
-            GB_TRY(copy_async(c, lead, c->h_stage, lo, cudaMemcpyHostToDevice, s));
-            GB_TRY(copy_async(c, lead + hi, c->h_stage + hi, (size_t)W * mb - hi, cudaMemcpyHostToDevice, s));
+        if (c->chunk_bytes == 0) {
+            // one hop on the caller's stream: every rank's block goes to the
+            // host slots, then each leader receives the other islands' blocks
+            for (int q = 0; q < W; ++q)
+                GB_TRY(copy_async(c, c->h_stage + (size_t)q * mb, in[q], mb, cudaMemcpyDeviceToHost, s));
+            for (int i = 0; i < I; ++i) {
+                unsigned char *lead = (unsigned char *)out[c->first[i]];
+                const size_t lo = (size_t)c->first[i] * mb, hi = (size_t)c->first[i + 1] * mb;
+                GB_TRY(copy_async(c, lead, c->h_stage, lo, cudaMemcpyHostToDevice, s));
+                GB_TRY(copy_async(c, lead + hi, c->h_stage + hi, (size_t)W * mb - hi, cudaMemcpyHostToDevice, s));
+            }
+        } else {
+            // pipelined: groups of consecutive ranks of one island (about
+            // chunk_bytes each) go to the host on copy stream D; as soon as
+            // a group has landed, stream H carries it to every other leader
+            const size_t per_s = mb >= c->chunk_bytes ? 1 : c->chunk_bytes / mb;
+            const int per = per_s > (size_t)W ? W : (int)per_s;
+            cudaStream_t D = c->sd, H = c->sh;
+            GB_TRY(record(c, c->ev_join_d, s));  // the copy streams start after the caller's prior work
+            GB_TRY(wait_on(c, D, c->ev_join_d));
+            GB_TRY(wait_on(c, H, c->ev_join_d));
+            int ng = 0;
+            for (int i = 0; i < I; ++i) {
+                for (int q0 = c->first[i]; q0 < c->first[i + 1]; q0 += per) {
+                    const int q1 = (q0 + per) < c->first[i + 1] ? (q0 + per) : c->first[i + 1];
+                    for (int q = q0; q < q1; ++q)
+                        GB_TRY(copy_async(c, c->h_stage + (size_t)q * mb, in[q], mb, cudaMemcpyDeviceToHost, D));
+                    GB_TRY(record(c, c->ev_ag[ng], D));
+                    GB_TRY(wait_on(c, H, c->ev_ag[ng]));
+                    ++ng;
+                    for (int g = 0; g < I; ++g) {
+                        if (g == i) continue;
+                        unsigned char *lead = (unsigned char *)out[c->first[g]];
+                        GB_TRY(copy_async(c, lead + (size_t)q0 * mb, c->h_stage + (size_t)q0 * mb,
+                                          (size_t)(q1 - q0) * mb, cudaMemcpyHostToDevice, H));
+                    }
+                }
+            }
+            GB_TRY(record(c, c->ev_join_d, D));
+            GB_TRY(record(c, c->ev_join_h, H));
+            GB_TRY(wait_on(c, s, c->ev_join_d));
+            GB_TRY(wait_on(c, s, c->ev_join_h));
         }
         GB_TRY(mark(c, mm, 3, s));
     }

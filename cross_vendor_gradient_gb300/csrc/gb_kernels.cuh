@@ -31,10 +31,12 @@ struct ReduceEncodeArgs {
 // rounds to the rank dtype and writes the result.
 //   all_reduce (rs == 0): unit = group g; every rank buffer
 //     dst[first[g] .. first[g+1]) receives the same elements;
-//   reduce_scatter (rs == 1): unit = rank r; global elements
-//     [r*m, (r+1)*m) go to dst[r]; group g = the island of r.  vec == 0
-//     forces the element-wise path (used when m is not a multiple of 8,
-//     which would misalign the vector accesses).
+//   reduce_scatter (rs == 1): unit = rank r; the unit's rs_len[r] elements
+//     start at payload element rs_src[r] and go to dst[r] (the host offsets
+//     dst[r] to the slice position they land on); group g = the island of
+//     r.  One chunk of the pipeline covers the parts of the slices that fall
+//     inside it.  vec == 0 forces the element-wise path (used when the slice
+//     length is not a multiple of 8, which would misalign vector accesses).
 struct DecodeBcastArgs {
     void *dst[GB_MAX_RANKS];
     const void *payload[GB_MAX_ISLANDS][GB_MAX_ISLANDS];
@@ -50,8 +52,9 @@ struct DecodeBcastArgs {
     uint64_t scales_off;
     int rs;
     int vec;
-    uint64_t m;      // reduce_scatter slice length
-    uint32_t tiles;  // all_reduce: tiles per group; reduce_scatter: tiles per slice
+    uint64_t rs_src[GB_MAX_RANKS];  // reduce_scatter: first payload element of unit r
+    uint64_t rs_len[GB_MAX_RANKS];  // reduce_scatter: elements of unit r (0: none)
+    uint32_t tiles;  // all_reduce: tiles per group; reduce_scatter: tiles of the longest unit
 };
 
 // accum = dec(payload) or accum + dec(payload).

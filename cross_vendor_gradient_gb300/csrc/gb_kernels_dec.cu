@@ -181,8 +181,8 @@ __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ De
         g = a.group_of_rank[u];
         r_lo = u;
         r_hi = u + 1;
-        gofs = (uint64_t)u * a.m;
-        limit = a.m;
+        gofs = a.rs_src[u];
+        limit = a.rs_len[u];
     } else {
         g = u;
         r_lo = a.first[g];

@@ -158,8 +158,8 @@ __global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ D
         g = a.group_of_rank[u];
         r_lo = u;
         r_hi = u + 1;
-        gofs = (uint64_t)u * a.m;
-        limit = a.m;
+        gofs = a.rs_src[u];
+        limit = a.rs_len[u];
     } else {
         g = u;
         r_lo = a.first[g];
@@ -231,8 +231,13 @@ static cudaError_t launch_pair(bool combine, const void *args, cudaStream_t s) {
         return launch_vec<k_exact_reduce<T, OP>>((a.n + N - 1) / N, (unsigned)a.n_islands, a, s);
     }
     const DecodeBcastArgs &a = *(const DecodeBcastArgs *)args;
-    const uint64_t limit = a.rs ? a.m : a.n;
     const unsigned units = a.rs ? (unsigned)a.first[a.n_groups] : (unsigned)a.n_groups;
+    uint64_t limit = a.n;
+    if (a.rs) {  // the longest unit
+        limit = 0;
+        for (unsigned u = 0; u < units; ++u)
+            if (a.rs_len[u] > limit) limit = a.rs_len[u];
+    }
     return launch_vec<k_exact_combine<T, OP>>((limit + N - 1) / N, units, a, s);
 }
 

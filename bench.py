@@ -62,7 +62,8 @@ def parse():
     p.add_argument("--sharded", action="store_true", help="sharded-bridge policy for the timed step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--roofline-only", action="store_true",
-                   help="only the per-kernel timed region (one bridge hop per call); for profiling")
+                   help="only the per-kernel timed regions (kernels inside one-hop steps, and back to "
+                        "back); for profiling")
     p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
     return p.parse_args()
 

@@ -7,10 +7,13 @@
 // once by the world size (API table, all_reduce row); the total, rounded to
 // the rank dtype, goes to every rank of the island.
 //
-// How: one warp per 256-element tile per output group (grid y), 8 contiguous
-// elements per lane; the payloads of a tile are all loaded before the first
-// add (compile-time count for 1 or 2 islands); the result leaves as one
-// 32-byte (float32) or 16-byte (bf16) streaming store per lane per rank.
+// How: one warp per 256-element tile per output unit (grid y: an island's
+// group of ranks, or one rank for reduce_scatter), 8 contiguous elements per
+// lane; the payloads of a tile are all loaded before the first add
+// (compile-time count for 1 or 2 islands), and for those counts the loads of
+// the warp's next tile are issued before the current one is decoded and
+// stored; the result leaves as one 32-byte (float32) or 16-byte (bf16)
+// streaming store per lane per rank.
 #include <atomic>
 #include <cuda_runtime.h>
 

@@ -100,3 +100,38 @@ def test_host_entry_point_leaves_host_guards():
         torch.cuda.synchronize()
         for r in raw:
             assert torch.all(r[:32] == 7.0) and torch.all(r[32 + n:] == 7.0)
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(2, 2), (2, 1, 3)])
+def test_newer_entry_points_stay_in_bounds(codec, block, sizes):
+    """The fused halves, the sharded-bridge policy, the bucket pipeline and
+    error feedback write nothing outside their buffers."""
+    W, I = sum(sizes), len(sizes)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(1024, True)
+        for n in (1, 9, 257, 5001, 40003):
+            ranks = [Guarded(n, torch.float32) for _ in range(W)]
+            for r, g in enumerate(ranks):
+                fill(g, 20 + r)
+            pays = [Guarded(payload_bytes(codec, block, n), torch.uint8) for _ in range(I)]
+            ctx.island_reduce_compress([g.t for g in ranks], codec, block, [p.t for p in pays])
+            ctx.decompress_island_broadcast([p.t for p in pays], "avg", codec, block, [g.t for g in ranks])
+            ctx.set_sharded_bridge(True)
+            for _ in range(2):
+                ctx.all_reduce([g.t for g in ranks], "sum", codec, block)
+            res = [Guarded(n, torch.float32) for _ in range(I)]
+            for g in res:
+                g.t.zero_()
+            ctx.all_reduce_ef([g.t for g in ranks], [g.t for g in res], "sum", codec, block)
+            ctx.set_sharded_bridge(False)
+            numels = [n, 3, n // 2 + 1]
+            buckets = [[Guarded(m, torch.bfloat16) for _ in range(W)] for m in numels]
+            for b, row in enumerate(buckets):
+                for r, g in enumerate(row):
+                    fill(g, 100 * b + r)
+            for _ in range(2):
+                ctx.all_reduce_buckets([[g.t for g in row] for row in buckets], "sum", codec, block)
+            torch.cuda.synchronize()
+            for g in ranks + pays + res + [g for row in buckets for g in row]:
+                assert g.intact(), (codec, sizes, n)

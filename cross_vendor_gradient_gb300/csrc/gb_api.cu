@@ -642,13 +642,14 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
 // first use (link 0 is the pipelined policy's pair).
 gb_status ensure_links(gb_ctx *c, int L) {
     for (int l = 1; l < L && l < kMaxLinks; ++l) {
-        if (c->lsd[l]) continue;
-        cudaError_t e;
-        if ((e = cudaStreamCreateWithFlags(&c->lsd[l], cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaStreamCreateWithFlags(&c->lsh[l], cudaStreamNonBlocking)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&c->ev_ljd[l], cudaEventDisableTiming)) != cudaSuccess ||
-            (e = cudaEventCreateWithFlags(&c->ev_ljh[l], cudaEventDisableTiming)) != cudaSuccess)
-            return fail(c, GB_ERR_CUDA, "bridge link streams", e);
+        // each handle on its own, so that a failure part way leaves nothing
+        // half made for a later call to use
+        cudaError_t e = cudaSuccess;
+        if (!c->lsd[l]) e = cudaStreamCreateWithFlags(&c->lsd[l], cudaStreamNonBlocking);
+        if (e == cudaSuccess && !c->lsh[l]) e = cudaStreamCreateWithFlags(&c->lsh[l], cudaStreamNonBlocking);
+        if (e == cudaSuccess && !c->ev_ljd[l]) e = cudaEventCreateWithFlags(&c->ev_ljd[l], cudaEventDisableTiming);
+        if (e == cudaSuccess && !c->ev_ljh[l]) e = cudaEventCreateWithFlags(&c->ev_ljh[l], cudaEventDisableTiming);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "bridge link streams", e);
     }
     return GB_OK;
 }

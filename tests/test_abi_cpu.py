@@ -165,3 +165,31 @@ def test_no_device_is_reported_not_sticky():
         assert "device" in B.gb_last_error_message(ctx)
     finally:
         B.gb_destroy(ctx)
+
+
+def test_plain_c_caller(tmp_path):
+    """include/gb.h is a C99 header: a C program built against it alone links
+    libgb.so and gets the host-only answers (topology, payload sizes,
+    argument errors before any CUDA call, the bucket plan)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    exe = str(tmp_path / "c_abi_host")
+    libdir = os.path.dirname(B.LIB_PATH)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_host.c"),
+                    "-L", libdir, "-lgb", "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    got = dict(line.split(" ", 1) for line in out.strip().splitlines())
+    assert got["create"] == "0" and got["destroy"] == "0"
+    assert got["world"] == "6" and got["islands"] == "3"
+    assert got["first2"] == "5" and got["island_of4"] == "1"
+    assert int(got["payload_e4m3"]) == B.gb_payload_bytes(B.GB_CODEC_E4M3, 256, 6553600) == 6656000
+    assert int(got["payload_bf16"]) == 2000
+    assert int(got["scales_off"]) == B.gb_payload_scales_offset(B.GB_CODEC_E5M2, 128, 1001)
+    assert got["null_bufs"] == str(B.GB_ERR_INVALID_ARG) and got["sticky"] == "0"
+    assert got["status_string"] == "GB_ERR_MISALIGNED"
+    _, _, bn = orc.bucket_plan([600, 500, 1200, 10, 990], 4, 4000, 1)
+    assert got["plan"].split() == ["0", str(len(bn))] + [str(int(v)) for v in bn]

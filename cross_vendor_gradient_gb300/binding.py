@@ -53,6 +53,7 @@ SIGNATURES = {
     "gb_reserve": (_i, [_vp, _sz, _i, _i, _i]),
     "gb_set_pipeline": (_i, [_vp, _sz, _i]),
     "gb_context_status": (_i, [_vp]),
+    "gb_last_error": (_i, [_vp]),
     "gb_last_error_message": (ctypes.c_char_p, [_vp]),
     "gb_status_string": (ctypes.c_char_p, [_i]),
     "gb_payload_bytes": (_sz, [_i, _i, _sz]),
@@ -154,6 +155,10 @@ def gb_set_pipeline(ctx, chunk_bytes, use_graphs=1):
 
 def gb_context_status(ctx):
     return lib().gb_context_status(ctx)
+
+
+def gb_last_error(ctx):
+    return lib().gb_last_error(ctx)
 
 
 def gb_last_error_message(ctx):

@@ -52,6 +52,7 @@ struct gb_ctx {
     int island_of[GB_MAX_RANKS] = {};
     int device = -1;
     gb_status sticky = GB_OK;
+    gb_status last = GB_OK;  // the most recent failed call's status, sticky or not
     char msg[256] = {};
     int inject = 0;
     // device staging, chunk-major: C x I own-payload parts, then I leaders x
@@ -108,6 +109,7 @@ constexpr uint64_t kMaxElems = 1ull << 38;
 
 gb_status set_msg(gb_ctx *c, gb_status s, const char *fmt, ...) {
     if (c) {
+        if (s != GB_OK) c->last = s;
         va_list ap;
         va_start(ap, fmt);
         vsnprintf(c->msg, sizeof c->msg, fmt, ap);
@@ -119,6 +121,7 @@ gb_status set_msg(gb_ctx *c, gb_status s, const char *fmt, ...) {
 // A failure after validation: the context becomes failed for good.
 gb_status fail(gb_ctx *c, gb_status s, const char *what, cudaError_t e = cudaSuccess) {
     c->sticky = s;
+    c->last = s;
     if (e != cudaSuccess)
         snprintf(c->msg, sizeof c->msg, "%s: %s", what, cudaGetErrorString(e));
     else
@@ -145,7 +148,7 @@ bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
 
 gb_status check_ctx(gb_ctx *c) {
     if (!c) return GB_ERR_INVALID_ARG;
-    if (c->sticky != GB_OK) return GB_ERR_CONTEXT_FAILED;
+    if (c->sticky != GB_OK) return c->last = GB_ERR_CONTEXT_FAILED;  // the message keeps the cause
     return GB_OK;
 }
 
@@ -1240,6 +1243,7 @@ int gb_island_of_rank(const gb_ctx *c, int r) { return (c && r >= 0 && r < c->W)
 
 gb_status gb_context_status(const gb_ctx *c) { return c ? c->sticky : GB_ERR_INVALID_ARG; }
 const char *gb_last_error_message(const gb_ctx *c) { return c ? c->msg : "NULL context"; }
+gb_status gb_last_error(const gb_ctx *c) { return c ? c->last : GB_ERR_INVALID_ARG; }
 
 const char *gb_status_string(gb_status s) {
     switch (s) {

@@ -191,9 +191,16 @@ gb_status gb_set_pipeline(gb_ctx *ctx, size_t chunk_bytes, int use_graphs);
  * Waits for the context's outstanding work. */
 gb_status gb_set_sharded_bridge(gb_ctx *ctx, int on);
 
-/* The context's sticky status (GB_OK until a call fails after enqueueing)
- * and a one-line description of the last error on this context. */
+/* gb_context_status: the context's sticky status (GB_OK until a call fails
+ * after enqueueing; then that failure, for good).  gb_last_error: the status
+ * of the most recent call on this context that failed, sticky or not (an
+ * argument error included), GB_OK if none has; a later successful call does
+ * not clear it; calls refused by a failed context set it to
+ * GB_ERR_CONTEXT_FAILED.  gb_last_error_message: a one-line description of
+ * the last error (for a failed context, of the failure that caused it).
+ * With a NULL context the first two return GB_ERR_INVALID_ARG. */
 gb_status gb_context_status(const gb_ctx *ctx);
+gb_status gb_last_error(const gb_ctx *ctx);
 const char *gb_last_error_message(const gb_ctx *ctx);
 const char *gb_status_string(gb_status status);
 

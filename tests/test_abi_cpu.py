@@ -103,6 +103,7 @@ def test_create_validation_and_topology():
         assert [B.gb_island_of_rank(ctx, r) for r in range(6)] == [0, 0, 1, 1, 1, 2]
         assert B.gb_island_size(ctx, 1) == 3 and B.gb_island_size(ctx, 3) == -1
         assert B.gb_context_status(ctx) == B.GB_OK
+        assert B.gb_last_error(ctx) == B.GB_OK
     finally:
         assert B.gb_destroy(ctx) == B.GB_OK
 
@@ -146,8 +147,9 @@ def test_argument_errors_need_no_device():
         # n == 0 is a valid no-op, answered without a device
         assert B.gb_all_reduce(ctx, fake, 0, 0, 0, 2, 256) == B.GB_OK
         assert B.gb_all_gather(ctx, fake, fake, 0, 1) == B.GB_OK
-        # none of these is sticky
+        # none of these is sticky; the last one is remembered
         assert B.gb_context_status(ctx) == B.GB_OK
+        assert B.gb_last_error(ctx) == B.GB_ERR_INVALID_ARG  # the last refused call above
         assert B.gb_debug_inject(ctx, 77) == B.GB_ERR_INVALID_ARG
     finally:
         B.gb_destroy(ctx)

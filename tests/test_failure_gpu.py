@@ -48,9 +48,12 @@ def test_injected_bridge_fault_is_sticky_and_writes_nothing(call):
         assert np.array_equal(to_host(bufs[r]), before[r])
         assert np.array_equal(to_host(outs[r]), outs_before[r])
     assert ctx.status() == B.GB_ERR_BRIDGE
+    assert B.gb_last_error(ctx.handle) == B.GB_ERR_BRIDGE
     with pytest.raises(GbError) as e2:
         ctx.all_reduce(bufs, "sum", "none", 256)
     assert e2.value.status == B.GB_ERR_CONTEXT_FAILED
+    assert B.gb_last_error(ctx.handle) == B.GB_ERR_CONTEXT_FAILED
+    assert "injected" in B.gb_last_error_message(ctx.handle)  # the cause is kept
     with pytest.raises(GbError) as e3:
         ctx.island_reduce(0, bufs[:2], torch.empty(n, device="cuda"))
     assert e3.value.status == B.GB_ERR_CONTEXT_FAILED

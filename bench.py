@@ -186,17 +186,69 @@ def cpu_baseline(w, xs, codec, budget_s=10.0):
 
 # -------------------------------------------------------------- GPU leg
 
-def alg_bytes(W, I, n, b, P, I2=True):
+def alg_bytes(W, I, n, b, P):
     """Algorithmic HBM bytes of the two kernels for one all_reduce:
-    reduce+encode reads W*n*b and writes I*P; decode+broadcast reads each
-    island's I payloads (I*I*P) and writes W*n*b."""
-    return W * n * b + I * P, I * I * P + W * n * b
+    reduce+encode reads W*n*b and writes I*P; decode+broadcast reads the I
+    payloads once (I*P) and writes W*n*b."""
+    return W * n * b + I * P, I * P + W * n * b
 
 
 def dataclasses_replace_f32(w):
     """The workload drawn as float32 (the draw's own type)."""
     import dataclasses
     return dataclasses.replace(w, dtype="f32")
+
+
+def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, batches,
+                  names=("k_reduce_encode", "k_decode_bcast")):
+    """Timed region 3: each kernel launched back to back, as the fused halves
+    of the path (gb_island_reduce_compress, gb_decompress_island_broadcast),
+    with the same grid as in a step.  S distinct input sets, outputs and
+    payloads (together at least 4 x L2 when a set is large, else 16 sets) are
+    cycled.  A batch starts from a clean L2 (256 MiB read) after a ~0.4 ms
+    GPU spin, so the host has queued the whole batch before its first event;
+    each kernel's first launch of the batch is untimed and CUDA events on the
+    launching stream bracket the other S - 1.  So no launch finds its inputs
+    in L2, and every timed launch also writes back what its predecessor left
+    dirty there: the steady state of a stream of buckets.  Returns per-launch
+    milliseconds of both kernels."""
+    import torch
+    W = len(pristine)
+    n = pristine[0].numel()
+    b = pristine[0].element_size()
+    set_bytes = W * n * b + I * P
+    S = max(5, min(-(-(4 * L2_BYTES) // set_bytes), 16 if set_bytes * 16 < 4 * L2_BYTES else 1 << 30,
+                   (8 << 30) // set_bytes))
+    dev = pristine[0].device
+    ins = [[p.clone() for p in pristine] for _ in range(S)]
+    outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
+    pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
+    # every leader decodes the same I payloads: in a step the received parts
+    # were written by the host -> device copy just before the decode and are
+    # still in L2, so only one read of each part comes from DRAM there too
+    rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
+    ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(batches)]
+    with torch.cuda.stream(stream):
+        for it in range(warm + batches):
+            e = ea[it - warm] if it >= warm else None
+            clean.amax()
+            torch.cuda._sleep(800_000)
+            for q in range(S):
+                ctx.island_reduce_compress(ins[q], codec, block, pays[q], stream=stream)
+                if e and q == 0:
+                    e[0].record(stream)
+            if e:
+                e[1].record(stream)
+            for q in range(S):
+                ctx.decompress_island_broadcast(rows[q], op, codec, block, outs[q], stream=stream)
+                if e and q == 0:
+                    e[2].record(stream)
+            if e:
+                e[3].record(stream)
+    torch.cuda.synchronize()
+    return {"sets": S, "timed_launches_per_batch": S - 1, "batches": batches, "set_bytes": set_bytes,
+            names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
+            names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
 
 
 def run_gb(args, world, rank, local, pg):
@@ -328,56 +380,16 @@ def run_gb(args, world, rank, local, pg):
     k1_bytes, k2_bytes = alg_bytes(W, I, n, b, P)
     peak, peak_kind = measured_peaks()
 
-    # ---- timed region 3: each kernel back to back, as the fused halves of
-    # the path (gb_island_reduce_compress, gb_decompress_island_broadcast).
-    # S input sets, outputs and payloads, together several times L2, are
-    # cycled so that no launch finds its inputs in L2.  A batch starts from a
-    # clean L2 (256 MiB read); its first launch of each kernel is untimed, and
-    # CUDA events on the launching stream bracket the other S - 1, so that
-    # every timed launch also writes back what its predecessor left dirty in
-    # L2: the steady state of a stream of buckets.
+    # ---- timed region 3: each kernel back to back (see kernel_stream)
     ks = None
     if not exact and I > 1:
-        set_bytes = W * n * b + I * P
-        S = max(5, min(-(-(4 * L2_BYTES) // set_bytes), (8 << 30) // set_bytes))
-        ins = [[p.clone() for p in pristine] for _ in range(S)]
-        outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
-        pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
-        # every leader decodes the same I payloads: in a step the received
-        # parts were written by the host -> device copy just before the
-        # decode and are still in L2, so only one read of each part comes
-        # from DRAM there too
-        rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
-        Kk = max(3, min(Kr, 50))
-        ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kk)]
-        with torch.cuda.stream(stream):
-            for it in range(Wm + Kk):
-                e = ea[it - Wm] if it >= Wm else None
-                clean.amax()
-                # hold the stream ~0.4 ms so that the host has queued the whole
-                # batch before its first event: the batch then runs GPU-bound
-                torch.cuda._sleep(800_000)
-                for q in range(S):
-                    ctx.island_reduce_compress(ins[q], codec, w.block, pays[q], stream=stream)
-                    if e and q == 0:
-                        e[0].record(stream)
-                if e:
-                    e[1].record(stream)
-                for q in range(S):
-                    ctx.decompress_island_broadcast(rows[q], w.op, codec, w.block, outs[q], stream=stream)
-                    if e and q == 0:
-                        e[2].record(stream)
-                if e:
-                    e[3].record(stream)
-        torch.cuda.synchronize()
-        ks = {"sets": S, "timed_launches_per_batch": S - 1, "batches": Kk, "set_bytes": set_bytes,
-              names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
-              names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
-        del ins, outs, pays, rows
+        ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, Wm, max(3, min(Kr, 50)),
+                           names)
+        S, set_bytes = ks["sets"], ks["set_bytes"]
     if ks:
         r1, r2 = ks[names[0]], ks[names[1]]
         region = ("timed region 3: each kernel launched back to back over %d input sets (%.0f MB each, "
-                  "cycled so that none is in L2); CUDA events around the last %d launches of each batch"
+                  "distinct, from a clean L2); CUDA events around the last %d launches of each batch"
                   % (S, set_bytes / 1e6, S - 1))
     else:
         r1, r2 = k1_ms, k2_ms
@@ -632,8 +644,9 @@ def run_sweep(args, local):
     """Payload sweep (workload c3): 4 KiB .. 256 MiB of float32 per rank at
     2 islands x 2 ranks, codecs none / bf16 / e4m3; one JSON line per row.
     Per row: the step as run by default (pipelined graph, no marks) for the
-    algorithm GB/s, then one-hop steps with phase marks for the kernels' HBM
-    roofline fractions and the bridge's fraction of pinned copy bandwidth.
+    algorithm GB/s; one-hop steps with phase marks for the kernels inside a
+    step and the bridge's fraction of pinned copy bandwidth; and each kernel
+    back to back (kernel_stream) for the HBM roofline fractions.
     L2 is flushed (write then clean read) before every timed step."""
     import torch
     from cross_vendor_gradient_gb300 import Context, payload_bytes
@@ -685,17 +698,25 @@ def run_sweep(args, local):
             steps(3, False)
             plain = steps(K, True)
             ph = np.array([ctx.phase_times(a) for a in range(K)])
-            ctx.close()
+            ctx.set_phase_timing(0)
             k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
             P = payload_bytes(codec, w.block, n)
             b1, b2 = alg_bytes(W, I, n, 4, P)
+            ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, 2,
+                               max(3, min(20, int(2e9 // (n * 4 * W)))))
+            ctx.close()
+            s1, s2 = ks["k_reduce_encode"], ks["k_decode_bcast"]
             print(json.dumps({
                 "metric": METRIC, "sweep_row": True, "workload": "c3", "codec": codec, "n": n,
                 "bytes_per_rank": 4 * n, "value": 4 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
                 "steps": K, "one_hop_ms_per_step": plain,
-                "hbm_frac": {"k_reduce_encode": b1 / (k1 * 1e-3) / 1e9 / peak,
-                             "k_decode_bcast": b2 / (k2 * 1e-3) / 1e9 / peak, "peak_gbs": peak,
-                             "peak_kind": peak_kind},
+                "hbm_frac": {"k_reduce_encode": b1 / (s1 * 1e-3) / 1e9 / peak,
+                             "k_decode_bcast": b2 / (s2 * 1e-3) / 1e9 / peak, "peak_gbs": peak,
+                             "peak_kind": peak_kind,
+                             "region": "each kernel back to back over %d distinct input sets" % ks["sets"]},
+                "kernels_stream_ms": {"k_reduce_encode": s1, "k_decode_bcast": s2},
+                "in_step_hbm_frac": {"k_reduce_encode": b1 / (k1 * 1e-3) / 1e9 / peak,
+                                     "k_decode_bcast": b2 / (k2 * 1e-3) / 1e9 / peak},
                 "kernels_ms": {"k_reduce_encode": k1, "bridge_hop": br, "k_decode_bcast": k2},
                 "bridge_gbs": (I * P + I * (I - 1) * P) / (br * 1e-3) / 1e9 if br > 0 else None,
             }), flush=True)

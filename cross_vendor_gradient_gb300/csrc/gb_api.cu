@@ -601,12 +601,10 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
                 }
             }
         }
-        for (int g = 0; g < I; ++g)
-            for (int j = 0; j < I; ++j)
-                da.payload[g][j] = (j == g) ? (const void *)outbox(ch, j) : (const void *)inbox(g, ch, j);
-        for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
-        da.n_groups = I;
-        da.n_src = I;
+        const void *received[GB_MAX_ISLANDS];
+        for (int j = 0; j < I; ++j)
+            received[j] = I == 1 ? (const void *)outbox(ch, 0) : (const void *)inbox((j + 1) % I, ch, j);
+        gb::decode_once(da, p.W, I, received);
         da.avg = p.op == GB_AVG;
         da.world = (float)p.W;
         da.world_pow2 = (p.W & (p.W - 1)) == 0;
@@ -740,12 +738,10 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
             da.dst[r] = (unsigned char *)dev[r] + e0 * p.eb;
             da.group_of_rank[r] = c->island_of[r];
         }
-        for (int g = 0; g < I; ++g)
-            for (int j = 0; j < I; ++j)
-                da.payload[g][j] = (j == g) ? (const void *)outbox(ch, j) : (const void *)inbox(g, ch, j);
-        for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
-        da.n_groups = I;
-        da.n_src = I;
+        const void *received[GB_MAX_ISLANDS];
+        for (int j = 0; j < I; ++j)
+            received[j] = I == 1 ? (const void *)outbox(ch, 0) : (const void *)inbox((j + 1) % I, ch, j);
+        gb::decode_once(da, W, I, received);
         da.avg = p.op == GB_AVG;
         da.world = (float)W;
         da.world_pow2 = (W & (W - 1)) == 0;
@@ -850,12 +846,10 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
             da.dst[r] = (unsigned char *)bufs[(size_t)w.b * W + r] + w.e0 * p.eb;
             da.group_of_rank[r] = c->island_of[r];
         }
-        for (int g = 0; g < I; ++g)
-            for (int j = 0; j < I; ++j)
-                da.payload[g][j] = (j == g) ? (const void *)outbox(slot, j) : (const void *)inbox(g, slot, j);
-        for (int q = 0; q <= I; ++q) da.first[q] = c->first[q];
-        da.n_groups = I;
-        da.n_src = I;
+        const void *received[GB_MAX_ISLANDS];
+        for (int j = 0; j < I; ++j)
+            received[j] = I == 1 ? (const void *)outbox(slot, 0) : (const void *)inbox((j + 1) % I, slot, j);
+        gb::decode_once(da, W, I, received);
         da.avg = p.op == GB_AVG;
         da.world = (float)W;
         da.world_pow2 = (W & (W - 1)) == 0;
@@ -1066,12 +1060,10 @@ gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n
         da.dst[r] = out[r];
         da.group_of_rank[r] = c->island_of[r];
     }
-    for (int g = 0; g < I; ++g)
-        for (int j = 0; j < I; ++j)
-            da.payload[g][j] = (j == g) ? (const void *)outbox(j) : (const void *)inbox(g, j);
-    for (int i = 0; i <= I; ++i) da.first[i] = c->first[i];
-    da.n_groups = I;
-    da.n_src = I;
+    const void *received[GB_MAX_ISLANDS];
+    for (int j = 0; j < I; ++j)
+        received[j] = I == 1 ? (const void *)outbox(0) : (const void *)inbox((j + 1) % I, j);
+    gb::decode_once(da, W, I, received);
     da.world = (float)W;
     da.world_pow2 = (W & (W - 1)) == 0;
     da.inv_world = 1.0f / (float)W;
@@ -1457,11 +1449,18 @@ gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads,
         da.dst[r] = rank_bufs[r];
         da.group_of_rank[r] = c->island_of[r];
     }
-    for (int g = 0; g < c->I; ++g)
-        for (int j = 0; j < c->I; ++j) da.payload[g][j] = payloads[g * c->I + j];
-    for (int i = 0; i <= c->I; ++i) da.first[i] = c->first[i];
-    da.n_groups = c->I;
-    da.n_src = c->I;
+    bool same_rows = true;  // every leader holds the same pointers: decode once
+    for (int g = 1; g < c->I && same_rows; ++g)
+        for (int j = 0; j < c->I; ++j) same_rows = same_rows && payloads[g * c->I + j] == payloads[j];
+    if (same_rows) {
+        gb::decode_once(da, c->W, c->I, payloads);
+    } else {
+        for (int g = 0; g < c->I; ++g)
+            for (int j = 0; j < c->I; ++j) da.payload[g][j] = payloads[g * c->I + j];
+        for (int i = 0; i <= c->I; ++i) da.first[i] = c->first[i];
+        da.n_groups = c->I;
+        da.n_src = c->I;
+    }
     da.avg = op == GB_AVG;
     da.world = (float)c->W;
     da.world_pow2 = (c->W & (c->W - 1)) == 0;

@@ -57,6 +57,19 @@ struct DecodeBcastArgs {
     uint32_t tiles;  // all_reduce: tiles per group; reduce_scatter: tiles of the longest unit
 };
 
+// One decode for every rank.  Every leader would compute the same total
+// from the same payload bits, so on one GPU a single pass over the payloads
+// as they crossed the bridge (received[j]: island j's part, as some other
+// leader received it; with one island, its own) writes all W ranks.
+inline void decode_once(DecodeBcastArgs &da, int W, int I, const void *const *received) {
+    da.n_groups = 1;
+    da.first[0] = 0;
+    da.first[1] = W;
+    for (int r = 0; r < W; ++r) da.group_of_rank[r] = 0;
+    da.n_src = I;
+    for (int j = 0; j < I; ++j) da.payload[0][j] = received[j];
+}
+
 // accum = dec(payload) or accum + dec(payload).
 struct DecompressAccArgs {
     const void *payload;

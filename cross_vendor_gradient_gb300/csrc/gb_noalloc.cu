@@ -140,13 +140,13 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
         da.dst[r] = rank_bufs[r];
         da.group_of_rank[r] = gb_island_of_rank(ctx, r);
     }
-    for (int g = 0; g < I; ++g)
-        for (int j = 0; j < I; ++j)
-            da.payload[g][j] = (j == g) ? (const void *)(scratch + (size_t)j * slot)
-                                        : (const void *)(inbox + ((size_t)g * (I - 1) + (j < g ? j : j - 1)) * slot);
-    for (int i = 0; i <= I; ++i) da.first[i] = first[i];
-    da.n_groups = I;
-    da.n_src = I;
+    const void *received[GB_MAX_ISLANDS];
+    for (int j = 0; j < I; ++j) {
+        const int g = (j + 1) % I;  // the leader whose received copy of island j is read
+        received[j] = I == 1 ? (const void *)scratch
+                             : (const void *)(inbox + ((size_t)g * (I - 1) + (j < g ? j : j - 1)) * slot);
+    }
+    gb::decode_once(da, W, I, received);
     da.avg = op == GB_AVG;
     da.world = (float)W;
     da.world_pow2 = (W & (W - 1)) == 0;

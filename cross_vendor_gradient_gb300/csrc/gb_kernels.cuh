@@ -116,9 +116,16 @@ uint64_t launches();
 void count_launch();
 int sm_count();
 
-// One resident wave of 256-thread blocks spread over `units` grid rows (or
-// fewer when there is less work); the kernels walk their tiles with a grid
-// stride.  The occupancy is looked up once per kernel instantiation.
+// 256-thread blocks, one 256-element tile per warp, over `units` grid rows;
+// the kernels walk their tiles with a grid stride.  The grid follows the
+// work rather than one resident wave: with several waves, blocks that finish
+// early are replaced by new ones, so the last tiles are spread over every SM
+// instead of leaving the tail to the few warps that hold one tile more (on a
+// 25 MiB float32 bucket per rank this took 9 % off the decode kernel and 4 %
+// off the encode, back to back).
+// It is capped at kMaxWaves resident waves, after which warps loop.  The
+// occupancy is looked up once per kernel instantiation.
+constexpr uint64_t kMaxWaves = 32;
 template <auto Kern, typename Args>
 cudaError_t launch_grid(uint64_t tiles_per_unit, unsigned units, const Args &a, cudaStream_t s) {
     static int per_sm = 0;
@@ -127,7 +134,7 @@ cudaError_t launch_grid(uint64_t tiles_per_unit, unsigned units, const Args &a, 
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, Kern, 256, 0);
         per_sm = v > 0 ? v : 1;
     }
-    const uint64_t cap = (uint64_t)per_sm * (uint64_t)sm_count();
+    const uint64_t cap = kMaxWaves * (uint64_t)per_sm * (uint64_t)sm_count();
     const uint64_t per_unit_cap = cap / units > 0 ? cap / units : 1;
     const uint64_t want = (tiles_per_unit + 7) / 8;  // 8 warps (tiles) per block
     const uint64_t gx = want < per_unit_cap ? want : per_unit_cap;

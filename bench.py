@@ -223,9 +223,8 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
     ins = [[p.clone() for p in pristine] for _ in range(S)]
     outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
     pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
-    # every leader decodes the same I payloads: in a step the received parts
-    # were written by the host -> device copy just before the decode and are
-    # still in L2, so only one read of each part comes from DRAM there too
+    # every leader's row holds the same I payloads: the call decodes them
+    # once and writes all ranks, as the decode in a step does
     rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
     ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(batches)]
     with torch.cuda.stream(stream):

@@ -627,8 +627,8 @@ def run_buckets_bench(args, world, rank, local, pg):
                                    w.key, W, list(w.island_sizes), len(numels), w.dtype, sum(numels), len(bn),
                                    w.dist, w.op, codec, w.block),
                    "buckets": len(bn), "values_per_rank": sum(bn),
-                   "policy": "one pipeline over all buckets (%d KiB payload chunks), one CUDA graph per step" % (
-                       chunk_bytes >> 10),
+                   "policy": "one pipeline over all buckets (payload chunks of at most 3 x %d KiB, each bucket "
+                             "cut evenly), one CUDA graph per step" % (chunk_bytes >> 10),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_step": dom[1],

@@ -24,6 +24,7 @@ constexpr int kMarks = 4 + 2 * kMaxChunks;
 constexpr int kMaxGraphs = 16;
 // sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
 constexpr int kMaxLinks = 8;
+constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
 }  // namespace
 
 // Identity of a captured all_reduce (every value its graph bakes in).
@@ -417,7 +418,8 @@ size_t part_bytes(const Plan &p, uint64_t m) {
 }
 
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
-               bool sharded_ok = false) {
+               bool sharded_ok = false, size_t chunk_bytes = 0) {
+    if (chunk_bytes == 0) chunk_bytes = c->chunk_bytes;
     Plan p;
     p.I = c->I;
     p.W = c->W;
@@ -438,10 +440,10 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         // whole codec blocks), one per bridge link
         const uint64_t seg = round_up((n + (uint64_t)k - 1) / (uint64_t)k, gb::kTile);
         if (seg < n) p.chunk = seg;
-    } else if (c->I > 1 && c->chunk_bytes > 0) {
+    } else if (c->I > 1 && chunk_bytes > 0) {
         // chunk_bytes of one island's payload per chunk
         const double per_elem = (double)p.cb + (is_fp8(p.eff) ? 4.0 / p.blk : 0.0);
-        uint64_t ch = (uint64_t)((double)c->chunk_bytes / per_elem) / gb::kTile * gb::kTile;
+        uint64_t ch = (uint64_t)((double)chunk_bytes / per_elem) / gb::kTile * gb::kTile;
         if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
         const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
         if (ch < min_ch) ch = min_ch;
@@ -875,14 +877,24 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
 
 gb_status run_buckets(gb_ctx *c, int nb, void *const *bufs, const size_t *numel, gb_dtype dtype, gb_op op,
                       gb_codec codec, int block, cudaStream_t s) {
-    // the chunk shape of the largest bucket fixes the slot size
+    // the chunk shape of the largest bucket fixes the slot size.  Chunks are
+    // kBucketChunkScale x the pipeline chunk: across a gradient set the
+    // pipeline fills once, so larger copies only save per-copy cost (on
+    // GB300, 6 MiB beat 2, 4 and 8 MiB for both the GPT-2 small and the 1.1B
+    // Llama-style bf16 sets)
     size_t nmax = 0;
     for (int b = 0; b < nb; ++b) nmax = numel[b] > nmax ? numel[b] : nmax;
-    Plan p = make_plan(c, nmax, dtype, op, codec, block, 0);
+    Plan p = make_plan(c, nmax, dtype, op, codec, block, 0, false, kBucketChunkScale * c->chunk_bytes);
+    // each bucket in balanced chunks of whole tiles, none larger than the
+    // plan's chunk (so a bucket never ends in a sliver of a chunk)
     std::vector<WorkChunk> work;
-    for (int b = 0; b < nb; ++b)
-        for (uint64_t e0 = 0; e0 < numel[b]; e0 += p.chunk)
-            work.push_back({b, e0, (numel[b] - e0) < p.chunk ? (numel[b] - e0) : p.chunk});
+    for (int b = 0; b < nb; ++b) {
+        const uint64_t k = (numel[b] + p.chunk - 1) / p.chunk;
+        const uint64_t ch = k ? round_up((numel[b] + k - 1) / k, gb::kTile) : p.chunk;
+        const uint64_t cb = ch < p.chunk ? ch : p.chunk;
+        for (uint64_t e0 = 0; e0 < numel[b]; e0 += cb)
+            work.push_back({b, e0, (numel[b] - e0) < cb ? (numel[b] - e0) : cb});
+    }
     const size_t recv = c->I == 2 ? 2 : (size_t)c->I * c->I;
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(c->I + recv) * 2 * p.part));
     GB_TRY(grow_host(c, (size_t)c->I * 2 * p.part));

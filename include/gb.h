@@ -359,7 +359,9 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, 
  * bucket_numel[b] elements.  The tensors of the plan are views into these
  * flat buffers, so nothing is copied in or out.  Under the pipelined policy
  * (float32 / bfloat16 SUM / AVG, two or more islands, no phase marks kept)
- * the buckets run as one pipeline of chunks on a two-slot staging ring, the
+ * the buckets run as one pipeline of chunks (each bucket cut evenly into
+ * chunks of at most 3 x chunk_bytes of payload: the pipeline fills once per
+ * set, so larger copies pay) on a two-slot staging ring, the
  * bridge of one bucket overlapping the kernels of the next, captured as one
  * CUDA graph for the whole set from the second call with the same buffers
  * (one launch per gradient sync); otherwise one gb_all_reduce per bucket.

@@ -25,6 +25,7 @@ constexpr int kMaxGraphs = 16;
 // sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
 constexpr int kMaxLinks = 8;
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
+constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2
 }  // namespace
 
 // Identity of a captured all_reduce (every value its graph bakes in).
@@ -1682,7 +1683,10 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
     GB_TRY(grow_device(c, &c->d_ranks, &c->d_ranks_bytes, (size_t)c->W * stride));
     void *dev[GB_MAX_RANKS];
     for (int r = 0; r < c->W; ++r) dev[r] = c->d_ranks + (size_t)r * stride;
-    const Plan p = make_plan(c, n, dtype, op, codec, block, 0);
+    // chunks of half the pipeline chunk: here every chunk also carries W rank
+    // buffers' worth of staging in and out, so the pipeline's fill and drain
+    // weigh more (1 MiB beat 0.5, 0.75, 1.5 and 2 MiB on GB300)
+    const Plan p = make_plan(c, n, dtype, op, codec, block, 0, false, c->chunk_bytes / kHostChunkDiv);
     if (!is_exact(dtype, op) && p.C > 1 && c->tcap == 0) {
         // pipelined: staging in, bridge and copy-back overlap chunk by chunk
         GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));

@@ -329,8 +329,10 @@ gb_status gb_broadcast(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype d
  * tensors: staged onto the rank's GPU, carried by the same topology and
  * copied back).  Under the pipelined policy (float32 / bfloat16 SUM / AVG,
  * no phase marks kept) the staging, the bridge hop and the copy-back run
- * chunk by chunk on the context's copy streams so that both directions of
- * the host link stay busy, replayed as a CUDA graph from the second call
+ * chunk by chunk (chunks of half of chunk_bytes of payload: every chunk also
+ * carries the rank buffers in and out) on the context's copy streams so that
+ * both directions of the host link stay busy, replayed as a CUDA graph from
+ * the second call
  * with the same buffers; otherwise staging, all_reduce and copy-back run in
  * sequence.  Host buffers need no alignment; they must not be touched until
  * `stream` has completed the call. */

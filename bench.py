@@ -65,6 +65,9 @@ def parse():
                    help="only the per-kernel timed regions (kernels inside one-hop steps, and back to "
                         "back); for profiling")
     p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
+    p.add_argument("--collective", default="all_reduce",
+                   choices=["all_reduce", "reduce_scatter", "all_gather", "broadcast"],
+                   help="the collective one step runs (all_reduce: the default bench line)")
     return p.parse_args()
 
 
@@ -767,6 +770,126 @@ def run_reference(args, world, rank, pg):
     }
 
 
+def run_collective(args, world, rank, local, pg):
+    """reduce_scatter, all_gather or broadcast on the default workload's
+    ranks and buffer size: one step is one call of the collective.
+    reduce_scatter: n elements per rank in, n / W out (the codec applies);
+    all_gather: n / W in, n out (exact); broadcast: n in place from rank 0
+    (exact).  value = n * b / step time (bytes of one full rank buffer).  The
+    kernels' HBM fractions come from one-hop calls with phase marks, with the
+    algorithmic bytes of each collective: reduce_scatter encode W*n*b + I*P,
+    decode I*P + n*b; all_gather copy W*m*b read + W*W*m*b written (m = n /
+    W); broadcast copy n*b read + (W - 1)*n*b written."""
+    import torch
+    from cross_vendor_gradient_gb300 import Context, kernel_launch_count, payload_bytes
+    from cross_vendor_gradient_gb300 import workloads as wl
+    from cross_vendor_gradient_gb300 import build as gbuild
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.workload]
+    coll = args.collective
+    codec = (args.codec or w.codecs[0]) if coll == "reduce_scatter" else "none"
+    W, I = w.world_size, len(w.island_sizes)
+    n = (args.n or w.n) // W * W
+    m = n // W
+    xs = wl.host_rank_inputs(dataclasses_replace_f32(w), n=n)
+    pristine = [torch.from_numpy(x).to(dev) for x in xs]
+    if coll == "all_gather":
+        pristine = [p[:m].clone() for p in pristine]
+    ins = [p.clone() for p in pristine]
+    outs = ([torch.empty(m, dtype=torch.float32, device=dev) for _ in range(W)] if coll == "reduce_scatter" else
+            [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(W)] if coll == "all_gather" else None)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    K, Wm = args.steps, max(3, args.warmup)
+    ctx = Context(w.island_sizes)
+    chunk_bytes = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
+    b = 4
+
+    def call():
+        if coll == "reduce_scatter":
+            ctx.reduce_scatter(ins, outs, w.op, codec, w.block, stream=stream)
+        elif coll == "all_gather":
+            ctx.all_gather(ins, outs, stream=stream)
+        else:
+            ctx.broadcast(ins, 0, stream=stream)
+
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def steps(count, timed):
+        with torch.cuda.stream(stream):
+            for i in range(count):
+                for x, y in zip(pristine, ins):
+                    y.copy_(x, non_blocking=True)
+                flush.zero_()
+                clean.amax()
+                if timed:
+                    ev0[i].record(stream)
+                call()
+                if timed:
+                    ev1[i].record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(count)])) if timed else 0.0
+
+    ctx.set_pipeline(chunk_bytes, not args.no_graphs)
+    steps(Wm, False)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(pg)
+    l0 = kernel_launch_count()
+    ms = steps(K, True)
+    launches = kernel_launch_count() - l0
+    barrier(pg)
+    clk = clocks.stop()
+    ms = max_over_ranks(pg, ms, dev if pg is not None else None)
+    Kr = min(K, 200)
+    ctx.set_pipeline(0, False)
+    ctx.set_phase_timing(Kr)
+    steps(3, False)
+    one_hop = steps(Kr, True)
+    ph = np.array([ctx.phase_times(a) for a in range(Kr)])
+    ctx.close()
+    k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
+    P = payload_bytes(codec, w.block, n) if coll == "reduce_scatter" else m * b
+    if coll == "reduce_scatter":
+        kern = [("k_reduce_encode", W * n * b + I * P, k1), ("k_decode_bcast (slices)", I * P + n * b, k2)]
+        link = I * P + I * (I - 1) * P
+    elif coll == "all_gather":
+        kern = [("k_copy", W * m * b + W * W * m * b, k2)]
+        link = W * m * b + (I - 1) * W * m * b
+    else:
+        kern = [("k_copy", n * b + (W - 1) * n * b, k2)]
+        link = n * b + (I - 1) * n * b
+    peak, peak_kind = measured_peaks()
+    dom = max(kern, key=lambda t: t[2])
+    achieved = dom[1] / (dom[2] * 1e-3) / 1e9
+    return {
+        "metric": "%s algorithm GB/s and %% of GB300 HBM roofline" % coll, "value": world * n * b / (ms * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded PCG64 per rank; no dataset)",
+        "config": {"workload": "%s: %d simulated ranks as islands %s, %s of one %.0f MiB f32 buffer per rank "
+                               "(n=%d), %s%s" % (w.key, W, list(w.island_sizes), coll, n * b / 2 ** 20, n, w.dist,
+                                                 (", op %s, codec %s block %d" % (w.op, codec, w.block))
+                                                 if coll == "reduce_scatter" else ", exact"),
+                   "policy": "pipelined, %d KiB chunks" % (chunk_bytes >> 10) if coll != "broadcast" else
+                   "one bridge hop",
+                   "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
+        "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_launch": dom[1],
+                     "avg_launch_ms": dom[2], "traffic": None,
+                     "region": "one bridge hop per call, CUDA events around each phase"},
+        "kernels": [{"kernel": k, "alg_bytes": nb, "ms": t, "hbm_frac": nb / (t * 1e-3) / 1e9 / peak}
+                    for k, nb, t in kern],
+        "bridge": {"bytes_per_step": link, "ms": br, "achieved_gbs": link / (br * 1e-3) / 1e9 if br > 0 else None},
+        "one_hop_ms_per_step": one_hop, "gpu_launches": int(launches), "clocks": clk,
+        "e2e": None, "e2e_note": "no host-buffer entry point for this collective",
+    }
+
+
 def main():
     args = parse()
     world, rank, local, pg = dist_setup(args)
@@ -785,6 +908,13 @@ def main():
     from cross_vendor_gradient_gb300 import workloads as _wl
     if _wl.WORKLOADS[args.workload].tensors:
         line = run_buckets_bench(args, world, rank, local, pg)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    if args.collective != "all_reduce":
+        line = run_collective(args, world, rank, local, pg)
         if rank == 0:
             print(json.dumps(line), flush=True)
         if pg is not None:

@@ -1642,10 +1642,38 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
         GB_TRY(mark(c, mm, 2, s));
         // src's island leader sends over the bridge (the bytes are src's);
         // every other leader receives in place
-        GB_TRY(copy_async(c, c->h_stage, rank_bufs[src], nb, cudaMemcpyDeviceToHost, s));
-        for (int i = 0; i < I; ++i)
-            if (i != si)
-                GB_TRY(copy_async(c, rank_bufs[c->first[i]], c->h_stage, nb, cudaMemcpyHostToDevice, s));
+        if (c->chunk_bytes == 0 || nb <= c->chunk_bytes) {
+            GB_TRY(copy_async(c, c->h_stage, rank_bufs[src], nb, cudaMemcpyDeviceToHost, s));
+            for (int i = 0; i < I; ++i)
+                if (i != si)
+                    GB_TRY(copy_async(c, rank_bufs[c->first[i]], c->h_stage, nb, cudaMemcpyHostToDevice, s));
+        } else {
+            // pipelined: pieces of about chunk_bytes (at most GB_MAX_RANKS of
+            // them) go to the host on copy stream D; as soon as one has
+            // landed, stream H carries it on to every other leader
+            size_t piece = round_up((nb + GB_MAX_RANKS - 1) / GB_MAX_RANKS, 256);
+            if (piece < c->chunk_bytes) piece = c->chunk_bytes;
+            cudaStream_t D = c->sd, H = c->sh;
+            GB_TRY(record(c, c->ev_join_d, s));  // the copy streams start after the caller's prior work
+            GB_TRY(wait_on(c, D, c->ev_join_d));
+            GB_TRY(wait_on(c, H, c->ev_join_d));
+            int k = 0;
+            for (size_t off = 0; off < nb; off += piece, ++k) {
+                const size_t len = (nb - off) < piece ? (nb - off) : piece;
+                GB_TRY(copy_async(c, c->h_stage + off, (const unsigned char *)rank_bufs[src] + off, len,
+                                  cudaMemcpyDeviceToHost, D));
+                GB_TRY(record(c, c->ev_ag[k], D));
+                GB_TRY(wait_on(c, H, c->ev_ag[k]));
+                for (int i = 0; i < I; ++i)
+                    if (i != si)
+                        GB_TRY(copy_async(c, (unsigned char *)rank_bufs[c->first[i]] + off, c->h_stage + off, len,
+                                          cudaMemcpyHostToDevice, H));
+            }
+            GB_TRY(record(c, c->ev_join_d, D));
+            GB_TRY(record(c, c->ev_join_h, H));
+            GB_TRY(wait_on(c, s, c->ev_join_d));
+            GB_TRY(wait_on(c, s, c->ev_join_h));
+        }
         GB_TRY(mark(c, mm, 3, s));
     }
     GB_TRY(mark(c, mm, 4, s));

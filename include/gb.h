@@ -172,7 +172,8 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  * parts of the slices they cover).  all_gather with chunk_bytes > 0 moves
  * groups of whole rank blocks of about chunk_bytes: one group's host ->
  * device copies overlap the next group's device -> host copies.  broadcast
- * always takes one hop.  Waits for the context's outstanding work. */
+ * with chunk_bytes > 0 moves the source in pieces of about chunk_bytes (at
+ * most 64 pieces) the same way.  Waits for the context's outstanding work. */
 gb_status gb_set_pipeline(gb_ctx *ctx, size_t chunk_bytes, int use_graphs);
 
 /* The sharded-bridge policy of gb_all_reduce and gb_all_reduce_ef (gpubridge

@@ -575,3 +575,22 @@ def test_pipelined_reduce_scatter_and_all_gather(codec, block, sizes, dtype, chu
             torch.cuda.synchronize()
             for r in range(W):
                 assert_bits_equal(to_host(gathered[r]), ar[r], "RS then AG == AR m=%d rank %d" % (m, r))
+
+
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (2, 1, 3), (4,)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pipelined_broadcast_is_exact(sizes, dtype):
+    """With small pipeline chunks the broadcast's bridge hop moves the source
+    in pieces; every rank still ends with the source's bits."""
+    W = sum(sizes)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(1024)
+        for n in (1, 255, 300, 4099, 70001):
+            for src in sorted({0, W - 1, W // 2}):
+                xs = inputs(sizes, n, dtype, cid=91 + n % 7)
+                bufs = [to_dev(x) for x in xs]
+                ctx.broadcast(bufs, src)
+                want = orc.broadcast(xs, src)
+                torch.cuda.synchronize()
+                for r in range(W):
+                    assert_bits_equal(to_host(bufs[r]), want[r], "bcast %s n=%d src=%d rank %d" % (sizes, n, src, r))

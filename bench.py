@@ -571,7 +571,7 @@ def run_buckets_bench(args, world, rank, local, pg):
         slices = [[torch.empty(nb // W, dtype=tdt, device=dev) for _ in range(W)] for nb in bn]
         Ks = max(2, min(K, 5))
 
-        def step_rs(i, timed):
+        def step_rs(i, timed, sets):
             for row_p, row_b in zip(pristine, bufs):
                 for x, y in zip(row_p, row_b):
                     y.copy_(x, non_blocking=True)
@@ -579,22 +579,32 @@ def run_buckets_bench(args, world, rank, local, pg):
             clean.amax()
             if timed:
                 ev0[i].record(stream)
-            for row, sl in zip(bufs, slices):
-                ctx.reduce_scatter(row, sl, w.op, codec, w.block, stream=stream)
-                ctx.all_gather(sl, row, stream=stream)
+            if sets:  # the whole set per call: one pipeline, one graph each
+                ctx.reduce_scatter_buckets(bufs, slices, w.op, codec, w.block, stream=stream)
+                ctx.all_gather_buckets(slices, bufs, stream=stream)
+            else:
+                for row, sl in zip(bufs, slices):
+                    ctx.reduce_scatter(row, sl, w.op, codec, w.block, stream=stream)
+                    ctx.all_gather(sl, row, stream=stream)
             if timed:
                 ev1[i].record(stream)
 
-        with torch.cuda.stream(stream):
-            step_rs(0, False)
-            for i in range(Ks):
-                step_rs(i, True)
-        torch.cuda.synchronize()
-        ms_rs = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Ks)]))
+        ms_rs = {}
+        for sets in (True, False):
+            with torch.cuda.stream(stream):
+                for i in range(Wm):
+                    step_rs(i, False, sets)
+                for i in range(Ks):
+                    step_rs(i, True, sets)
+            torch.cuda.synchronize()
+            ms_rs[sets] = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Ks)]))
         per = sum(bn) * w.elem_bytes
-        rs_line = {"what": "reduce_scatter then all_gather of every bucket, pipelined policy (%d KiB payload "
-                           "chunks; all_gather in groups of whole rank blocks)" % (chunk_bytes >> 10),
-                   "ms_per_step": ms_rs, "value": per / (ms_rs * 1e-3) / 1e9, "unit": "GB/s", "steps": Ks}
+        rs_line = {"what": "gb_reduce_scatter_buckets then gb_all_gather_buckets of the whole set (one pipeline "
+                           "and one graph each, payload chunks of at most 3 x %d KiB; all_gather in groups of "
+                           "whole rank blocks)" % (chunk_bytes >> 10),
+                   "ms_per_step": ms_rs[True], "value": per / (ms_rs[True] * 1e-3) / 1e9, "unit": "GB/s",
+                   "steps": Ks,
+                   "per_bucket_calls_ms_per_step": ms_rs[False]}
         del slices
     # roofline region: one hop per bucket, phase marks around every kernel
     Kr = max(2, min(K, 5))

@@ -167,6 +167,25 @@ class Context:
                                             [b[0].numel() for b in buckets], dt, _op(op), _codec(codec),
                                             block, _stream(stream)))
 
+    def reduce_scatter_buckets(self, in_buckets, out_buckets, op="sum", codec="none", block=256, stream=None):
+        """in_buckets[b]: W flat tensors of bucket b; out_buckets[b]: W
+        tensors of numel / W elements."""
+        ins = [t for b in in_buckets for t in b]
+        outs = [t for b in out_buckets for t in b]
+        dt = _dtype(ins)
+        self._check(B.gb_reduce_scatter_buckets(self.handle, [t.data_ptr() for t in ins],
+                                                [t.data_ptr() for t in outs], [b[0].numel() for b in in_buckets],
+                                                dt, _op(op), _codec(codec), block, _stream(stream)))
+
+    def all_gather_buckets(self, in_buckets, out_buckets, stream=None):
+        """in_buckets[b]: W tensors of m_b elements; out_buckets[b]: W
+        tensors of W * m_b elements."""
+        ins = [t for b in in_buckets for t in b]
+        outs = [t for b in out_buckets for t in b]
+        dt = _dtype(ins)
+        self._check(B.gb_all_gather_buckets(self.handle, [t.data_ptr() for t in ins], [t.data_ptr() for t in outs],
+                                            [b[0].numel() for b in in_buckets], dt, _stream(stream)))
+
     # ------------------------------------------------------- phase blocks
     def island_reduce(self, island, tensors, island_sum, stream=None):
         dt = _dtype(tensors)

@@ -73,6 +73,8 @@ SIGNATURES = {
     "gb_all_reduce_host": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_bucket_plan": (_i, [_P(_sz), _i, _sz, _sz, _sz, _P(_i), _P(_sz), _P(_sz), _i, _P(_i)]),
     "gb_all_reduce_buckets": (_i, [_vp, _i, _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
+    "gb_reduce_scatter_buckets": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
+    "gb_all_gather_buckets": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _vp]),
     "gb_set_phase_timing": (_i, [_vp, _i]),
     "gb_phase_times": (_i, [_vp, _i, _P(ctypes.c_float)]),
     "gb_last_phase_times": (_i, [_vp, _P(ctypes.c_float)]),
@@ -251,6 +253,19 @@ def gb_all_reduce_buckets(ctx, bucket_bufs, bucket_numel, dtype, op, codec, bloc
     nb = len(bucket_numel)
     return lib().gb_all_reduce_buckets(ctx, nb, _ptrs(bucket_bufs), _sizes(bucket_numel), dtype, op,
                                        codec, block, stream)
+
+
+def gb_reduce_scatter_buckets(ctx, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, stream=0):
+    """in_bufs / out_bufs: flat lists of n_buckets * W device pointers, bucket-major."""
+    nb = len(bucket_numel)
+    return lib().gb_reduce_scatter_buckets(ctx, nb, _ptrs(in_bufs), _ptrs(out_bufs), _sizes(bucket_numel), dtype,
+                                           op, codec, block, stream)
+
+
+def gb_all_gather_buckets(ctx, in_bufs, out_bufs, bucket_numel_in, dtype, stream=0):
+    nb = len(bucket_numel_in)
+    return lib().gb_all_gather_buckets(ctx, nb, _ptrs(in_bufs), _ptrs(out_bufs), _sizes(bucket_numel_in), dtype,
+                                       stream)
 
 
 def gb_set_phase_timing(ctx, capacity):

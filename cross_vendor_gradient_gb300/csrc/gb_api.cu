@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <functional>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -787,8 +788,11 @@ struct WorkChunk {
     uint64_t e0, m;
 };
 
-gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, void *const *bufs,
-                          cudaStream_t s) {
+// in / out: nb x W rank buffers, bucket-major.  rs == 0: all_reduce (out
+// may equal in); rs == 1: reduce_scatter, out[b * W + r] receives slice r of
+// bucket b (numel[b] / W elements).
+gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, const void *const *in,
+                          void *const *out, const size_t *numel, int rs, cudaStream_t s) {
     const int I = p.I, W = p.W;
     constexpr int R = 2;
     auto outbox = [&](int slot, int i) { return c->d_stage + ((size_t)slot * I + i) * p.part; };
@@ -809,7 +813,7 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         const int slot = i % R, ev = i % kMaxChunks;
         gb::ReduceEncodeArgs ra;
         memset(&ra, 0, sizeof ra);
-        for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)bufs[(size_t)w.b * W + r] + w.e0 * p.eb;
+        for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)in[(size_t)w.b * W + r] + w.e0 * p.eb;
         for (int q = 0; q < I; ++q) ra.payload[q] = outbox(slot, q);
         for (int q = 0; q <= I; ++q) ra.first[q] = c->first[q];
         ra.n_islands = I;
@@ -845,9 +849,22 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         GB_TRY(wait_on(c, s, c->ev_h2d[ev]));
         gb::DecodeBcastArgs da;
         memset(&da, 0, sizeof da);
-        for (int r = 0; r < W; ++r) {
-            da.dst[r] = (unsigned char *)bufs[(size_t)w.b * W + r] + w.e0 * p.eb;
-            da.group_of_rank[r] = c->island_of[r];
+        uint64_t rs_max = 0;
+        for (int r = 0; r < W; ++r) da.dst[r] = (unsigned char *)out[(size_t)w.b * W + r] + w.e0 * p.eb;
+        if (rs) {  // the parts of bucket b's slices that fall inside this chunk
+            const uint64_t ms = numel[w.b] / (uint64_t)W;
+            for (int r = 0; r < W; ++r) {
+                const uint64_t s0 = (uint64_t)r * ms;
+                const uint64_t lo = w.e0 > s0 ? w.e0 : s0;
+                const uint64_t hi = (w.e0 + w.m) < (s0 + ms) ? (w.e0 + w.m) : (s0 + ms);
+                da.dst[r] = out[(size_t)w.b * W + r];
+                if (hi > lo) {
+                    da.rs_src[r] = lo - w.e0;
+                    da.rs_len[r] = hi - lo;
+                    da.dst[r] = (unsigned char *)out[(size_t)w.b * W + r] + (lo - s0) * p.eb;
+                    if (hi - lo > rs_max) rs_max = hi - lo;
+                }
+            }
         }
         const void *received[GB_MAX_ISLANDS];
         for (int j = 0; j < I; ++j)
@@ -859,9 +876,16 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         da.inv_world = 1.0f / (float)W;
         da.n = w.m;
         da.scales_off = is_fp8(p.eff) ? round_up(w.m * p.cb, 16) : 0;
-        da.vec = 1;
-        da.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
-        GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        if (rs) {
+            da.rs = 1;
+            da.vec = ((numel[w.b] / (uint64_t)W) % 8) == 0;
+            da.tiles = (uint32_t)((rs_max + gb::kTile - 1) / gb::kTile);
+        } else {
+            da.vec = 1;
+            da.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
+        }
+        if (da.tiles > 0)
+            GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
         return GB_OK;
     };
     GB_TRY(front(0));
@@ -876,8 +900,60 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
     return GB_OK;
 }
 
-gb_status run_buckets(gb_ctx *c, int nb, void *const *bufs, const size_t *numel, gb_dtype dtype, gb_op op,
-                      gb_codec codec, int block, cudaStream_t s) {
+// A whole gradient set as one CUDA graph: the first call with a key runs
+// `enqueue` directly (loading modules, sizing grids) and remembers the key;
+// the second captures it on the context's private stream; later calls
+// replay it.  Up to 8 sets are cached (least recently used out).  `kernels`
+// is the number of kernel launches one replay makes.
+gb_status run_set_graph(gb_ctx *c, const std::vector<uint64_t> &key, int kernels,
+                        const std::function<gb_status(cudaStream_t)> &enqueue, cudaStream_t s) {
+    gb_ctx::BucketGraph *bg = nullptr;
+    for (auto &g : c->bucket_graphs)
+        if (g.key == key) bg = &g;
+    if (!bg) {  // first time: run directly, remember the shape
+        if (c->bucket_graphs.size() >= 8) {
+            size_t lru = 0;
+            for (size_t i = 1; i < c->bucket_graphs.size(); ++i)
+                if (c->bucket_graphs[i].last_use < c->bucket_graphs[lru].last_use) lru = i;
+            if (c->bucket_graphs[lru].exec) cudaGraphExecDestroy(c->bucket_graphs[lru].exec);
+            if (c->bucket_graphs[lru].graph) cudaGraphDestroy(c->bucket_graphs[lru].graph);
+            c->bucket_graphs.erase(c->bucket_graphs.begin() + lru);
+        }
+        c->bucket_graphs.emplace_back();
+        c->bucket_graphs.back().key = key;
+        c->bucket_graphs.back().last_use = ++c->clock;
+        GB_TRY(enqueue(s));
+        return end(c, s);
+    }
+    bg->last_use = ++c->clock;
+    if (!bg->exec) {
+        cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
+        gb_status st = enqueue(c->scap);
+        cudaGraph_t g = nullptr;
+        e = cudaStreamEndCapture(c->scap, &g);
+        if (st != GB_OK) {
+            if (g) cudaGraphDestroy(g);
+            return st;
+        }
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamEndCapture", e);
+        cudaGraphExec_t x = nullptr;
+        if ((e = cudaGraphInstantiate(&x, g, 0)) != cudaSuccess) {
+            cudaGraphDestroy(g);
+            return fail(c, GB_ERR_CUDA, "cudaGraphInstantiate", e);
+        }
+        bg->graph = g;
+        bg->exec = x;
+        bg->kernels = kernels;
+    }
+    cudaError_t e = cudaGraphLaunch(bg->exec, s);
+    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphLaunch", e);
+    for (int k = 0; k < bg->kernels; ++k) gb::count_launch();
+    return end(c, s);
+}
+
+gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel,
+                      gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs, cudaStream_t s) {
     // the chunk shape of the largest bucket fixes the slot size.  Chunks are
     // kBucketChunkScale x the pipeline chunk: across a gradient set the
     // pipeline fills once, so larger copies only save per-copy cost (on
@@ -901,58 +977,21 @@ gb_status run_buckets(gb_ctx *c, int nb, void *const *bufs, const size_t *numel,
     GB_TRY(grow_host(c, (size_t)c->I * 2 * p.part));
     GB_TRY(begin(c, s));
     if (!c->use_graphs) {
-        GB_TRY(enqueue_buckets(c, p, work, bufs, s));
+        GB_TRY(enqueue_buckets(c, p, work, in, out, numel, rs, s));
         return end(c, s);
     }
-    std::vector<uint64_t> key = {(uint64_t)nb, (uint64_t)dtype, (uint64_t)op, (uint64_t)p.eff, (uint64_t)p.blk,
-                                 (uint64_t)p.chunk, (uint64_t)(uintptr_t)c->d_stage, (uint64_t)(uintptr_t)c->h_stage};
+    std::vector<uint64_t> key = {1, (uint64_t)nb, (uint64_t)dtype, (uint64_t)op, (uint64_t)p.eff, (uint64_t)p.blk,
+                                 (uint64_t)p.chunk, (uint64_t)(uintptr_t)c->d_stage, (uint64_t)(uintptr_t)c->h_stage,
+                                 (uint64_t)rs};
     for (int b = 0; b < nb; ++b) {
         key.push_back(numel[b]);
-        for (int r = 0; r < c->W; ++r) key.push_back((uint64_t)(uintptr_t)bufs[(size_t)b * c->W + r]);
-    }
-    gb_ctx::BucketGraph *bg = nullptr;
-    for (auto &g : c->bucket_graphs)
-        if (g.key == key) bg = &g;
-    if (!bg) {  // first time: run directly, remember the shape
-        if (c->bucket_graphs.size() >= 8) {
-            size_t lru = 0;
-            for (size_t i = 1; i < c->bucket_graphs.size(); ++i)
-                if (c->bucket_graphs[i].last_use < c->bucket_graphs[lru].last_use) lru = i;
-            if (c->bucket_graphs[lru].exec) cudaGraphExecDestroy(c->bucket_graphs[lru].exec);
-            if (c->bucket_graphs[lru].graph) cudaGraphDestroy(c->bucket_graphs[lru].graph);
-            c->bucket_graphs.erase(c->bucket_graphs.begin() + lru);
+        for (int r = 0; r < c->W; ++r) {
+            key.push_back((uint64_t)(uintptr_t)in[(size_t)b * c->W + r]);
+            key.push_back((uint64_t)(uintptr_t)out[(size_t)b * c->W + r]);
         }
-        c->bucket_graphs.emplace_back();
-        c->bucket_graphs.back().key = key;
-        c->bucket_graphs.back().last_use = ++c->clock;
-        GB_TRY(enqueue_buckets(c, p, work, bufs, s));
-        return end(c, s);
     }
-    bg->last_use = ++c->clock;
-    if (!bg->exec) {
-        cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
-        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
-        gb_status st = enqueue_buckets(c, p, work, bufs, c->scap);
-        cudaGraph_t g = nullptr;
-        e = cudaStreamEndCapture(c->scap, &g);
-        if (st != GB_OK) {
-            if (g) cudaGraphDestroy(g);
-            return st;
-        }
-        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamEndCapture", e);
-        cudaGraphExec_t x = nullptr;
-        if ((e = cudaGraphInstantiate(&x, g, 0)) != cudaSuccess) {
-            cudaGraphDestroy(g);
-            return fail(c, GB_ERR_CUDA, "cudaGraphInstantiate", e);
-        }
-        bg->graph = g;
-        bg->exec = x;
-        bg->kernels = 2 * (int)work.size();
-    }
-    cudaError_t e = cudaGraphLaunch(bg->exec, s);
-    if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaGraphLaunch", e);
-    for (int k = 0; k < bg->kernels; ++k) gb::count_launch();
-    return end(c, s);
+    return run_set_graph(c, key, 2 * (int)work.size(),
+                         [&](cudaStream_t st) { return enqueue_buckets(c, p, work, in, out, numel, rs, st); }, s);
 }
 
 // Capture one pipelined all_reduce on the context's capture stream and
@@ -1097,6 +1136,80 @@ gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n
     GB_TRY(mark(c, mm, 5, s));
     commit_marks(c, 1, I > 1);
     return end(c, s);
+}
+
+// all_gather of every bucket as one pipeline (bucket b: W inputs of
+// numel_in[b] elements, W outputs of W * numel_in[b]).  Bucket b's rank
+// blocks cross the bridge through host slot b % 2: groups of consecutive
+// ranks of one island (about chunk_bytes) go device -> host on copy stream
+// D, each group on to every other leader on stream H as soon as it has
+// landed; the in-island copy kernels of bucket b then run on s while the
+// next bucket's blocks are on the link.  A slot is written again only after
+// the host -> device copies that read it.
+gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel_in,
+                             size_t eb, size_t slot_bytes, cudaStream_t s) {
+    const int W = c->W, I = c->I;
+    cudaStream_t D = c->sd, H = c->sh;
+    if (c->inject == GB_INJECT_BRIDGE) {
+        c->inject = 0;
+        return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
+    }
+    GB_TRY(record(c, c->ev_join_d, s));  // the copy streams start after the caller's prior work
+    GB_TRY(wait_on(c, D, c->ev_join_d));
+    GB_TRY(wait_on(c, H, c->ev_join_d));
+    int ng = 0, done = 0;
+    for (int b = 0; b < nb; ++b) {
+        if (numel_in[b] == 0) continue;
+        const size_t mb = numel_in[b] * eb;
+        const int slot = done % 2;
+        unsigned char *host = c->h_stage + (size_t)slot * slot_bytes;
+        const void *const *bin = in + (size_t)b * W;
+        void *const *bout = out + (size_t)b * W;
+        if (done >= 2) GB_TRY(wait_on(c, D, c->ev_in[slot]));  // the slot's last reader has finished
+        const size_t per_s = mb >= c->chunk_bytes ? 1 : c->chunk_bytes / mb;
+        const int per = per_s > (size_t)W ? W : (int)per_s;
+        for (int i = 0; i < I; ++i) {
+            for (int q0 = c->first[i]; q0 < c->first[i + 1]; q0 += per) {
+                const int q1 = (q0 + per) < c->first[i + 1] ? (q0 + per) : c->first[i + 1];
+                for (int q = q0; q < q1; ++q)
+                    GB_TRY(copy_async(c, host + (size_t)q * mb, bin[q], mb, cudaMemcpyDeviceToHost, D));
+                cudaEvent_t ev = c->ev_ag[ng++ % GB_MAX_RANKS];
+                GB_TRY(record(c, ev, D));
+                GB_TRY(wait_on(c, H, ev));
+                for (int g = 0; g < I; ++g) {
+                    if (g == i) continue;
+                    unsigned char *lead = (unsigned char *)bout[c->first[g]];
+                    GB_TRY(copy_async(c, lead + (size_t)q0 * mb, host + (size_t)q0 * mb, (size_t)(q1 - q0) * mb,
+                                      cudaMemcpyHostToDevice, H));
+                }
+            }
+        }
+        GB_TRY(record(c, c->ev_in[slot], H));  // bucket b has landed; slot free again
+        GB_TRY(wait_on(c, s, c->ev_in[slot]));
+        for (int i = 0; i < I; ++i) {
+            gb::CopyArgs a;
+            memset(&a, 0, sizeof a);
+            const unsigned char *lead = (const unsigned char *)bout[c->first[i]];
+            a.n_jobs = W;
+            a.bytes = mb;
+            a.vec = (mb % 16) == 0;
+            for (int q = 0; q < W; ++q) {
+                const bool own = c->island_of[q] == i;
+                a.src[q] = own ? (const unsigned char *)bin[q] : lead + (size_t)q * mb;
+                a.dst_off[q] = (size_t)q * mb;
+                a.dst_lo[q] = 0;
+                a.dst_hi[q] = c->size[i];
+            }
+            for (int k = 0; k < c->size[i]; ++k) a.dst[k] = (unsigned char *)bout[c->first[i] + k];
+            GB_TRY(check_launch(c, gb::launch_copy(a, s), "all_gather copy"));
+        }
+        ++done;
+    }
+    GB_TRY(record(c, c->ev_join_d, D));
+    GB_TRY(record(c, c->ev_join_h, H));
+    GB_TRY(wait_on(c, s, c->ev_join_d));
+    GB_TRY(wait_on(c, s, c->ev_join_h));
+    return GB_OK;
 }
 
 // Reduce-bridge-broadcast over W rank buffers `in` (n elements).  rs == 0:
@@ -1827,12 +1940,96 @@ gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bu
     if (total == 0) return GB_OK;
     if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0 && !c->sharded) {
         GB_TRY(bind(c));
-        return run_buckets(c, n_buckets, bucket_bufs, bucket_numel, dtype, op, codec, block, (cudaStream_t)stream);
+        return run_buckets(c, n_buckets, (const void *const *)bucket_bufs, bucket_bufs, bucket_numel, dtype, op, codec,
+                           block, 0, (cudaStream_t)stream);
     }
     for (int b = 0; b < n_buckets; ++b)
         if (bucket_numel[b] > 0)
             GB_TRY(gb_all_reduce(c, bucket_bufs + (size_t)b * c->W, bucket_numel[b], dtype, op, codec, block,
                                  stream));
+    return GB_OK;
+}
+
+gb_status gb_reduce_scatter_buckets(gb_ctx *c, int n_buckets, const void *const *in_bufs, void *const *out_bufs,
+                                    const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec, int block,
+                                    gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    if (n_buckets < 0 || (n_buckets > 0 && (!in_bufs || !out_bufs || !bucket_numel)))
+        return set_msg(c, GB_ERR_INVALID_ARG, "bucket arrays");
+    GB_TRY(check_collective(c, 0, dtype, op, codec, block));
+    size_t total = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        GB_TRY(check_n(c, bucket_numel[b]));
+        if (bucket_numel[b] == 0) continue;  // an empty bucket's pointers are never used
+        if (bucket_numel[b] % (size_t)c->W)
+            return set_msg(c, GB_ERR_INVALID_ARG, "bucket %d: %zu elements is not a multiple of W = %d", b,
+                           bucket_numel[b], c->W);
+        GB_TRY(check_dev_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
+        GB_TRY(check_dev_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
+        total += bucket_numel[b];
+    }
+    if (total == 0) return GB_OK;
+    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
+        GB_TRY(bind(c));
+        return run_buckets(c, n_buckets, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, 1,
+                           (cudaStream_t)stream);
+    }
+    for (int b = 0; b < n_buckets; ++b)
+        if (bucket_numel[b] > 0)
+            GB_TRY(gb_reduce_scatter(c, in_bufs + (size_t)b * c->W, out_bufs + (size_t)b * c->W, bucket_numel[b],
+                                     dtype, op, codec, block, stream));
+    return GB_OK;
+}
+
+gb_status gb_all_gather_buckets(gb_ctx *c, int n_buckets, const void *const *in_bufs, void *const *out_bufs,
+                                const size_t *bucket_numel_in, gb_dtype dtype, gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    if (n_buckets < 0 || (n_buckets > 0 && (!in_bufs || !out_bufs || !bucket_numel_in)))
+        return set_msg(c, GB_ERR_INVALID_ARG, "bucket arrays");
+    GB_TRY(check_dtype(c, dtype));
+    size_t total = 0, mb_max = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        GB_TRY(check_n(c, bucket_numel_in[b]));
+        GB_TRY(check_n(c, bucket_numel_in[b] * (size_t)c->W));
+        if (bucket_numel_in[b] == 0) continue;
+        GB_TRY(check_dev_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
+        GB_TRY(check_dev_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
+        total += bucket_numel_in[b];
+        const size_t mb = bucket_numel_in[b] * elem_bytes(dtype);
+        if (mb > mb_max) mb_max = mb;
+    }
+    if (total == 0) return GB_OK;
+    if (c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
+        GB_TRY(bind(c));
+        cudaStream_t s = (cudaStream_t)stream;
+        const size_t slot_bytes = round_up((size_t)c->W * mb_max, 256);
+        GB_TRY(grow_host(c, 2 * slot_bytes));
+        GB_TRY(begin(c, s));
+        const size_t eb = elem_bytes(dtype);
+        int nonempty = 0;
+        for (int b = 0; b < n_buckets; ++b) nonempty += bucket_numel_in[b] > 0;
+        auto enqueue = [&](cudaStream_t st) {
+            return enqueue_ag_buckets(c, n_buckets, in_bufs, out_bufs, bucket_numel_in, eb, slot_bytes, st);
+        };
+        if (!c->use_graphs) {
+            GB_TRY(enqueue(s));
+            return end(c, s);
+        }
+        std::vector<uint64_t> key = {2, (uint64_t)n_buckets, (uint64_t)dtype, (uint64_t)c->chunk_bytes,
+                                     (uint64_t)(uintptr_t)c->h_stage};
+        for (int b = 0; b < n_buckets; ++b) {
+            key.push_back(bucket_numel_in[b]);
+            for (int r = 0; r < c->W; ++r) {
+                key.push_back((uint64_t)(uintptr_t)in_bufs[(size_t)b * c->W + r]);
+                key.push_back((uint64_t)(uintptr_t)out_bufs[(size_t)b * c->W + r]);
+            }
+        }
+        return run_set_graph(c, key, nonempty * c->I, enqueue, s);
+    }
+    for (int b = 0; b < n_buckets; ++b)
+        if (bucket_numel_in[b] > 0)
+            GB_TRY(gb_all_gather(c, in_bufs + (size_t)b * c->W, out_bufs + (size_t)b * c->W, bucket_numel_in[b],
+                                 dtype, stream));
     return GB_OK;
 }
 

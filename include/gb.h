@@ -373,6 +373,34 @@ gb_status gb_all_reduce_buckets(gb_ctx *ctx, int n_buckets, void *const *bucket_
                                 const size_t *bucket_numel, gb_dtype dtype, gb_op op,
                                 gb_codec codec, int block, gb_stream stream);
 
+/* reduce_scatter of every bucket (the gradient sets of a sharded data
+ * parallel step): out_bufs[b * W + r] receives slice r (bucket_numel[b] / W
+ * elements) of what gb_all_reduce would compute on bucket b's inputs
+ * in_bufs[b * W + 0 .. W - 1] (in bucket order; the island sums are encoded
+ * whole, with the all_reduce codec blocks).  bucket_numel[b] must be a
+ * multiple of W; inputs are not modified; outputs must not overlap inputs.
+ * Under the pipelined policy (float32 / bfloat16 SUM / AVG, two or more
+ * islands, no phase marks kept) the buckets run as one pipeline of chunks,
+ * as in gb_all_reduce_buckets, captured as one CUDA graph per set from the
+ * second call with the same buffers; otherwise one gb_reduce_scatter per
+ * bucket.  Empty buckets are allowed (their pointers may be NULL). */
+gb_status gb_reduce_scatter_buckets(gb_ctx *ctx, int n_buckets, const void *const *in_bufs, void *const *out_bufs,
+                                    const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec,
+                                    int block, gb_stream stream);
+
+/* all_gather of every bucket, exact: out_bufs[b * W + r] (W *
+ * bucket_numel_in[b] elements) receives in_bufs[b * W + 0], ...,
+ * in_bufs[b * W + W - 1] concatenated, for every r.  Under the pipelined
+ * policy (two or more islands, no phase marks kept) the buckets run as one
+ * pipeline: each bucket's rank blocks cross the bridge in groups of about
+ * chunk_bytes through two alternating host slots, and its in-island copy
+ * kernels overlap the next bucket's copies; captured as one CUDA graph per
+ * set from the second call with the same buffers.  Otherwise one
+ * gb_all_gather per bucket.  Empty buckets are allowed (pointers may be
+ * NULL).  Inputs must not overlap outputs. */
+gb_status gb_all_gather_buckets(gb_ctx *ctx, int n_buckets, const void *const *in_bufs, void *const *out_bufs,
+                                const size_t *bucket_numel_in, gb_dtype dtype, gb_stream stream);
+
 /* --------------------------------------------------------- phase timing */
 
 /* gpubridge README, "Observing collectives": timing marks per phase, taken

@@ -144,12 +144,20 @@ def test_argument_errors_need_no_device():
         assert B.gb_decompress_island_broadcast(ctx, pl4[:3] + [0], 10, 0, 0, 2, 256, fake) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce_compress(ctx, fake, 0, 0, 2, 256, pl) == B.GB_OK
         assert B.gb_decompress_island_broadcast(ctx, pl4, 0, 1, 1, 3, 128, fake) == B.GB_OK
+        # bucket sets
+        assert B.gb_reduce_scatter_buckets(ctx, fake, fake, [10], 0, 0, 2, 256) == B.GB_ERR_INVALID_ARG  # 10 % 4
+        assert B.gb_reduce_scatter_buckets(ctx, fake[:3] + [0], fake, [8], 0, 0, 2, 256) == B.GB_ERR_INVALID_ARG
+        assert B.gb_reduce_scatter_buckets(ctx, fake, fake, [8], 0, 0, 2, 64) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_all_gather_buckets(ctx, fake, fake, [8], 9) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert B.gb_all_gather_buckets(ctx, fake, fake[:3] + [0x10008], [8], 0) == B.GB_ERR_MISALIGNED
+        assert B.gb_reduce_scatter_buckets(ctx, [0] * 8, [0] * 8, [0, 0], 0, 0, 2, 256) == B.GB_OK  # empty
+        assert B.gb_all_gather_buckets(ctx, [0] * 4, [0] * 4, [0], 1) == B.GB_OK
         # n == 0 is a valid no-op, answered without a device
         assert B.gb_all_reduce(ctx, fake, 0, 0, 0, 2, 256) == B.GB_OK
         assert B.gb_all_gather(ctx, fake, fake, 0, 1) == B.GB_OK
         # none of these is sticky; the last one is remembered
         assert B.gb_context_status(ctx) == B.GB_OK
-        assert B.gb_last_error(ctx) == B.GB_ERR_INVALID_ARG  # the last refused call above
+        assert B.gb_last_error(ctx) == B.GB_ERR_MISALIGNED  # the last refused call: the misaligned bucket set
         assert B.gb_debug_inject(ctx, 77) == B.GB_ERR_INVALID_ARG
     finally:
         B.gb_destroy(ctx)

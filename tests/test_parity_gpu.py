@@ -594,3 +594,64 @@ def test_pipelined_broadcast_is_exact(sizes, dtype):
                 torch.cuda.synchronize()
                 for r in range(W):
                     assert_bits_equal(to_host(bufs[r]), want[r], "bcast %s n=%d src=%d rank %d" % (sizes, n, src, r))
+
+
+@pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (4, 4), (2, 1, 3), (3,)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bucket_sets_reduce_scatter_then_all_gather(codec, block, sizes, dtype):
+    """gb_reduce_scatter_buckets and gb_all_gather_buckets (one pipeline, one
+    graph per set): every bucket's slices are the oracle's reduce_scatter,
+    and the gathered buffers its all_reduce; empty buckets are skipped;
+    direct, captured and replayed calls agree."""
+    W = sum(sizes)
+    slices = [500, 0, 1, 3000, 64, 7919]  # elements per rank slice, per bucket
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(4096)
+        for op in ("sum", "avg"):
+            xs = [inputs(sizes, max(m, 1) * W, dtype, cid=120 + b) for b, m in enumerate(slices)]
+            ins = [[to_dev(x[:m * W]) for x in row] for row, m in zip(xs, slices)]
+            for call in range(3):
+                outs = [[torch.full((m,), 7.0, device="cuda").to(ins[0][0].dtype) for _ in range(W)] for m in slices]
+                ctx.reduce_scatter_buckets(ins, outs, op, codec, block)
+                gathered = [[torch.empty(m * W, dtype=ins[0][0].dtype, device="cuda") for _ in range(W)]
+                            for m in slices]
+                ctx.all_gather_buckets(outs, gathered)
+                torch.cuda.synchronize()
+                for b, m in enumerate(slices):
+                    if m == 0:
+                        continue
+                    part = [x[:m * W] for x in xs[b]]
+                    want_rs = orc.reduce_scatter(part, sizes, op, codec, block)
+                    want_ar = orc.all_reduce(part, sizes, op, codec, block)
+                    for r in range(W):
+                        assert_bits_equal(to_host(outs[b][r]), want_rs[r], "RS bucket %d rank %d call %d" % (b, r, call))
+                        assert_bits_equal(to_host(gathered[b][r]), want_ar[r], "AG bucket %d rank %d call %d" % (b, r, call))
+                        assert_bits_equal(to_host(ins[b][r]), part[r], "inputs untouched")
+
+
+def test_bucket_sets_exact_and_plain_paths():
+    """MAX and the plain policy take the per-bucket loop and agree with the
+    oracle too."""
+    sizes = (2, 2)
+    W = 4
+    slices = [100, 0, 257]
+    with Context(sizes) as ctx:
+        for chunk, op in ((0, "sum"), (2 << 20, "max")):
+            ctx.set_pipeline(chunk)
+            xs = [inputs(sizes, max(m, 1) * W, "f32", cid=140 + b) for b, m in enumerate(slices)]
+            ins = [[to_dev(x[:m * W]) for x in row] for row, m in zip(xs, slices)]
+            outs = [[torch.empty(m, device="cuda") for _ in range(W)] for m in slices]
+            ctx.reduce_scatter_buckets(ins, outs, op, "none", 256)
+            gathered = [[torch.empty(m * W, device="cuda") for _ in range(W)] for m in slices]
+            ctx.all_gather_buckets(outs, gathered)
+            torch.cuda.synchronize()
+            for b, m in enumerate(slices):
+                if m == 0:
+                    continue
+                part = [x[:m * W] for x in xs[b]]
+                want_rs = orc.reduce_scatter(part, sizes, op, "none", 256)
+                want_ar = orc.all_reduce(part, sizes, op, "none", 256)
+                for r in range(W):
+                    assert_bits_equal(to_host(outs[b][r]), want_rs[r], "RS %s bucket %d rank %d" % (op, b, r))
+                    assert_bits_equal(to_host(gathered[b][r]), want_ar[r], "AG %s bucket %d rank %d" % (op, b, r))

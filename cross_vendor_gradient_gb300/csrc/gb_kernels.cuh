@@ -128,12 +128,11 @@ int sm_count();
 constexpr uint64_t kMaxWaves = 32;
 template <auto Kern, typename Args>
 cudaError_t launch_grid(uint64_t tiles_per_unit, unsigned units, const Args &a, cudaStream_t s) {
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    static const int per_sm = [] {  // initialised once, thread-safe
         int v = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, Kern, 256, 0);
-        per_sm = v > 0 ? v : 1;
-    }
+        return v > 0 ? v : 1;
+    }();
     const uint64_t cap = kMaxWaves * (uint64_t)per_sm * (uint64_t)sm_count();
     const uint64_t per_unit_cap = cap / units > 0 ? cap / units : 1;
     const uint64_t want = (tiles_per_unit + 7) / 8;  // 8 warps (tiles) per block

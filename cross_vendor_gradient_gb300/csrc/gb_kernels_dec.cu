@@ -29,13 +29,12 @@ uint64_t launches() { return g_launches.load(); }
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int sm_count() {
-    static int count = 0;
-    if (count == 0) {
+    static const int count = [] {  // initialised once, thread-safe
         int dev = 0, v = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        count = v > 0 ? v : 1;
-    }
+        return v > 0 ? v : 1;
+    }();
     return count;
 }
 

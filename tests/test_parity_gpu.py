@@ -655,3 +655,45 @@ def test_bucket_sets_exact_and_plain_paths():
                 for r in range(W):
                     assert_bits_equal(to_host(outs[b][r]), want_rs[r], "RS %s bucket %d rank %d" % (op, b, r))
                     assert_bits_equal(to_host(gathered[b][r]), want_ar[r], "AG %s bucket %d rank %d" % (op, b, r))
+
+
+def test_two_contexts_on_two_threads_and_streams():
+    """Two contexts, each driven by its own host thread on its own stream,
+    run pipelined all_reduces, bucket sets and reduce_scatters at the same
+    time; every result matches the oracle (no state is shared between
+    contexts)."""
+    import threading
+    jobs = [((2, 2), "e4m3", 256, 31), ((1, 3), "bf16", 256, 32)]
+    errors = []
+
+    def work(sizes, codec, block, cid):
+        try:
+            W = sum(sizes)
+            stream = torch.cuda.Stream()
+            with Context(sizes) as ctx:
+                ctx.set_pipeline(4096)
+                for rep in range(4):
+                    n = 20000 + 256 * rep
+                    xs = inputs(sizes, n, "f32", cid=cid + rep)
+                    with torch.cuda.stream(stream):
+                        bufs = [to_dev(x) for x in xs]
+                        ctx.all_reduce(bufs, "sum", codec, block, stream=stream)
+                        outs = [torch.empty(n // W, device="cuda") for _ in range(W)]
+                        ins = [to_dev(x[:n // W * W]) for x in xs]
+                        ctx.reduce_scatter(ins, outs, "avg", codec, block, stream=stream)
+                    stream.synchronize()
+                    want = orc.all_reduce(xs, sizes, "sum", codec, block)
+                    want_rs = orc.reduce_scatter([x[:n // W * W] for x in xs], sizes, "avg", codec, block)
+                    for r in range(W):
+                        assert_bits_equal(to_host(bufs[r]), want[r], "thread %s rank %d" % (sizes, r))
+                        assert_bits_equal(to_host(outs[r]), want_rs[r], "thread %s RS rank %d" % (sizes, r))
+        except BaseException as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=work, args=j) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    if errors:
+        raise errors[0]

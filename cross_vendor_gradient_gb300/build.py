@@ -15,9 +15,10 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgb.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 
-SOURCES = ["gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_kernels_exact.cu", "gb_api.cu", "gb_noalloc.cu"]
+SOURCES = ["gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_kernels_exact.cu", "gb_runtime.cu", "gb_api.cu",
+           "gb_noalloc.cu"]
 HEADERS = [os.path.join(INCLUDE, "gb.h")] + [
-    os.path.join(CSRC, f) for f in ("gb_device.cuh", "gb_kernels.cuh")]
+    os.path.join(CSRC, f) for f in ("gb_device.cuh", "gb_kernels.cuh", "gb_internal.cuh")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]

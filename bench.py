@@ -56,6 +56,7 @@ def parse():
     p.add_argument("--dtype", default=None, help="rank dtype override (f32 bf16 f16 f64 i8 u8 i32 i64)")
     p.add_argument("--op", default=None, help="op override (sum avg max min)")
     p.add_argument("--n", type=int, default=None, help="override elements per rank")
+    p.add_argument("--islands", default=None, help="override the island sizes, e.g. 4,4 (single-buffer workloads)")
     p.add_argument("--chunk-kib", type=int, default=None,
                    help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
     p.add_argument("--no-graphs", action="store_true")
@@ -263,9 +264,11 @@ def run_gb(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
-    if args.dtype or args.op:
+    if args.dtype or args.op or args.islands:
         import dataclasses
-        w = dataclasses.replace(w, dtype=args.dtype or w.dtype, op=args.op or w.op)
+        w = dataclasses.replace(w, dtype=args.dtype or w.dtype, op=args.op or w.op,
+                                island_sizes=tuple(int(v) for v in args.islands.split(",")) if args.islands
+                                else w.island_sizes)
     exact = w.op in ("max", "min") or w.dtype not in ("f32", "bf16")
     codec = "none" if exact else (args.codec or w.codecs[0])
     n = args.n or w.n

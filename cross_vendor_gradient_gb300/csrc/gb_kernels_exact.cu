@@ -90,6 +90,20 @@ __device__ __forceinline__ PayloadT<T, OP> to_payload(typename Ex<T>::A a) {
     else return Ex<T>::narrow(a);
 }
 
+// 8-bit integers: four lanes per 32-bit word with the per-byte SIMD
+// intrinsics.  MAX / MIN of integers have no tie to break (equal values are
+// equal bits) and __vadd4 wraps each byte modulo 256, so a word-wise fold
+// gives the same bytes as the element-wise one.
+template <typename T>
+constexpr bool kByteSimd = sizeof(T) == 1 && std::is_integral<T>::value;
+
+template <typename T, int OP>
+__device__ __forceinline__ uint32_t fold4(uint32_t a, uint32_t b) {
+    if constexpr (OP == GB_MAX) return std::is_signed<T>::value ? __vmaxs4(a, b) : __vmaxu4(a, b);
+    else if constexpr (OP == GB_MIN) return std::is_signed<T>::value ? __vmins4(a, b) : __vminu4(a, b);
+    else return __vadd4(a, b);
+}
+
 // 16 bytes of T per thread step.
 template <typename T> struct V16 {
     static constexpr int N = 16 / sizeof(T);
@@ -119,6 +133,18 @@ __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ Re
          vi += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t j0 = vi * N;
         const int cnt = (a.n - j0) < (uint64_t)N ? (int)(a.n - j0) : N;
+        if constexpr (kByteSimd<T>) {
+            if (cnt == N) {
+                uint4 acc = ld_u4((const T *)a.src[r0] + j0);
+                for (int q = 1; q < K; ++q) {
+                    const uint4 y = ld_u4((const T *)a.src[r0 + q] + j0);
+                    acc = make_uint4(fold4<T, OP>(acc.x, y.x), fold4<T, OP>(acc.y, y.y), fold4<T, OP>(acc.z, y.z),
+                                     fold4<T, OP>(acc.w, y.w));
+                }
+                st_u4(out + j0, acc);
+                continue;
+            }
+        }
         A s[N];
         if (cnt == N) {
             const V16<T> x = load16((const T *)a.src[r0] + j0);
@@ -172,8 +198,20 @@ __global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ D
          vi += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t l0 = vi * N;
         const int cnt = (limit - l0) < (uint64_t)N ? (int)(limit - l0) : N;
-        A t[N];
         const bool full = a.vec && cnt == N;
+        if constexpr (kByteSimd<T> && OP != GB_AVG) {
+            if (full) {
+                uint4 acc = ld_u4((const T *)a.payload[g][0] + gofs + l0);
+                for (int j = 1; j < a.n_src; ++j) {
+                    const uint4 y = ld_u4((const T *)a.payload[g][j] + gofs + l0);
+                    acc = make_uint4(fold4<T, OP>(acc.x, y.x), fold4<T, OP>(acc.y, y.y), fold4<T, OP>(acc.z, y.z),
+                                     fold4<T, OP>(acc.w, y.w));
+                }
+                for (int r = r_lo; r < r_hi; ++r) st_stream_u4((T *)a.dst[r] + l0, acc);
+                continue;
+            }
+        }
+        A t[N];
         for (int j = 0; j < a.n_src; ++j) {
             const P *p = (const P *)a.payload[g][j] + gofs + l0;
             P x[N];

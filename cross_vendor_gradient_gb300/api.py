@@ -167,6 +167,19 @@ class Context:
                                             [b[0].numel() for b in buckets], dt, _op(op), _codec(codec),
                                             block, _stream(stream)))
 
+    def all_reduce_buckets_ef(self, buckets, residuals, op="sum", codec="none", block=256, stream=None):
+        """buckets[b]: W flat tensors; residuals[b]: I float32 tensors of the
+        bucket's length (zero at the start, kept across steps)."""
+        flat = [t for b in buckets for t in b]
+        res = [r for b in residuals for r in b]
+        for r in res:
+            if r.dtype != torch.float32 or not r.is_contiguous():
+                raise GbError(B.GB_ERR_INVALID_ARG, "residuals must be contiguous float32 tensors")
+        dt = _dtype(flat)
+        self._check(B.gb_all_reduce_buckets_ef(self.handle, [t.data_ptr() for t in flat], [r.data_ptr() for r in res],
+                                               [b[0].numel() for b in buckets], dt, _op(op), _codec(codec), block,
+                                               _stream(stream)))
+
     def reduce_scatter_buckets(self, in_buckets, out_buckets, op="sum", codec="none", block=256, stream=None):
         """in_buckets[b]: W flat tensors of bucket b; out_buckets[b]: W
         tensors of numel / W elements."""

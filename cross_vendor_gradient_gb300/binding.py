@@ -73,6 +73,7 @@ SIGNATURES = {
     "gb_all_reduce_host": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_bucket_plan": (_i, [_P(_sz), _i, _sz, _sz, _sz, _P(_i), _P(_sz), _P(_sz), _i, _P(_i)]),
     "gb_all_reduce_buckets": (_i, [_vp, _i, _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
+    "gb_all_reduce_buckets_ef": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
     "gb_reduce_scatter_buckets": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
     "gb_all_gather_buckets": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _vp]),
     "gb_set_phase_timing": (_i, [_vp, _i]),
@@ -253,6 +254,13 @@ def gb_all_reduce_buckets(ctx, bucket_bufs, bucket_numel, dtype, op, codec, bloc
     nb = len(bucket_numel)
     return lib().gb_all_reduce_buckets(ctx, nb, _ptrs(bucket_bufs), _sizes(bucket_numel), dtype, op,
                                        codec, block, stream)
+
+
+def gb_all_reduce_buckets_ef(ctx, bucket_bufs, residuals, bucket_numel, dtype, op, codec, block, stream=0):
+    """residuals: flat list of n_buckets * I float32 device pointers, bucket-major."""
+    nb = len(bucket_numel)
+    return lib().gb_all_reduce_buckets_ef(ctx, nb, _ptrs(bucket_bufs), _ptrs(residuals), _sizes(bucket_numel),
+                                          dtype, op, codec, block, stream)
 
 
 def gb_reduce_scatter_buckets(ctx, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, stream=0):

@@ -640,31 +640,52 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes_,
     return GB_OK;
 }
 
-gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bufs,
-                                const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec,
-                                int block, gb_stream stream) {
+// gb_all_reduce_buckets with (res != NULL) or without error feedback.
+static gb_status all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bufs, float *const *res,
+                                    const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec,
+                                    int block, gb_stream stream) {
     GB_TRY(check_ctx(c));
     if (n_buckets < 0 || (n_buckets > 0 && (!bucket_bufs || !bucket_numel)))
         return set_msg(c, GB_ERR_INVALID_ARG, "bucket arrays");
     GB_TRY(check_collective(c, 0, dtype, op, codec, block));
+    if (res && is_exact(dtype, op))
+        return set_msg(c, GB_ERR_UNSUPPORTED_OP, "error feedback applies to float32 / bfloat16 SUM / AVG");
     for (int b = 0; b < n_buckets; ++b) {
         GB_TRY(check_n(c, bucket_numel[b]));
-        if (bucket_numel[b] > 0)  // an empty bucket's pointers are never used
-            GB_TRY(check_dev_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
+        if (bucket_numel[b] == 0) continue;  // an empty bucket's pointers are never used
+        GB_TRY(check_dev_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
+        if (res)
+            GB_TRY(check_dev_bufs(c, (const void *const *)(res + (size_t)b * c->I), c->I, "residuals"));
     }
     size_t total = 0;
     for (int b = 0; b < n_buckets; ++b) total += bucket_numel[b];
     if (total == 0) return GB_OK;
     if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0 && !c->sharded) {
         GB_TRY(bind(c));
-        return run_buckets(c, n_buckets, (const void *const *)bucket_bufs, bucket_bufs, bucket_numel, dtype, op, codec,
-                           block, 0, (cudaStream_t)stream);
+        return run_buckets(c, n_buckets, (const void *const *)bucket_bufs, bucket_bufs, bucket_numel, dtype, op,
+                           codec, block, 0, res, (cudaStream_t)stream);
     }
-    for (int b = 0; b < n_buckets; ++b)
-        if (bucket_numel[b] > 0)
-            GB_TRY(gb_all_reduce(c, bucket_bufs + (size_t)b * c->W, bucket_numel[b], dtype, op, codec, block,
-                                 stream));
+    for (int b = 0; b < n_buckets; ++b) {
+        if (bucket_numel[b] == 0) continue;
+        if (res)
+            GB_TRY(gb_all_reduce_ef(c, bucket_bufs + (size_t)b * c->W, res + (size_t)b * c->I, bucket_numel[b], dtype,
+                                    op, codec, block, stream));
+        else
+            GB_TRY(gb_all_reduce(c, bucket_bufs + (size_t)b * c->W, bucket_numel[b], dtype, op, codec, block, stream));
+    }
     return GB_OK;
+}
+
+gb_status gb_all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucket_bufs, const size_t *bucket_numel,
+                                gb_dtype dtype, gb_op op, gb_codec codec, int block, gb_stream stream) {
+    return all_reduce_buckets(c, n_buckets, bucket_bufs, nullptr, bucket_numel, dtype, op, codec, block, stream);
+}
+
+gb_status gb_all_reduce_buckets_ef(gb_ctx *c, int n_buckets, void *const *bucket_bufs, float *const *residuals,
+                                   const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec, int block,
+                                   gb_stream stream) {
+    if (c && n_buckets > 0 && !residuals) return set_msg(c, GB_ERR_INVALID_ARG, "residuals is NULL");
+    return all_reduce_buckets(c, n_buckets, bucket_bufs, residuals, bucket_numel, dtype, op, codec, block, stream);
 }
 
 gb_status gb_reduce_scatter_buckets(gb_ctx *c, int n_buckets, const void *const *in_bufs, void *const *out_bufs,
@@ -688,7 +709,7 @@ gb_status gb_reduce_scatter_buckets(gb_ctx *c, int n_buckets, const void *const 
     if (total == 0) return GB_OK;
     if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
         GB_TRY(bind(c));
-        return run_buckets(c, n_buckets, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, 1,
+        return run_buckets(c, n_buckets, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, 1, nullptr,
                            (cudaStream_t)stream);
     }
     for (int b = 0; b < n_buckets; ++b)

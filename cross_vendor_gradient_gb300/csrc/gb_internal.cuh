@@ -193,11 +193,12 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
 gb_status ensure_links(gb_ctx *c, int L);
 gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, cudaStream_t s);
 gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, const void *const *in,
-                          void *const *out, const size_t *numel, int rs, cudaStream_t s);
+                          void *const *out, const size_t *numel, int rs, float *const *res, cudaStream_t s);
 gb_status run_set_graph(gb_ctx *c, const std::vector<uint64_t> &key, int kernels,
                         const std::function<gb_status(cudaStream_t)> &enqueue, cudaStream_t s);
 gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel,
-                      gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs, cudaStream_t s);
+                      gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs, float *const *res,
+                      cudaStream_t s);
 gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, float *const *res, bool timed,
                       GraphEntry *ge);
 GraphEntry *find_graph(gb_ctx *c, const GraphKey &k);

@@ -653,7 +653,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
 // may equal in); rs == 1: reduce_scatter, out[b * W + r] receives slice r of
 // bucket b (numel[b] / W elements).
 gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, const void *const *in,
-                          void *const *out, const size_t *numel, int rs, cudaStream_t s) {
+                          void *const *out, const size_t *numel, int rs, float *const *res, cudaStream_t s) {
     const int I = p.I, W = p.W;
     constexpr int R = 2;
     auto outbox = [&](int slot, int i) { return c->d_stage + ((size_t)slot * I + i) * p.part; };
@@ -675,6 +675,7 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         gb::ReduceEncodeArgs ra;
         memset(&ra, 0, sizeof ra);
         for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)in[(size_t)w.b * W + r] + w.e0 * p.eb;
+        for (int q = 0; res && q < I; ++q) ra.residual[q] = res[(size_t)w.b * I + q] + w.e0;  // error feedback
         for (int q = 0; q < I; ++q) ra.payload[q] = outbox(slot, q);
         for (int q = 0; q <= I; ++q) ra.first[q] = c->first[q];
         ra.n_islands = I;
@@ -814,7 +815,8 @@ gb_status run_set_graph(gb_ctx *c, const std::vector<uint64_t> &key, int kernels
 }
 
 gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel,
-                      gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs, cudaStream_t s) {
+                      gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs, float *const *res,
+                      cudaStream_t s) {
     // the chunk shape of the largest bucket fixes the slot size.  Chunks are
     // kBucketChunkScale x the pipeline chunk: across a gradient set the
     // pipeline fills once, so larger copies only save per-copy cost (on
@@ -838,7 +840,7 @@ gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out
     GB_TRY(grow_host(c, (size_t)c->I * 2 * p.part));
     GB_TRY(begin(c, s));
     if (!c->use_graphs) {
-        GB_TRY(enqueue_buckets(c, p, work, in, out, numel, rs, s));
+        GB_TRY(enqueue_buckets(c, p, work, in, out, numel, rs, res, s));
         return end(c, s);
     }
     std::vector<uint64_t> key = {1, (uint64_t)nb, (uint64_t)dtype, (uint64_t)op, (uint64_t)p.eff, (uint64_t)p.blk,
@@ -850,9 +852,11 @@ gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out
             key.push_back((uint64_t)(uintptr_t)in[(size_t)b * c->W + r]);
             key.push_back((uint64_t)(uintptr_t)out[(size_t)b * c->W + r]);
         }
+        for (int q = 0; res && q < c->I; ++q) key.push_back((uint64_t)(uintptr_t)res[(size_t)b * c->I + q]);
     }
+    key.push_back(res ? 1 : 0);
     return run_set_graph(c, key, 2 * (int)work.size(),
-                         [&](cudaStream_t st) { return enqueue_buckets(c, p, work, in, out, numel, rs, st); }, s);
+                         [&](cudaStream_t st) { return enqueue_buckets(c, p, work, in, out, numel, rs, res, st); }, s);
 }
 
 // Capture one pipelined all_reduce on the context's capture stream and

@@ -373,6 +373,16 @@ gb_status gb_all_reduce_buckets(gb_ctx *ctx, int n_buckets, void *const *bucket_
                                 const size_t *bucket_numel, gb_dtype dtype, gb_op op,
                                 gb_codec codec, int block, gb_stream stream);
 
+/* gb_all_reduce_buckets with error feedback (as gb_all_reduce_ef, per
+ * bucket): residuals holds n_buckets * I device float32 arrays, bucket-major
+ * (bucket b, island i at [b * I + i]), of bucket_numel[b] elements each,
+ * owned by the caller, zero before the first call and kept from step to
+ * step.  float32 / bfloat16 SUM / AVG only.  Same policy, pipeline and graph
+ * as gb_all_reduce_buckets; with one island the residuals are unchanged. */
+gb_status gb_all_reduce_buckets_ef(gb_ctx *ctx, int n_buckets, void *const *bucket_bufs, float *const *residuals,
+                                   const size_t *bucket_numel, gb_dtype dtype, gb_op op, gb_codec codec, int block,
+                                   gb_stream stream);
+
 /* reduce_scatter of every bucket (the gradient sets of a sharded data
  * parallel step): out_bufs[b * W + r] receives slice r (bucket_numel[b] / W
  * elements) of what gb_all_reduce would compute on bucket b's inputs

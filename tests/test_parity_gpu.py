@@ -697,3 +697,31 @@ def test_two_contexts_on_two_threads_and_streams():
         t.join()
     if errors:
         raise errors[0]
+
+
+@pytest.mark.parametrize("codec,block", [("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
+@pytest.mark.parametrize("sizes", [(2, 2), (2, 1, 3), (3,)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bucket_set_error_feedback_over_steps(codec, block, sizes, dtype):
+    """gb_all_reduce_buckets_ef (one pipeline, one graph per set) equals the
+    oracle's all_reduce_ef bucket by bucket over several steps, outputs and
+    every island's residual bit for bit."""
+    I = len(sizes)
+    numels = [3000, 0, 257, 20000]
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(4096)
+        res_h = [[np.zeros(m, np.float32) for _ in range(I)] for m in numels]
+        res_d = [[torch.zeros(m, dtype=torch.float32, device="cuda") for _ in range(I)] for m in numels]
+        for step in range(4):
+            xs = [inputs(sizes, max(m, 1), dtype, cid=160 + 10 * step + b) for b, m in enumerate(numels)]
+            bufs = [[to_dev(x[:m]) for x in row] for row, m in zip(xs, numels)]
+            ctx.all_reduce_buckets_ef(bufs, res_d, "avg", codec, block)
+            torch.cuda.synchronize()
+            for b, m in enumerate(numels):
+                if m == 0:
+                    continue
+                want = orc.all_reduce_ef([x[:m] for x in xs[b]], sizes, res_h[b], "avg", codec, block)
+                for r in range(sum(sizes)):
+                    assert_bits_equal(to_host(bufs[b][r]), want[r], "EF set step %d bucket %d rank %d" % (step, b, r))
+                for i in range(I):
+                    assert_bits_equal(to_host(res_d[b][i]), res_h[b][i], "EF set residual step %d bucket %d" % (step, b))

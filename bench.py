@@ -61,6 +61,8 @@ def parse():
                    help="pipelined bridge chunk (KiB of one island's payload); 0 = one hop per call")
     p.add_argument("--no-graphs", action="store_true")
     p.add_argument("--sharded", action="store_true", help="sharded-bridge policy for the timed step")
+    p.add_argument("--ef", action="store_true",
+                   help="error feedback: the step is gb_all_reduce_ef (gb_all_reduce_buckets_ef for c4 / c5)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--roofline-only", action="store_true",
                    help="only the per-kernel timed regions (kernels inside one-hop steps, and back to "
@@ -204,7 +206,7 @@ def dataclasses_replace_f32(w):
 
 
 def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, batches,
-                  names=("k_reduce_encode", "k_decode_bcast")):
+                  names=("k_reduce_encode", "k_decode_bcast"), ef=False):
     """Timed region 3: each kernel launched back to back, as the fused halves
     of the path (gb_island_reduce_compress, gb_decompress_island_broadcast),
     with the same grid as in a step.  S distinct input sets, outputs and
@@ -215,18 +217,20 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
     launching stream bracket the other S - 1.  So no launch finds its inputs
     in L2, and every timed launch also writes back what its predecessor left
     dirty there: the steady state of a stream of buckets.  Returns per-launch
-    milliseconds of both kernels."""
+    milliseconds of both kernels.  ef: the encode carries error feedback
+    (gb_island_reduce_compress_ef, one float32 residual per island and set)."""
     import torch
     W = len(pristine)
     n = pristine[0].numel()
     b = pristine[0].element_size()
-    set_bytes = W * n * b + I * P
+    set_bytes = W * n * b + I * P + (I * n * 4 if ef else 0)
     S = max(5, min(-(-(4 * L2_BYTES) // set_bytes), 16 if set_bytes * 16 < 4 * L2_BYTES else 1 << 30,
                    (8 << 30) // set_bytes))
     dev = pristine[0].device
     ins = [[p.clone() for p in pristine] for _ in range(S)]
     outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
     pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
+    res = [[torch.zeros(n, dtype=torch.float32, device=dev) for _ in range(I)] for _ in range(S)] if ef else None
     # every leader's row holds the same I payloads: the call decodes them
     # once and writes all ranks, as the decode in a step does
     rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
@@ -237,7 +241,10 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
             clean.amax()
             torch.cuda._sleep(800_000)
             for q in range(S):
-                ctx.island_reduce_compress(ins[q], codec, block, pays[q], stream=stream)
+                if ef:
+                    ctx.island_reduce_compress_ef(ins[q], res[q], codec, block, pays[q], stream=stream)
+                else:
+                    ctx.island_reduce_compress(ins[q], codec, block, pays[q], stream=stream)
                 if e and q == 0:
                     e[0].record(stream)
             if e:
@@ -314,6 +321,8 @@ def run_gb(args, world, rank, local, pg):
 
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ef = args.ef and not exact and I > 1
+    res = [torch.zeros(n, dtype=torch.float32, device=dev) for _ in range(I)] if ef else None
 
     def step(i, timed):
         for r in range(W):
@@ -322,7 +331,10 @@ def run_gb(args, world, rank, local, pg):
         clean.amax()    # ... then read 256 MiB, so the lines left in L2 are clean
         if timed:
             ev0[i].record(stream)
-        ctx.all_reduce(bufs, w.op, codec, w.block, stream=stream)
+        if ef:  # the residuals carry from step to step, as in training
+            ctx.all_reduce_ef(bufs, res, w.op, codec, w.block, stream=stream)
+        else:
+            ctx.all_reduce(bufs, w.op, codec, w.block, stream=stream)
         if timed:
             ev1[i].record(stream)
 
@@ -383,13 +395,15 @@ def run_gb(args, world, rank, local, pg):
         names = ("k_reduce_encode", "k_decode_bcast")
     k1_ms, bridge_ms, k2_ms = (float(np.mean(phases[:, j])) for j in range(3))
     k1_bytes, k2_bytes = alg_bytes(W, I, n, b, P)
+    if ef:  # the encode also reads and writes every island's float32 residual
+        k1_bytes += 2 * I * n * 4
     peak, peak_kind = measured_peaks()
 
     # ---- timed region 3: each kernel back to back (see kernel_stream)
     ks = None
     if not exact and I > 1:
         ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, Wm, max(3, min(Kr, 50)),
-                           names)
+                           names, ef=ef)
         S, set_bytes = ks["sets"], ks["set_bytes"]
     if ks:
         r1, r2 = ks[names[0]], ks[names[1]]
@@ -433,7 +447,7 @@ def run_gb(args, world, rank, local, pg):
                                    w.key, W, list(w.island_sizes), n * b / 2 ** 20, w.dtype, n, w.dist,
                                    w.op, codec, w.block),
                    "ranks": W, "islands": list(w.island_sizes), "n": n, "codec": codec, "block": w.block,
-                   "op": w.op,
+                   "op": w.op, "error_feedback": bool(ef),
                    "policy": (("sharded-bridge, %d links%s" % (
                        min(w.island_sizes), ", CUDA graph replay" if not args.no_graphs else ""))
                               if args.sharded and min(w.island_sizes) > 1 else
@@ -533,6 +547,8 @@ def run_buckets_bench(args, world, rank, local, pg):
     ctx.set_pipeline(chunk_bytes, not args.no_graphs)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ef = args.ef
+    res = [[torch.zeros(nb, dtype=torch.float32, device=dev) for _ in range(I)] for nb in bn] if ef else None
 
     def step(i, timed, per_bucket=False):
         for row_p, row_b in zip(pristine, bufs):
@@ -543,8 +559,13 @@ def run_buckets_bench(args, world, rank, local, pg):
         if timed:
             ev0[i].record(stream)
         if per_bucket:
-            for row in bufs:
-                ctx.all_reduce(row, w.op, codec, w.block, stream=stream)
+            for bi, row in enumerate(bufs):
+                if ef:
+                    ctx.all_reduce_ef(row, res[bi], w.op, codec, w.block, stream=stream)
+                else:
+                    ctx.all_reduce(row, w.op, codec, w.block, stream=stream)
+        elif ef:  # the residuals carry from step to step, as in training
+            ctx.all_reduce_buckets_ef(bufs, res, w.op, codec, w.block, stream=stream)
         else:
             ctx.all_reduce_buckets(bufs, w.op, codec, w.block, stream=stream)
         if timed:
@@ -627,6 +648,8 @@ def run_buckets_bench(args, world, rank, local, pg):
     for nb in bn:
         P = payload_bytes(codec, w.block, nb)
         x1, x2 = alg_bytes(W, I, nb, b, P)
+        if ef:  # the encode also reads and writes every island's float32 residual
+            x1 += 2 * I * nb * 4
         bytes1 += x1
         bytes2 += x2
     t1 = float(np.sum(ph[:, 0])) / Kr
@@ -643,6 +666,7 @@ def run_buckets_bench(args, world, rank, local, pg):
                                    w.key, W, list(w.island_sizes), len(numels), w.dtype, sum(numels), len(bn),
                                    w.dist, w.op, codec, w.block),
                    "buckets": len(bn), "values_per_rank": sum(bn),
+                   "error_feedback": bool(ef),
                    "policy": "one pipeline over all buckets (payload chunks of at most 3 x %d KiB, each bucket "
                              "cut evenly), one CUDA graph per step" % (chunk_bytes >> 10),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
@@ -934,7 +958,8 @@ def main():
             pg.destroy_process_group()
         return
     line, w, xs, codec = run_gb(args, world, rank, local, pg)
-    line["roofline"]["traffic"] = traffic_from_profiles(line["roofline"]["kernel"])
+    # the recorded capture is of the kernel without error feedback
+    line["roofline"]["traffic"] = None if args.ef else traffic_from_profiles(line["roofline"]["kernel"])
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, xs, codec)

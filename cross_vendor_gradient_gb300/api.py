@@ -228,6 +228,15 @@ class Context:
                                                 tensors[0].numel(), dt, _codec(codec), block,
                                                 [p.data_ptr() for p in payloads], _stream(stream)))
 
+    def island_reduce_compress_ef(self, tensors, residuals, codec, block, payloads, stream=None):
+        """island_reduce_compress with error feedback: residuals are I
+        float32 tensors of n elements (updated in place)."""
+        dt = _dtype(tensors)
+        self._check(B.gb_island_reduce_compress_ef(self.handle, [t.data_ptr() for t in tensors],
+                                                   [r.data_ptr() for r in residuals], tensors[0].numel(), dt,
+                                                   _codec(codec), block, [p.data_ptr() for p in payloads],
+                                                   _stream(stream)))
+
     def decompress_island_broadcast(self, payloads, op, codec, block, tensors, stream=None):
         """Fused decode of every island's payload + accumulate + broadcast
         into all rank tensors.  payloads: I tensors (every leader holds the

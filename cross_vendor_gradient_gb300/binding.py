@@ -64,6 +64,7 @@ SIGNATURES = {
     "gb_island_broadcast": (_i, [_vp, _i, _vp, _sz, _i, _P(_vp), _i, _vp]),
     "gb_set_sharded_bridge": (_i, [_vp, _i]),
     "gb_island_reduce_compress": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
+    "gb_island_reduce_compress_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
     "gb_decompress_island_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
     "gb_all_reduce": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_all_reduce_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
@@ -205,6 +206,11 @@ def gb_set_sharded_bridge(ctx, on):
 def gb_island_reduce_compress(ctx, rank_bufs, n, dtype, codec, block, payloads, stream=0):
     return lib().gb_island_reduce_compress(ctx, _ptrs(rank_bufs), n, dtype, codec, block, _ptrs(payloads),
                                            stream)
+
+
+def gb_island_reduce_compress_ef(ctx, rank_bufs, residuals, n, dtype, codec, block, payloads, stream=0):
+    return lib().gb_island_reduce_compress_ef(ctx, _ptrs(rank_bufs), _ptrs(residuals), n, dtype, codec, block,
+                                              _ptrs(payloads), stream)
 
 
 def gb_decompress_island_broadcast(ctx, payloads, n, dtype, op, codec, block, rank_bufs, stream=0):

@@ -248,14 +248,17 @@ gb_status gb_island_broadcast(gb_ctx *c, int island, const float *total, size_t 
                         "island broadcast");
 }
 
-gb_status gb_island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, size_t n, gb_dtype dtype,
-                                    gb_codec codec, int block, void *const *payloads, gb_stream stream) {
+// gb_island_reduce_compress with (res != NULL) or without error feedback.
+static gb_status island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, float *const *res, size_t n,
+                                        gb_dtype dtype, gb_codec codec, int block, void *const *payloads,
+                                        gb_stream stream) {
     GB_TRY(check_ctx(c));
     GB_TRY(check_codec_dtype(c, dtype));
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
     GB_TRY(check_dev_bufs(c, rank_bufs, c->W, "rank_bufs"));
     GB_TRY(check_dev_bufs(c, (const void *const *)payloads, c->I, "payloads"));
+    if (res) GB_TRY(check_dev_bufs(c, (const void *const *)res, c->I, "residuals"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
     const int blk = is_fp8(codec) ? block : 256;
@@ -263,6 +266,7 @@ gb_status gb_island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, siz
     memset(&ra, 0, sizeof ra);
     for (int r = 0; r < c->W; ++r) ra.src[r] = rank_bufs[r];
     for (int i = 0; i < c->I; ++i) ra.payload[i] = payloads[i];
+    for (int i = 0; res && i < c->I; ++i) ra.residual[i] = res[i];
     for (int i = 0; i <= c->I; ++i) ra.first[i] = c->first[i];
     ra.n_islands = c->I;
     ra.n = n;
@@ -270,6 +274,18 @@ gb_status gb_island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, siz
     ra.scales_off = scales_offset(codec, n);
     return check_launch(c, gb::launch_reduce_encode(ra, dtype, codec, blk, (cudaStream_t)stream),
                         "island reduce + compress");
+}
+
+gb_status gb_island_reduce_compress(gb_ctx *c, const void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                    gb_codec codec, int block, void *const *payloads, gb_stream stream) {
+    return island_reduce_compress(c, rank_bufs, nullptr, n, dtype, codec, block, payloads, stream);
+}
+
+gb_status gb_island_reduce_compress_ef(gb_ctx *c, const void *const *rank_bufs, float *const *residuals, size_t n,
+                                       gb_dtype dtype, gb_codec codec, int block, void *const *payloads,
+                                       gb_stream stream) {
+    if (c && !residuals) return set_msg(c, GB_ERR_INVALID_ARG, "residuals is NULL");
+    return island_reduce_compress(c, rank_bufs, residuals, n, dtype, codec, block, payloads, stream);
 }
 
 gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype,

@@ -278,6 +278,13 @@ gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_
  * Errors as for gb_all_reduce; n == 0 is a no-op.  Neither call allocates. */
 gb_status gb_island_reduce_compress(gb_ctx *ctx, const void *const *rank_bufs, size_t n, gb_dtype dtype,
                                     gb_codec codec, int block, void *const *payloads, gb_stream stream);
+/* gb_island_reduce_compress with error feedback: island i encodes
+ * s_i + residuals[i] and sets residuals[i] = (s_i + residuals[i]) -
+ * dec(payload_i), as gb_all_reduce_ef does (float32, n elements per island,
+ * device, 32-byte aligned, owned by the caller). */
+gb_status gb_island_reduce_compress_ef(gb_ctx *ctx, const void *const *rank_bufs, float *const *residuals, size_t n,
+                                       gb_dtype dtype, gb_codec codec, int block, void *const *payloads,
+                                       gb_stream stream);
 gb_status gb_decompress_island_broadcast(gb_ctx *ctx, const void *const *payloads, size_t n, gb_dtype dtype,
                                          gb_op op, gb_codec codec, int block, void *const *rank_bufs,
                                          gb_stream stream);

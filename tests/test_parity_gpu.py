@@ -725,3 +725,35 @@ def test_bucket_set_error_feedback_over_steps(codec, block, sizes, dtype):
                     assert_bits_equal(to_host(bufs[b][r]), want[r], "EF set step %d bucket %d rank %d" % (step, b, r))
                 for i in range(I):
                     assert_bits_equal(to_host(res_d[b][i]), res_h[b][i], "EF set residual step %d bucket %d" % (step, b))
+
+
+@pytest.mark.parametrize("codec,block", [("bf16", 256), ("e4m3", 256), ("e5m2", 128), ("none", 256)])
+@pytest.mark.parametrize("sizes", [(2, 2), (1, 3), (2, 1, 3)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_encode_half_with_error_feedback(codec, block, sizes, dtype):
+    """gb_island_reduce_compress_ef writes the oracle's error-feedback
+    encoding of every island sum and updates the residuals bit for bit,
+    over several steps."""
+    W, I = sum(sizes), len(sizes)
+    first = np.concatenate([[0], np.cumsum(sizes)]).astype(int)
+    n = 256 * 7 + 33
+    with Context(sizes) as ctx:
+        res_h = [np.zeros(n, np.float32) for _ in range(I)]
+        res_d = [torch.zeros(n, dtype=torch.float32, device="cuda") for _ in range(I)]
+        P = payload_bytes(codec, block, n)
+        cd = orc.code_dtype(codec)
+        cb = np.dtype(cd).itemsize
+        for step in range(3):
+            xs = inputs(sizes, n, dtype, cid=180 + step)
+            pay = [torch.empty(P, dtype=torch.uint8, device="cuda") for _ in range(I)]
+            ctx.island_reduce_compress_ef([to_dev(x) for x in xs], res_d, codec, block, pay)
+            torch.cuda.synchronize()
+            for i in range(I):
+                s = orc.island_sum(xs[first[i]:first[i + 1]])
+                codes, scales = orc.encode_ef(s, res_h[i], codec, block)
+                ph = to_host(pay[i])
+                assert_bits_equal(ph[:n * cb].view(cd), codes, "EF codes step %d island %d" % (step, i))
+                if scales.size:
+                    off = payload_scales_offset(codec, block, n)
+                    assert_bits_equal(ph[off:off + 4 * scales.size].view(np.float32), scales, "EF scales")
+                assert_bits_equal(to_host(res_d[i]), res_h[i], "EF residual step %d island %d" % (step, i))

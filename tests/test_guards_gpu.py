@@ -116,6 +116,10 @@ def test_newer_entry_points_stay_in_bounds(codec, block, sizes):
                 fill(g, 20 + r)
             pays = [Guarded(payload_bytes(codec, block, n), torch.uint8) for _ in range(I)]
             ctx.island_reduce_compress([g.t for g in ranks], codec, block, [p.t for p in pays])
+            efres = [Guarded(n, torch.float32) for _ in range(I)]
+            for g in efres:
+                g.t.zero_()
+            ctx.island_reduce_compress_ef([g.t for g in ranks], [g.t for g in efres], codec, block, [p.t for p in pays])
             ctx.decompress_island_broadcast([p.t for p in pays], "avg", codec, block, [g.t for g in ranks])
             ctx.set_sharded_bridge(True)
             for _ in range(2):
@@ -133,5 +137,5 @@ def test_newer_entry_points_stay_in_bounds(codec, block, sizes):
             for _ in range(2):
                 ctx.all_reduce_buckets([[g.t for g in row] for row in buckets], "sum", codec, block)
             torch.cuda.synchronize()
-            for g in ranks + pays + res + [g for row in buckets for g in row]:
+            for g in ranks + pays + res + efres + [g for row in buckets for g in row]:
                 assert g.intact(), (codec, sizes, n)

@@ -25,7 +25,8 @@ struct ReduceEncodeArgs {
 };
 
 // Fused decode + accumulate + broadcast (grid y = output unit).
-// Output group g (an island for all_reduce) reads the n_src payloads
+// Output group g (one group of all W ranks when the payloads are decoded
+// once, see decode_once; an island's ranks for per-leader rows) reads the n_src payloads
 // payload[g][0..n_src) (island order), adds their decoded values in float32,
 // divides by W for AVG (an exact multiply by 1/W when W is a power of two),
 // rounds to the rank dtype and writes the result.
@@ -33,8 +34,8 @@ struct ReduceEncodeArgs {
 //     dst[first[g] .. first[g+1]) receives the same elements;
 //   reduce_scatter (rs == 1): unit = rank r; the unit's rs_len[r] elements
 //     start at payload element rs_src[r] and go to dst[r] (the host offsets
-//     dst[r] to the slice position they land on); group g = the island of
-//     r.  One chunk of the pipeline covers the parts of the slices that fall
+//     dst[r] to the slice position they land on); group g =
+//     group_of_rank[r].  One chunk of the pipeline covers the parts of the slices that fall
 //     inside it.  vec == 0 forces the element-wise path (used when the slice
 //     length is not a multiple of 8, which would misalign vector accesses).
 struct DecodeBcastArgs {

@@ -7,9 +7,11 @@
 // once by the world size (API table, all_reduce row); the total, rounded to
 // the rank dtype, goes to every rank of the island.
 //
-// How: one warp per 256-element tile per output unit (grid y: an island's
-// group of ranks, or one rank for reduce_scatter), 8 contiguous elements per
-// lane; the payloads of a tile are all loaded before the first add
+// How: the host passes the payloads once, as one output group holding all
+// W ranks (every leader would compute the same bits), so each payload is
+// read and decoded once.  One warp per 256-element tile per output unit
+// (grid y: a group of ranks, or one rank for reduce_scatter), 8 contiguous
+// elements per lane; the payloads of a tile are all loaded before the first add
 // (compile-time count for 1 or 2 islands), and for those counts the loads of
 // the warp's next tile are issued before the current one is decoded and
 // stored; the result leaves as one 32-byte (float32) or 16-byte (bf16)

@@ -348,6 +348,8 @@ gb_status gb_all_reduce_ef(gb_ctx *c, void *const *rank_bufs, float *const *resi
                            gb_op op, gb_codec codec, int block, gb_stream stream) {
     GB_TRY(check_ctx(c));
     GB_TRY(check_collective(c, n, dtype, op, codec, block));
+    if (is_exact(dtype, op))
+        return set_msg(c, GB_ERR_UNSUPPORTED_OP, "error feedback applies to float32 / bfloat16 SUM / AVG");
     GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
     GB_TRY(check_dev_bufs(c, (const void *const *)residuals, c->I, "residuals"));
     if (n == 0) return GB_OK;

@@ -203,8 +203,6 @@ gb_status capture_rbb(gb_ctx *c, const Plan &p, const void *const *in, float *co
                       GraphEntry *ge);
 GraphEntry *find_graph(gb_ctx *c, const GraphKey &k);
 GraphEntry *new_graph_slot(gb_ctx *c);
-gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype, gb_op op,
-                    cudaStream_t s, int rs);
 gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel_in,
                              size_t eb, size_t slot_bytes, cudaStream_t s);
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,

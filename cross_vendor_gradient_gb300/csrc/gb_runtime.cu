@@ -301,10 +301,13 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
     p.dtype = dtype;
     p.op = op;
     p.rs = rs;
-    p.eff = c->I == 1 ? GB_CODEC_NONE : (int)codec;
+    p.eff = (c->I == 1 || is_exact(dtype, op)) ? GB_CODEC_NONE : (int)codec;
     p.blk = is_fp8(p.eff) ? block : 256;
     p.eb = elem_bytes(dtype);
-    p.cb = p.eff == GB_CODEC_NONE ? 4 : p.eff == GB_CODEC_BF16 ? 2 : 1;
+    // payload bytes per element: the codec's, or the exact path's (the dtype,
+    // or float32 sums of 16-bit floats)
+    p.cb = is_exact(dtype, op) ? gb::exact_payload_elem_bytes(dtype, op)
+                               : p.eff == GB_CODEC_NONE ? 4 : p.eff == GB_CODEC_BF16 ? 2 : 1;
     p.chunk = n;
     int k = c->I > 1 ? c->size[0] : 1;  // sharded-bridge: k = the smallest island's size
     for (int i = 1; i < c->I; ++i)
@@ -394,7 +397,10 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         ra.n = m;
         ra.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
         ra.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
-        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        if (is_exact(p.dtype, p.op))
+            GB_TRY(check_launch(c, gb::launch_exact_reduce(ra, p.dtype, p.op, s), "island fold"));
+        else
+            GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
         if (multi) GB_TRY(record(c, c->ev_k1[ch], s));
     }
     GB_TRY(mark(c, markmode, 1, s));
@@ -487,17 +493,25 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         da.inv_world = 1.0f / (float)p.W;
         da.n = m;
         da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
+        const bool exact = is_exact(p.dtype, p.op);
+        // vector accesses: 8 elements per lane (codec kernels) or 16 bytes per
+        // thread (exact kernels) must not straddle a slice boundary
+        const uint64_t vec_elems = exact ? 16 / p.eb : 8;
         if (p.rs) {
             da.rs = 1;
-            da.vec = ((p.n / (uint64_t)p.W) % 8) == 0;
+            da.vec = ((p.n / (uint64_t)p.W) % vec_elems) == 0;
             da.tiles = (uint32_t)((rs_max + gb::kTile - 1) / gb::kTile);
         } else {
             da.rs = 0;
             da.vec = 1;
             da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
         }
-        if (da.tiles > 0)
-            GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        if (da.tiles > 0) {
+            if (exact)
+                GB_TRY(check_launch(c, gb::launch_exact_combine(da, p.dtype, p.op, s), "fold + broadcast"));
+            else
+                GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        }
         GB_TRY(mark(c, markmode, 5 + 2 * ch, s));
     }
     if (multi) {  // the copy streams' last work precedes the end of the call
@@ -921,88 +935,6 @@ GraphEntry *new_graph_slot(gb_ctx *c) {
     return &g;
 }
 
-// The exact path: island fold -> payload (the dtype, or float32 sums of
-// 16-bit floats), one bridge hop on the caller's stream, fold of the
-// payloads in island order -> ranks.  Same staging layout as a one-chunk
-// Plan.
-gb_status run_exact(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype, gb_op op,
-                    cudaStream_t s, int rs) {
-    const int I = c->I, W = c->W;
-    const size_t P = n * gb::exact_payload_elem_bytes(dtype, op);
-    const size_t part = round_up(P, 256);
-    const int recv = I == 1 ? 0 : I == 2 ? 2 : I * I;
-    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(I + recv) * part));
-    if (I > 1) GB_TRY(grow_host(c, (size_t)I * part));
-    GB_TRY(begin(c, s));
-    const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
-    auto outbox = [&](int i) { return c->d_stage + (size_t)i * part; };
-    auto inbox = [&](int g, int j) {
-        unsigned char *base = c->d_stage + (size_t)I * part;
-        return I == 2 ? base + (size_t)j * part : base + ((size_t)g * I + j) * part;
-    };
-    GB_TRY(mark(c, mm, 0, s));
-    gb::ReduceEncodeArgs ra;
-    memset(&ra, 0, sizeof ra);
-    for (int r = 0; r < W; ++r) ra.src[r] = in[r];
-    for (int i = 0; i < I; ++i) ra.payload[i] = outbox(i);
-    for (int i = 0; i <= I; ++i) ra.first[i] = c->first[i];
-    ra.n_islands = I;
-    ra.n = n;
-    GB_TRY(check_launch(c, gb::launch_exact_reduce(ra, dtype, op, s), "island fold"));
-    GB_TRY(mark(c, mm, 1, s));
-    if (I > 1) {
-        if (c->inject == GB_INJECT_BRIDGE) {
-            c->inject = 0;
-            return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
-        }
-        GB_TRY(mark(c, mm, 2, s));
-        GB_TRY(copy_async(c, c->h_stage, outbox(0), (size_t)(I - 1) * part + P, cudaMemcpyDeviceToHost, s));
-        if (I == 2) {
-            GB_TRY(copy_async(c, inbox(1, 0), c->h_stage, part + P, cudaMemcpyHostToDevice, s));
-        } else {
-            for (int g = 0; g < I; ++g) {
-                if (g > 0)
-                    GB_TRY(copy_async(c, inbox(g, 0), c->h_stage, (size_t)(g - 1) * part + P, cudaMemcpyHostToDevice, s));
-                if (g < I - 1)
-                    GB_TRY(copy_async(c, inbox(g, g + 1), c->h_stage + (size_t)(g + 1) * part,
-                                      (size_t)(I - g - 2) * part + P, cudaMemcpyHostToDevice, s));
-            }
-        }
-        GB_TRY(mark(c, mm, 3, s));
-    }
-    GB_TRY(mark(c, mm, 4, s));
-    gb::DecodeBcastArgs da;
-    memset(&da, 0, sizeof da);
-    for (int r = 0; r < W; ++r) {
-        da.dst[r] = out[r];
-        da.group_of_rank[r] = c->island_of[r];
-    }
-    const void *received[GB_MAX_ISLANDS];
-    for (int j = 0; j < I; ++j)
-        received[j] = I == 1 ? (const void *)outbox(0) : (const void *)inbox((j + 1) % I, j);
-    gb::decode_once(da, W, I, received);
-    da.world = (float)W;
-    da.world_pow2 = (W & (W - 1)) == 0;
-    da.inv_world = 1.0f / (float)W;
-    da.n = n;
-    const uint64_t V = 16 / elem_bytes(dtype);
-    if (rs) {
-        const uint64_t m = n / (uint64_t)W;
-        da.rs = 1;
-        for (int r = 0; r < W; ++r) {
-            da.rs_src[r] = (uint64_t)r * m;
-            da.rs_len[r] = m;
-        }
-        da.vec = (m % V) == 0;
-    } else {
-        da.vec = 1;
-    }
-    GB_TRY(check_launch(c, gb::launch_exact_combine(da, dtype, op, s), "fold + broadcast"));
-    GB_TRY(mark(c, mm, 5, s));
-    commit_marks(c, 1, I > 1);
-    return end(c, s);
-}
-
 // all_gather of every bucket as one pipeline (bucket b: W inputs of
 // numel_in[b] elements, W outputs of W * numel_in[b]).  Bucket b's rank
 // blocks cross the bridge through host slot b % 2: groups of consecutive
@@ -1084,7 +1016,6 @@ gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *con
 // buffers and shape (the first runs directly) and replayed afterwards.
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
                   gb_op op, gb_codec codec, int block, cudaStream_t s, int rs, float *const *res) {
-    if (is_exact(dtype, op)) return run_exact(c, in, out, n, dtype, op, s, rs);
     const Plan p = make_plan(c, n, dtype, op, codec, block, rs, true);
     GB_TRY(ensure_links(c, p.links));
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));

@@ -306,7 +306,9 @@ gb_status gb_all_reduce(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype 
  * Each leader encodes s_i + r_i and sets r_i = (s_i + r_i) - dec(payload_i)
  * (float32); the rest is gb_all_reduce.  With one island there is no bridge
  * and the residuals are left unchanged.  Saving and restoring the residual
- * arrays checkpoints and resumes the feedback state. */
+ * arrays checkpoints and resumes the feedback state.  float32 / bfloat16
+ * SUM / AVG only (the exact path has nothing to feed back):
+ * GB_ERR_UNSUPPORTED_OP otherwise. */
 gb_status gb_all_reduce_ef(gb_ctx *ctx, void *const *rank_bufs, float *const *residuals, size_t n,
                            gb_dtype dtype, gb_op op, gb_codec codec, int block, gb_stream stream);
 

@@ -144,6 +144,7 @@ def test_argument_errors_need_no_device():
         assert B.gb_decompress_island_broadcast(ctx, pl4[:3] + [0], 10, 0, 0, 2, 256, fake) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce_compress(ctx, fake, 0, 0, 2, 256, pl) == B.GB_OK
         assert B.gb_decompress_island_broadcast(ctx, pl4, 0, 1, 1, 3, 128, fake) == B.GB_OK
+        assert B.gb_all_reduce_ef(ctx, fake, fake[:2], 16, 0, B.GB_MAX, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
         # bucket sets
         assert B.gb_all_reduce_buckets_ef(ctx, fake, fake[:2], [16], 0, B.GB_MAX, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
         assert B.gb_all_reduce_buckets_ef(ctx, fake, [0x40000, 0], [16], 0, 0, 2, 256) == B.GB_ERR_INVALID_ARG

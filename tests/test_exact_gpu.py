@@ -48,9 +48,11 @@ def guarded(n, tdt):
 
 @pytest.mark.parametrize("dt", DTYPES, ids=str)
 @pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (2, 1, 3), (3,)])
-def test_exact_collectives_match_oracle(dt, sizes):
+@pytest.mark.parametrize("chunk", [2 << 20, 1024])  # 1 KiB: many pipeline chunks, slices straddling them
+def test_exact_collectives_match_oracle(dt, sizes, chunk):
     W = sum(sizes)
     with Context(sizes) as ctx:
+        ctx.set_pipeline(chunk)
         for n in (1, 15, 16, 17, 1000, 4096 * W + 3 * W, 70_001):
             n -= n % W if n >= W else 0
             n = max(n, W)

@@ -563,7 +563,7 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
     // buffers' worth of staging in and out, so the pipeline's fill and drain
     // weigh more (1 MiB beat 0.5, 0.75, 1.5 and 2 MiB on GB300)
     const Plan p = make_plan(c, n, dtype, op, codec, block, 0, false, c->chunk_bytes / kHostChunkDiv);
-    if (!is_exact(dtype, op) && p.C > 1 && c->tcap == 0) {
+    if (p.C > 1 && c->tcap == 0) {
         // pipelined: staging in, bridge and copy-back overlap chunk by chunk
         GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
         GB_TRY(grow_host(c, p.host_bytes));
@@ -678,7 +678,7 @@ static gb_status all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucke
     size_t total = 0;
     for (int b = 0; b < n_buckets; ++b) total += bucket_numel[b];
     if (total == 0) return GB_OK;
-    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0 && !c->sharded) {
+    if (c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0 && !c->sharded) {
         GB_TRY(bind(c));
         return run_buckets(c, n_buckets, (const void *const *)bucket_bufs, bucket_bufs, bucket_numel, dtype, op,
                            codec, block, 0, res, (cudaStream_t)stream);
@@ -725,7 +725,7 @@ gb_status gb_reduce_scatter_buckets(gb_ctx *c, int n_buckets, const void *const 
         total += bucket_numel[b];
     }
     if (total == 0) return GB_OK;
-    if (!is_exact(dtype, op) && c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
+    if (c->I > 1 && c->chunk_bytes > 0 && c->tcap == 0) {
         GB_TRY(bind(c));
         return run_buckets(c, n_buckets, in_bufs, out_bufs, bucket_numel, dtype, op, codec, block, 1, nullptr,
                            (cudaStream_t)stream);

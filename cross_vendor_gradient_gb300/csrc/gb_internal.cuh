@@ -184,6 +184,9 @@ size_t part_bytes(const Plan &p, uint64_t m);
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
                bool sharded_ok = false, size_t chunk_bytes = 0);
 gb_status check_launch(gb_ctx *c, cudaError_t e, const char *what);
+gb_status launch_encode(gb_ctx *c, const Plan &p, const gb::ReduceEncodeArgs &ra, cudaStream_t s);
+gb_status launch_decode(gb_ctx *c, const Plan &p, const gb::DecodeBcastArgs &da, cudaStream_t s);
+uint64_t vec_elems(const Plan &p);
 gb_status copy_async(gb_ctx *c, void *dst, const void *src, size_t bytes, cudaMemcpyKind kind,
                      cudaStream_t s);
 gb_status wait_on(gb_ctx *c, cudaStream_t s, cudaEvent_t ev);

@@ -343,6 +343,23 @@ gb_status check_launch(gb_ctx *c, cudaError_t e, const char *what) {
     return GB_OK;
 }
 
+// The two kernels of a plan: the codec path's, or the exact path's (MAX /
+// MIN, exact dtypes).
+gb_status launch_encode(gb_ctx *c, const Plan &p, const gb::ReduceEncodeArgs &ra, cudaStream_t s) {
+    if (is_exact(p.dtype, p.op)) return check_launch(c, gb::launch_exact_reduce(ra, p.dtype, p.op, s), "island fold");
+    return check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode");
+}
+
+gb_status launch_decode(gb_ctx *c, const Plan &p, const gb::DecodeBcastArgs &da, cudaStream_t s) {
+    if (is_exact(p.dtype, p.op))
+        return check_launch(c, gb::launch_exact_combine(da, p.dtype, p.op, s), "fold + broadcast");
+    return check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast");
+}
+
+// Vector accesses move 8 elements per lane (codec kernels) or 16 bytes per
+// thread (exact kernels); a reduce_scatter slice length must be a multiple.
+uint64_t vec_elems(const Plan &p) { return is_exact(p.dtype, p.op) ? 16 / p.eb : 8; }
+
 gb_status copy_async(gb_ctx *c, void *dst, const void *src, size_t bytes, cudaMemcpyKind kind,
                      cudaStream_t s) {
     if (bytes == 0) return GB_OK;
@@ -397,10 +414,7 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         ra.n = m;
         ra.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
         ra.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
-        if (is_exact(p.dtype, p.op))
-            GB_TRY(check_launch(c, gb::launch_exact_reduce(ra, p.dtype, p.op, s), "island fold"));
-        else
-            GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        GB_TRY(launch_encode(c, p, ra, s));
         if (multi) GB_TRY(record(c, c->ev_k1[ch], s));
     }
     GB_TRY(mark(c, markmode, 1, s));
@@ -493,25 +507,16 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         da.inv_world = 1.0f / (float)p.W;
         da.n = m;
         da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
-        const bool exact = is_exact(p.dtype, p.op);
-        // vector accesses: 8 elements per lane (codec kernels) or 16 bytes per
-        // thread (exact kernels) must not straddle a slice boundary
-        const uint64_t vec_elems = exact ? 16 / p.eb : 8;
         if (p.rs) {
             da.rs = 1;
-            da.vec = ((p.n / (uint64_t)p.W) % vec_elems) == 0;
+            da.vec = ((p.n / (uint64_t)p.W) % vec_elems(p)) == 0;
             da.tiles = (uint32_t)((rs_max + gb::kTile - 1) / gb::kTile);
         } else {
             da.rs = 0;
             da.vec = 1;
             da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
         }
-        if (da.tiles > 0) {
-            if (exact)
-                GB_TRY(check_launch(c, gb::launch_exact_combine(da, p.dtype, p.op, s), "fold + broadcast"));
-            else
-                GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
-        }
+        if (da.tiles > 0) GB_TRY(launch_decode(c, p, da, s));
         GB_TRY(mark(c, markmode, 5 + 2 * ch, s));
     }
     if (multi) {  // the copy streams' last work precedes the end of the call
@@ -591,7 +596,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
         ra.n = m;
         ra.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
         ra.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
-        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        GB_TRY(launch_encode(c, p, ra, s));
         GB_TRY(record(c, c->ev_k1[ch], s));
         if (I > 1) {
             GB_TRY(wait_on(c, D, c->ev_k1[ch]));
@@ -640,7 +645,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
         da.scales_off = is_fp8(p.eff) ? round_up(m * p.cb, 16) : 0;
         da.vec = 1;
         da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
-        GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+        GB_TRY(launch_decode(c, p, da, s));
         GB_TRY(record(c, c->ev_k2[ch], s));
         GB_TRY(wait_on(c, D, c->ev_k2[ch]));
         for (int r = 0; r < W; ++r) {
@@ -696,7 +701,7 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         ra.n = w.m;
         ra.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
         ra.scales_off = is_fp8(p.eff) ? round_up(w.m * p.cb, 16) : 0;
-        GB_TRY(check_launch(c, gb::launch_reduce_encode(ra, p.dtype, p.eff, p.blk, s), "island reduce + encode"));
+        GB_TRY(launch_encode(c, p, ra, s));
         GB_TRY(record(c, c->ev_k1[ev], s));
         GB_TRY(wait_on(c, D, c->ev_k1[ev]));
         GB_TRY(copy_async(c, hslot(slot, 0), outbox(slot, 0), (size_t)(I - 1) * p.part + part_bytes(p, w.m),
@@ -754,14 +759,14 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         da.scales_off = is_fp8(p.eff) ? round_up(w.m * p.cb, 16) : 0;
         if (rs) {
             da.rs = 1;
-            da.vec = ((numel[w.b] / (uint64_t)W) % 8) == 0;
+            da.vec = ((numel[w.b] / (uint64_t)W) % vec_elems(p)) == 0;
             da.tiles = (uint32_t)((rs_max + gb::kTile - 1) / gb::kTile);
         } else {
             da.vec = 1;
             da.tiles = (uint32_t)((w.m + gb::kTile - 1) / gb::kTile);
         }
         if (da.tiles > 0)
-            GB_TRY(check_launch(c, gb::launch_decode_bcast(da, p.dtype, p.eff, p.blk, s), "decode + broadcast"));
+            GB_TRY(launch_decode(c, p, da, s));
         return GB_OK;
     };
     GB_TRY(front(0));

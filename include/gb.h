@@ -337,13 +337,12 @@ gb_status gb_broadcast(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype d
  * buffers are staged onto the GPU in context-owned device buffers, reduced
  * there and copied back (gpubridge README, torch.distributed backend, CPU
  * tensors: staged onto the rank's GPU, carried by the same topology and
- * copied back).  Under the pipelined policy (float32 / bfloat16 SUM / AVG,
- * no phase marks kept) the staging, the bridge hop and the copy-back run
- * chunk by chunk (chunks of half of chunk_bytes of payload: every chunk also
- * carries the rank buffers in and out) on the context's copy streams so that
- * both directions of the host link stay busy, replayed as a CUDA graph from
- * the second call
- * with the same buffers; otherwise staging, all_reduce and copy-back run in
+ * copied back).  Under the pipelined policy (no phase marks kept) the
+ * staging, the bridge hop and the copy-back run chunk by chunk (chunks of
+ * half of chunk_bytes of payload: every chunk also carries the rank buffers
+ * in and out) on the context's copy streams so that both directions of the
+ * host link stay busy, replayed as a CUDA graph from the second call with
+ * the same buffers; otherwise staging, all_reduce and copy-back run in
  * sequence.  Host buffers need no alignment; they must not be touched until
  * `stream` has completed the call. */
 gb_status gb_all_reduce_host(gb_ctx *ctx, void *const *host_bufs, size_t n, gb_dtype dtype,
@@ -370,11 +369,11 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, 
  * pointers, bucket-major (bucket b, rank r at [b * W + r]); bucket b has
  * bucket_numel[b] elements.  The tensors of the plan are views into these
  * flat buffers, so nothing is copied in or out.  Under the pipelined policy
- * (float32 / bfloat16 SUM / AVG, two or more islands, no phase marks kept)
- * the buckets run as one pipeline of chunks (each bucket cut evenly into
- * chunks of at most 3 x chunk_bytes of payload: the pipeline fills once per
- * set, so larger copies pay) on a two-slot staging ring, the
- * bridge of one bucket overlapping the kernels of the next, captured as one
+ * (two or more islands, no phase marks kept) the buckets run as one
+ * pipeline of chunks (each bucket cut evenly into chunks of at most
+ * 3 x chunk_bytes of payload: the pipeline fills once per set, so larger
+ * copies pay) on a two-slot staging ring, the bridge of one bucket
+ * overlapping the kernels of the next, captured as one
  * CUDA graph for the whole set from the second call with the same buffers
  * (one launch per gradient sync); otherwise one gb_all_reduce per bucket.
  * Empty buckets are allowed (nothing to do; their pointers may be NULL). */
@@ -398,9 +397,9 @@ gb_status gb_all_reduce_buckets_ef(gb_ctx *ctx, int n_buckets, void *const *buck
  * in_bufs[b * W + 0 .. W - 1] (in bucket order; the island sums are encoded
  * whole, with the all_reduce codec blocks).  bucket_numel[b] must be a
  * multiple of W; inputs are not modified; outputs must not overlap inputs.
- * Under the pipelined policy (float32 / bfloat16 SUM / AVG, two or more
- * islands, no phase marks kept) the buckets run as one pipeline of chunks,
- * as in gb_all_reduce_buckets, captured as one CUDA graph per set from the
+ * Under the pipelined policy (two or more islands, no phase marks kept)
+ * the buckets run as one pipeline of chunks, as in gb_all_reduce_buckets,
+ * captured as one CUDA graph per set from the
  * second call with the same buffers; otherwise one gb_reduce_scatter per
  * bucket.  Empty buckets are allowed (their pointers may be NULL). */
 gb_status gb_reduce_scatter_buckets(gb_ctx *ctx, int n_buckets, const void *const *in_bufs, void *const *out_bufs,

@@ -103,3 +103,40 @@ def test_exact_path_refusals():
         ctx.all_reduce(f64, "sum", "none")
         torch.cuda.synchronize()
         assert ctx.status() == B.GB_OK
+
+
+@pytest.mark.parametrize("dt", [np.float16, np.float64, np.int8, np.uint8, np.int32, np.int64, np.float32], ids=str)
+@pytest.mark.parametrize("sizes", [(2, 2), (2, 1, 3)])
+def test_exact_bucket_sets_and_host_buffers(dt, sizes):
+    """The exact path through the bucket pipelines (all_reduce and
+    reduce_scatter sets, one graph per set) and the host-buffer pipeline,
+    bit for bit against the oracle."""
+    W = sum(sizes)
+    numels = [1000 * W, 0, 37 * W, 5000 * W]
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(4096)
+        for op in (["sum", "max"] if dt != np.float32 else ["max", "min"]):
+            for call in range(2):  # direct, then captured
+                xs = [[draw(dt, max(m, 1), 300 + 17 * r + b)[:m] for r in range(W)] for b, m in enumerate(numels)]
+                bufs = [[to_dev(x) for x in row] for row in xs]
+                ctx.all_reduce_buckets(bufs, op, "none", 256)
+                outs = [[torch.empty(m // W, dtype=TORCH[dt], device="cuda") for _ in range(W)] for m in numels]
+                ins = [[to_dev(x) for x in row] for row in xs]
+                ctx.reduce_scatter_buckets(ins, outs, op, "none", 256)
+                torch.cuda.synchronize()
+                for b, m in enumerate(numels):
+                    if m == 0:
+                        continue
+                    want = orc.all_reduce(xs[b], sizes, op)
+                    want_rs = orc.reduce_scatter(xs[b], sizes, op)
+                    for r in range(W):
+                        assert_bits_equal(to_host(bufs[b][r]), want[r], "%s %s bucket %d rank %d" % (dt, op, b, r))
+                        assert_bits_equal(to_host(outs[b][r]), want_rs[r], "RS %s %s bucket %d rank %d" % (dt, op, b, r))
+            n = 7000 * W + 3
+            xs = [draw(dt, n, 400 + r) for r in range(W)]
+            host = [torch.from_numpy(x.copy()).pin_memory() for x in xs]
+            ctx.all_reduce_host(host, op, "none", 256)
+            torch.cuda.synchronize()
+            want = orc.all_reduce(xs, sizes, op)
+            for r in range(W):
+                assert_bits_equal(host[r].numpy(), want[r], "host %s %s rank %d" % (dt, op, r))

@@ -27,6 +27,7 @@ constexpr int kMaxGraphs = 16;
 // sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
 constexpr int kMaxLinks = 8;
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
+constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
 constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2
 constexpr uint64_t kMaxElems = 1ull << 38;
 }  // namespace gbrt
@@ -140,13 +141,8 @@ struct Plan {
     size_t dev_bytes = 0, host_bytes = 0;
 };
 
-// gb_all_reduce_buckets as one pipeline over every bucket's chunks: chunk
-// i's encode, bridge hop and decode use staging slot i % 2 (a two-slot
-// ring), and chunks are issued one ahead (encode + device -> host of chunk
-// i+1 before host -> device + decode of chunk i), so the bridge of one
-// bucket overlaps the kernels of the next and never idles between buckets.
-// The ring is safe because on the kernel stream encode(i+1) follows
-// decode(i-1), which waited for every copy of chunk i-1.
+// One chunk of a bucket set's pipeline (enqueue_buckets): bucket b,
+// elements [e0, e0 + m).
 struct WorkChunk {
     int b;
     uint64_t e0, m;

@@ -668,13 +668,22 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
 }
 
 
+// A bucket set as one pipeline over every bucket's chunks.  Chunk i's
+// encode, bridge hop and decode use staging slot i % R (an R-slot ring), and
+// chunks are issued R - 1 ahead (encode + device -> host of chunk i + R - 1
+// before host -> device + decode of chunk i), so both copy streams always
+// have their next copy queued and the bridge of one bucket overlaps the
+// kernels of the next.  The ring is safe because on the kernel stream
+// encode(i + R - 1) follows decode(i - 1), which waited for every copy of
+// chunk i - 1, the slot's previous user.  Three slots took the 1.1B set from
+// 19.2 to 15.8 ms against two; four gained nothing more.
 // in / out: nb x W rank buffers, bucket-major.  rs == 0: all_reduce (out
 // may equal in); rs == 1: reduce_scatter, out[b * W + r] receives slice r of
-// bucket b (numel[b] / W elements).
+// bucket b (numel[b] / W elements).  res: error feedback, nb x I residuals.
 gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, const void *const *in,
                           void *const *out, const size_t *numel, int rs, float *const *res, cudaStream_t s) {
     const int I = p.I, W = p.W;
-    constexpr int R = 2;
+    constexpr int R = kBucketSlots;
     auto outbox = [&](int slot, int i) { return c->d_stage + ((size_t)slot * I + i) * p.part; };
     auto inbox = [&](int g, int slot, int j) {
         unsigned char *base = c->d_stage + (size_t)I * R * p.part;
@@ -769,9 +778,14 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
             GB_TRY(launch_decode(c, p, da, s));
         return GB_OK;
     };
-    GB_TRY(front(0));
+    // chunks are issued R - 1 ahead: chunk i + R - 1's encode and device ->
+    // host copy are queued before chunk i's host -> device copy and decode,
+    // so each copy stream always has the next copy waiting (its slot was
+    // last used by chunk i - 1, whose decode is already queued before it)
+    constexpr int ahead = R - 1;
+    for (int k = 0; k < ahead && k < N; ++k) GB_TRY(front(k));
     for (int i = 0; i < N; ++i) {
-        if (i + 1 < N) GB_TRY(front(i + 1));
+        if (i + ahead < N) GB_TRY(front(i + ahead));
         GB_TRY(back(i));
     }
     GB_TRY(record(c, c->ev_join_d, D));
@@ -855,8 +869,8 @@ gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out
             work.push_back({b, e0, (numel[b] - e0) < cb ? (numel[b] - e0) : cb});
     }
     const size_t recv = c->I == 2 ? 2 : (size_t)c->I * c->I;
-    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(c->I + recv) * 2 * p.part));
-    GB_TRY(grow_host(c, (size_t)c->I * 2 * p.part));
+    GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, (size_t)(c->I + recv) * kBucketSlots * p.part));
+    GB_TRY(grow_host(c, (size_t)c->I * kBucketSlots * p.part));
     GB_TRY(begin(c, s));
     if (!c->use_graphs) {
         GB_TRY(enqueue_buckets(c, p, work, in, out, numel, rs, res, s));

@@ -372,7 +372,7 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, 
  * (two or more islands, no phase marks kept) the buckets run as one
  * pipeline of chunks (each bucket cut evenly into chunks of at most
  * 3 x chunk_bytes of payload: the pipeline fills once per set, so larger
- * copies pay) on a two-slot staging ring, the bridge of one bucket
+ * copies pay) on a three-slot staging ring, the bridge of one bucket
  * overlapping the kernels of the next, captured as one
  * CUDA graph for the whole set from the second call with the same buffers
  * (one launch per gradient sync); otherwise one gb_all_reduce per bucket.

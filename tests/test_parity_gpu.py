@@ -387,7 +387,7 @@ def test_all_reduce_host_pipelined(codec, block, sizes, dtype):
 @pytest.mark.parametrize("codec,block", [("none", 256), ("bf16", 256), ("e4m3", 256), ("e5m2", 128)])
 @pytest.mark.parametrize("sizes", [(1, 1), (2, 2), (4, 4), (2, 1, 3)])
 def test_bucket_pipeline_matches_oracle(codec, block, sizes):
-    """gb_all_reduce_buckets as one pipeline over all buckets' chunks (two-slot
+    """gb_all_reduce_buckets as one pipeline over all buckets' chunks (three-slot
     staging ring, one CUDA graph for the set): every bucket gets the
     oracle's bits, on three calls with the same buffers."""
     W = sum(sizes)

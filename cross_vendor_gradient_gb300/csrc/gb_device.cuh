@@ -26,6 +26,20 @@ constexpr int kWarp = 32;
 // block 2t+1; with blocks of 256 the whole warp is one block.
 __device__ __forceinline__ unsigned lane_elem(int lane, int k) { return (unsigned)(lane * 8 + k); }
 
+// ------------------------------------------ programmatic dependent launch
+// Every kernel is launched allowed to start while the kernel before it on the
+// stream drains (launch_grid), which hides the gap between back-to-back
+// launches.  Before its first global memory access each kernel waits here
+// until that kernel has completed and its writes are visible (immediate when
+// the previous operation on the stream is not a kernel).  The returned 0 is
+// added to the kernel's first index, so every address it touches depends on
+// the wait and no load can be scheduled ahead of it.
+__device__ __forceinline__ uint32_t wait_prior_grid() {
+    uint32_t z;
+    asm volatile("griddepcontrol.wait;\n\tmov.u32 %0, 0;" : "=r"(z) : : "memory");
+    return z;
+}
+
 // ------------------------------------------------------- memory accesses
 // Rank buffers are read once per collective: bypass L1 and mark the lines
 // evict-first in L2.  Payloads are re-read soon (copy engines, the decode

@@ -138,8 +138,25 @@ cudaError_t launch_grid(uint64_t tiles_per_unit, unsigned units, const Args &a, 
     const uint64_t per_unit_cap = cap / units > 0 ? cap / units : 1;
     const uint64_t want = (tiles_per_unit + 7) / 8;  // 8 warps (tiles) per block
     const uint64_t gx = want < per_unit_cap ? want : per_unit_cap;
-    Kern<<<dim3((unsigned)(gx ? gx : 1), units), 256, 0, s>>>(a);
+    // programmatic dependent launch: the grid may be scheduled while the
+    // previous kernel on the stream drains; the kernel itself waits for that
+    // kernel's completion before touching memory (wait_prior_grid)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(gx ? gx : 1), units);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, Kern, a);
     count_launch();
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear it: the caller reports e
+        return e;
+    }
     return cudaGetLastError();
 }
 

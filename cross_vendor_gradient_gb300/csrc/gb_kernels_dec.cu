@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ De
     const int nsrc = NS > 0 ? NS : a.n_src;
     const uint32_t wpb = blockDim.x >> 5;
     const uint32_t stride = gridDim.x * wpb;
-    uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5);
+    uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5) + wait_prior_grid();
     if constexpr (NS > 0) {
         // Full tiles (vector path), software-pipelined: the payload loads of
         // the warp's next tile are in flight while the current one is decoded
@@ -263,7 +263,8 @@ __global__ void __launch_bounds__(256) k_decompress_acc(const __grid_constant__ 
     const int lane = threadIdx.x & 31;
     const uint32_t wpb = blockDim.x >> 5;
     const uint32_t tiles = (uint32_t)((a.n + kTile - 1) / kTile);
-    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < tiles; tile += gridDim.x * wpb) {
+    const uint32_t first = blockIdx.x * wpb + (threadIdx.x >> 5) + wait_prior_grid();
+    for (uint32_t tile = first; tile < tiles; tile += gridDim.x * wpb) {
         const uint64_t base = (uint64_t)tile * kTile;
         const bool full = base + kTile <= a.n;
         float d[8];
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(256) k_decompress_acc(const __grid_constant__ 
 }
 
 __global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a) {
-    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x + wait_prior_grid();
     const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
     if (a.vec) {
         const uint64_t chunks = a.bytes / 16;

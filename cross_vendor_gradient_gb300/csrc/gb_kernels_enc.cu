@@ -206,9 +206,10 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
     const uint32_t stride = gridDim.x * wpb;
     const uint64_t n = a.n;
     unsigned char *payload = (unsigned char *)a.payload[isl];
+    const uint32_t warp0 = blockIdx.x * wpb + (threadIdx.x >> 5) + wait_prior_grid();
     if constexpr (kTilesPerStep<T, KT, EF> == 2) {
         const uint32_t steps = (a.tiles + 1) / 2;
-        for (uint32_t st = blockIdx.x * wpb + (threadIdx.x >> 5); st < steps; st += stride) {
+        for (uint32_t st = warp0; st < steps; st += stride) {
             const uint32_t t0 = 2 * st;
             uint4 raw[2][KT > 0 ? KT : 1];
             bool full[2];
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
         }
         return;
     }
-    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5); tile < a.tiles; tile += stride) {
+    for (uint32_t tile = warp0; tile < a.tiles; tile += stride) {
         const uint64_t base = (uint64_t)tile * kTile;
         const bool full = base + kTile <= n;
         float v[8];

@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ Re
     const int K = a.first[isl + 1] - r0;
     P *out = (P *)a.payload[isl];
     const uint64_t nvec = (a.n + N - 1) / N;
-    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; vi < nvec;
+    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid(); vi < nvec;
          vi += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t j0 = vi * N;
         const int cnt = (a.n - j0) < (uint64_t)N ? (int)(a.n - j0) : N;
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ D
         limit = a.n;
     }
     const uint64_t nvec = (limit + N - 1) / N;
-    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; vi < nvec;
+    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid(); vi < nvec;
          vi += (uint64_t)gridDim.x * blockDim.x) {
         const uint64_t l0 = vi * N;
         const int cnt = (limit - l0) < (uint64_t)N ? (int)(limit - l0) : N;

@@ -29,7 +29,11 @@
  *     nothing enqueued; otherwise it enqueues its work on `stream` and returns
  *     without waiting for it (stream order, as torch.distributed's NCCL
  *     collectives: gpubridge README, "Stream semantics").  Inputs must not be
- *     written, and outputs not read, before that work completes.
+ *     written, and outputs not read, before that work completes.  The
+ *     kernels are programmatic dependent launches: one may be scheduled
+ *     while the kernel before it on the stream drains, but it touches no
+ *     memory until that kernel has completed, so plain stream order holds
+ *     for the caller's own kernels on both sides.
  *   - n = 0 is a valid no-op.
  *   - A context owns its pinned host slots and device staging buffers.  They
  *     grow to the largest call made so far and are released by gb_destroy

@@ -340,7 +340,7 @@ def run_gb(args, world, rank, local, pg):
 
     # ---- timed region 1: the step as a user runs it (pipelined policy, graph
     # replay, no phase marks: a CUDA event between kernels drains the stream)
-    launches, clk, t_wall, ms = 0, None, 0.0, None
+    launches, clk, t_wall, ms, host_us = 0, None, 0.0, None, None
     if not args.roofline_only:
         ctx.set_pipeline(chunk_bytes, not args.no_graphs)
         ctx.set_sharded_bridge(args.sharded)
@@ -364,6 +364,8 @@ def run_gb(args, world, rank, local, pg):
         clk = clocks.stop()
         step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
         ms = max_over_ranks(pg, float(np.mean(step_ms)), dev if pg is not None else None)
+        if not ef:
+            host_us = host_call_us(ctx, bufs, pristine, w.op, codec, w.block, stream)
 
     # ---- timed region 2: per-kernel durations for the roofline.  One full
     # launch of each kernel per step (one bridge hop per call), CUDA events
@@ -481,8 +483,47 @@ def run_gb(args, world, rank, local, pg):
         "gpu_launches": int(launches),
         "timed_wall_s": t_wall,
         "clocks": clk,
+        **({"host_call_us": host_us} if host_us else {}),
     }
     return line, w, xs, codec
+
+
+def host_call_us(ctx, bufs, pristine, op, codec, block, stream, calls=200):
+    """Host wall time of one all_reduce call: the library's own work per call
+    (argument checks, plan and graph lookup, the enqueue) through a ctypes
+    call with prepared arguments, and the same call through the tensor-level
+    Context.  The queue is drained every 20 calls, outside the timed calls,
+    so that no call waits for queue space.  The rank buffers are restored
+    between calls, also outside the timed calls."""
+    import torch
+    from cross_vendor_gradient_gb300 import binding as B
+    from cross_vendor_gradient_gb300.api import _codec, _dtype, _op
+    arr = B._ptrs([t.data_ptr() for t in bufs])
+    args = (ctx.handle, arr, bufs[0].numel(), _dtype(bufs), _op(op), _codec(codec), block, stream.cuda_stream)
+    fn = B.lib().gb_all_reduce
+    out = {}
+    for name, call in (("library", lambda: fn(*args)),
+                       ("python_api", lambda: ctx.all_reduce(bufs, op, codec, block, stream=stream))):
+        torch.cuda.synchronize()
+        t = []
+        for k in range(calls):
+            if k % 20 == 0:
+                torch.cuda.synchronize()  # keep the queue short: no call waits for queue space
+            with torch.cuda.stream(stream):
+                for b, p0 in zip(bufs, pristine):
+                    b.copy_(p0, non_blocking=True)
+            t0 = time.perf_counter()
+            st = call()
+            t.append(time.perf_counter() - t0)
+            if name == "library" and st != 0:
+                raise RuntimeError("gb_all_reduce failed: %d" % st)
+        torch.cuda.synchronize()
+        out[name + "_median_us"] = statistics.median(t) * 1e6
+    out["calls"] = calls
+    out["what"] = ("host wall time per gb_all_reduce call (enqueue of the graph-replayed pipelined step; "
+                   "the device work runs after): a ctypes call with prepared arguments, and "
+                   "Context.all_reduce")
+    return out
 
 
 KERNEL_SOURCES = ("gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_device.cuh", "gb_kernels.cuh")

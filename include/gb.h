@@ -289,6 +289,8 @@ gb_status gb_island_reduce_compress(gb_ctx *ctx, const void *const *rank_bufs, s
 gb_status gb_island_reduce_compress_ef(gb_ctx *ctx, const void *const *rank_bufs, float *const *residuals, size_t n,
                                        gb_dtype dtype, gb_codec codec, int block, void *const *payloads,
                                        gb_stream stream);
+/* The second half, decode + accumulate + broadcast (described with
+ * gb_island_reduce_compress above). */
 gb_status gb_decompress_island_broadcast(gb_ctx *ctx, const void *const *payloads, size_t n, gb_dtype dtype,
                                          gb_op op, gb_codec codec, int block, void *const *rank_bufs,
                                          gb_stream stream);

@@ -64,9 +64,11 @@ typedef void *gb_stream;
 typedef enum {
     GB_OK = 0,
     GB_ERR_INVALID_ARG = 1,       /* null pointer, bad layout, bad size, bad rank index   */
-    GB_ERR_UNSUPPORTED_DTYPE = 2, /* dtype other than GB_F32 / GB_BF16                    */
-    GB_ERR_UNSUPPORTED_OP = 3,    /* op other than GB_SUM / GB_AVG                        */
-    GB_ERR_UNSUPPORTED_CODEC = 4, /* unknown codec, or fp8 block not 128 / 256            */
+    GB_ERR_UNSUPPORTED_DTYPE = 2, /* not a gb_dtype, or a dtype the call does not take    */
+    GB_ERR_UNSUPPORTED_OP = 3,    /* not a gb_op, AVG on integers, or an op the call does */
+                                  /* not take (MAX / MIN where only SUM / AVG apply)      */
+    GB_ERR_UNSUPPORTED_CODEC = 4, /* unknown codec, fp8 block not 128 / 256, or a codec   */
+                                  /* on float16 / float64 SUM / AVG                       */
     GB_ERR_MISALIGNED = 5,        /* a device buffer not 32-byte aligned                  */
     GB_ERR_ALLOC = 6,             /* pinned or device staging allocation failed (sticky)  */
     GB_ERR_CUDA = 7,              /* a CUDA runtime call failed (sticky)                  */

@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--impl", choices=["gb", "reference"], default="gb")
     p.add_argument("--workload", default="c2")
     p.add_argument("--codec", default=None)
+    p.add_argument("--block", type=int, default=None, help="fp8 scale block override (128 or 256)")
     p.add_argument("--dtype", default=None, help="rank dtype override (f32 bf16 f16 f64 i8 u8 i32 i64)")
     p.add_argument("--op", default=None, help="op override (sum avg max min)")
     p.add_argument("--n", type=int, default=None, help="override elements per rank")
@@ -271,11 +272,11 @@ def run_gb(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = wl.WORKLOADS[args.workload]
-    if args.dtype or args.op or args.islands:
+    if args.dtype or args.op or args.islands or args.block:
         import dataclasses
         w = dataclasses.replace(w, dtype=args.dtype or w.dtype, op=args.op or w.op,
                                 island_sizes=tuple(int(v) for v in args.islands.split(",")) if args.islands
-                                else w.island_sizes)
+                                else w.island_sizes, block=args.block or w.block)
     exact = w.op in ("max", "min") or w.dtype not in ("f32", "bf16")
     codec = "none" if exact else (args.codec or w.codecs[0])
     n = args.n or w.n

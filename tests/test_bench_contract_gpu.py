@@ -1,0 +1,64 @@
+"""bench.py's output contract on the GPU: one JSON line with the metric, the
+device-timed value, the roofline of the dominant kernel, the end-to-end
+figure through host buffers, the oracle baseline, the kernel count and the
+clocks, all self-consistent."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_bench(*args):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, capture_output=True,
+                         text=True, timeout=900)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_default_line_contract():
+    d = run_bench("--steps", "20", "--warmup", "3")
+    with open(os.path.join(ROOT, "BASELINE.json")) as f:
+        metric = json.load(f)["metric"]
+    assert d["metric"] == metric and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3 and d["scaling"] == "weak"
+    assert d["vs_baseline"] is None and d["dtype"] == "f32" and "synthetic" in d["data"]
+    assert d["config"]["workload"].startswith("c2") and "flushed" in d["config"]["l2"]
+    # value = bytes of one rank buffer per step / step time
+    n = d["config"]["n"]
+    assert abs(d["value"] - n * 4 / (d["ms_per_step"] * 1e-3) / 1e9) < 1e-6 * d["value"]
+    r = d["roofline"]
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["kernel"] in ("k_decode_bcast", "k_reduce_encode")
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-9
+    assert abs(r["achieved"] - r["alg_bytes_per_launch"] / (r["avg_launch_ms"] * 1e-3) / 1e9) < 1e-6 * r["achieved"]
+    assert 0.3 < r["frac"] < 1.3  # a copy-peak denominator: a little above 1.0 is possible, far above is not
+    assert r["traffic"] is None or r["traffic"] > 0
+    e = d["e2e"]
+    assert e["unit"] == "GB/s" and e["h2d_bytes_per_step"] == 4 * n * 4 and e["d2h_bytes_per_step"] == 4 * n * 4
+    assert 0 < e["value"] < d["value"]  # the host link bounds it below the device-resident step
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    assert d["gpu_launches"] == 20 * 8  # 4 chunks x (encode + decode) per graph-replayed step
+    c = d["clocks"]
+    assert c["sm_mhz"] > 0 and isinstance(c["reasons"], list)
+
+
+def test_reference_arm_contract():
+    d = run_bench("--impl", "reference", "--steps", "3", "--warmup", "3")
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0

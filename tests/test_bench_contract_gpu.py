@@ -32,9 +32,8 @@ def run_bench(*args):
 
 def test_default_line_contract():
     d = run_bench("--steps", "20", "--warmup", "3")
-    with open(os.path.join(ROOT, "BASELINE.json")) as f:
-        metric = json.load(f)["metric"]
-    assert d["metric"] == metric and d["unit"] == "GB/s" and d["higher_is_better"] is True
+    assert d["metric"] == "all_reduce algorithm GB/s and % of GB300 HBM roofline vs payload size, per codec"
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 20 and d["warmup"] == 3 and d["scaling"] == "weak"
     assert d["vs_baseline"] is None and d["dtype"] == "f32" and "synthetic" in d["data"]
     assert d["config"]["workload"].startswith("c2") and "flushed" in d["config"]["l2"]

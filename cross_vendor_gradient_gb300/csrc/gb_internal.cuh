@@ -177,8 +177,10 @@ size_t payload_bytes(int codec, int block, size_t n);
 size_t scales_offset(int codec, size_t n);
 bool is_fp8(int codec);
 size_t part_bytes(const Plan &p, uint64_t m);
+// balance: cut n into equal chunks of whole tiles (no short remainder);
+// the bucket pipeline balances per bucket itself and passes false.
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
-               bool sharded_ok = false, size_t chunk_bytes = 0);
+               bool sharded_ok = false, size_t chunk_bytes = 0, bool balance = true);
 gb_status check_launch(gb_ctx *c, cudaError_t e, const char *what);
 gb_status launch_encode(gb_ctx *c, const Plan &p, const gb::ReduceEncodeArgs &ra, cudaStream_t s);
 gb_status launch_decode(gb_ctx *c, const Plan &p, const gb::DecodeBcastArgs &da, cudaStream_t s);

@@ -292,7 +292,7 @@ size_t part_bytes(const Plan &p, uint64_t m) {
 }
 
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
-               bool sharded_ok, size_t chunk_bytes) {
+               bool sharded_ok, size_t chunk_bytes, bool balance) {
     if (chunk_bytes == 0) chunk_bytes = c->chunk_bytes;
     Plan p;
     p.I = c->I;
@@ -324,6 +324,13 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
         const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
         if (ch < min_ch) ch = min_ch;
+        if (balance && ch < n) {
+            // as many chunks as chunk_bytes needs, of equal size (whole tiles):
+            // no short remainder chunk whose copies would cost their fixed
+            // overhead for a sliver of data
+            const uint64_t cnt = (n + ch - 1) / ch;
+            ch = round_up((n + cnt - 1) / cnt, gb::kTile);
+        }
         if (ch < n) p.chunk = ch;
     }
     p.C = (int)((n + p.chunk - 1) / p.chunk);
@@ -857,7 +864,7 @@ gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out
     // Llama-style bf16 sets)
     size_t nmax = 0;
     for (int b = 0; b < nb; ++b) nmax = numel[b] > nmax ? numel[b] : nmax;
-    Plan p = make_plan(c, nmax, dtype, op, codec, block, 0, false, kBucketChunkScale * c->chunk_bytes);
+    Plan p = make_plan(c, nmax, dtype, op, codec, block, 0, false, kBucketChunkScale * c->chunk_bytes, false);
     // each bucket in balanced chunks of whole tiles, none larger than the
     // plan's chunk (so a bucket never ends in a sliver of a chunk)
     std::vector<WorkChunk> work;

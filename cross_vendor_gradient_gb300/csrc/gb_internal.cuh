@@ -29,6 +29,8 @@ constexpr int kMaxLinks = 8;
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
 constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
 constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2
+constexpr size_t kRsChunkDiv = 2;        // gb_reduce_scatter: chunk = the pipeline chunk / 2
+constexpr size_t kBcastPieceScale = 4;   // gb_broadcast: pieces of up to 4 x the pipeline chunk
 constexpr uint64_t kMaxElems = 1ull << 38;
 }  // namespace gbrt
 

@@ -175,12 +175,14 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  *   use_graphs != 0 (default): a pipelined call is captured into a CUDA
  *     graph the second time the same buffers and shape are seen, and
  *     replayed from then on (one launch instead of a few dozen).
- * reduce_scatter follows the same policy (its chunks' decodes write the
- * parts of the slices they cover).  all_gather with chunk_bytes > 0 moves
- * groups of whole rank blocks of about chunk_bytes: one group's host ->
- * device copies overlap the next group's device -> host copies.  broadcast
- * with chunk_bytes > 0 moves the source in pieces of about chunk_bytes (at
- * most 64 pieces) the same way.  Waits for the context's outstanding work. */
+ * reduce_scatter follows the same policy with chunks of half chunk_bytes
+ * (its chunks' decodes write the parts of the slices they cover).
+ * all_gather with chunk_bytes > 0 moves groups of whole rank blocks of
+ * about chunk_bytes: one group's host -> device copies overlap the next
+ * group's device -> host copies.  broadcast with chunk_bytes > 0 moves the
+ * source the same way in equal pieces of up to 4 x chunk_bytes (at most 64
+ * pieces; one hop up to that size).  Waits for the context's outstanding
+ * work. */
 gb_status gb_set_pipeline(gb_ctx *ctx, size_t chunk_bytes, int use_graphs);
 
 /* The sharded-bridge policy of gb_all_reduce and gb_all_reduce_ef (gpubridge

@@ -454,7 +454,7 @@ def run_gb(args, world, rank, local, pg):
                    "policy": (("sharded-bridge, %d links%s" % (
                        min(w.island_sizes), ", CUDA graph replay" if not args.no_graphs else ""))
                               if args.sharded and min(w.island_sizes) > 1 else
-                              ("pipelined-reduce-bridge-broadcast, %d KiB payload chunks%s" % (
+                              ("pipelined-reduce-bridge-broadcast, equal payload chunks of at most %d KiB%s" % (
                                   chunk_bytes >> 10, ", CUDA graph replay" if not args.no_graphs else ""))
                               if chunk_bytes else "reduce-bridge-broadcast"),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB "
@@ -954,8 +954,12 @@ def run_collective(args, world, rank, local, pg):
                                "(n=%d), %s%s" % (w.key, W, list(w.island_sizes), coll, n * b / 2 ** 20, n, w.dist,
                                                  (", op %s, codec %s block %d" % (w.op, codec, w.block))
                                                  if coll == "reduce_scatter" else ", exact"),
-                   "policy": "pipelined, %d KiB chunks" % (chunk_bytes >> 10) if coll != "broadcast" else
-                   "one bridge hop",
+                   "policy": {"reduce_scatter": "pipelined, equal payload chunks of at most %d KiB" % (
+                                  chunk_bytes >> 11),
+                              "all_gather": "pipelined, groups of whole rank blocks of about %d KiB" % (
+                                  chunk_bytes >> 10),
+                              "broadcast": "pipelined, equal pieces of up to %d KiB" % (chunk_bytes >> 8)}[coll]
+                   if chunk_bytes else "one bridge hop",
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_launch": dom[1],

@@ -148,12 +148,30 @@ __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ Re
         A s[N];
         if (cnt == N) {
             const V16<T> x = load16((const T *)a.src[r0] + j0);
+            if constexpr (sizeof(T) == 2 && !std::is_integral<T>::value) {
+                // 16-bit floats: widening takes conversions, so the next
+                // rank's load is issued before the current one is folded
+                // (f16 AVG fold 20.6 -> 17.4 us on 4 x 13 MB; for 32-bit types
+                // the same change measured slower)
+                V16<T> y = x;
+                if (K > 1) y = load16((const T *)a.src[r0 + 1] + j0);
 #pragma unroll
-            for (int k = 0; k < N; ++k) s[k] = Ex<T>::widen(x.v[k]);
-            for (int q = 1; q < K; ++q) {
-                const V16<T> y = load16((const T *)a.src[r0 + q] + j0);
+                for (int k = 0; k < N; ++k) s[k] = Ex<T>::widen(x.v[k]);
+                for (int q = 1; q < K; ++q) {
+                    V16<T> nx = y;
+                    if (q + 1 < K) nx = load16((const T *)a.src[r0 + q + 1] + j0);
 #pragma unroll
-                for (int k = 0; k < N; ++k) s[k] = fold<OP>(s[k], Ex<T>::widen(y.v[k]));
+                    for (int k = 0; k < N; ++k) s[k] = fold<OP>(s[k], Ex<T>::widen(y.v[k]));
+                    y = nx;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < N; ++k) s[k] = Ex<T>::widen(x.v[k]);
+                for (int q = 1; q < K; ++q) {
+                    const V16<T> y = load16((const T *)a.src[r0 + q] + j0);
+#pragma unroll
+                    for (int k = 0; k < N; ++k) s[k] = fold<OP>(s[k], Ex<T>::widen(y.v[k]));
+                }
             }
             P o[N];
 #pragma unroll

@@ -12,14 +12,28 @@ SRC = os.path.join(HERE, "oracle.c")
 LIB = os.path.join(HERE, "liboracle.so")
 
 
+SELFTEST_SRC = os.path.join(HERE, "selftest.c")
+SELFTEST = os.path.join(HERE, "selftest")
+
+
+def _fresh(out, *srcs):
+    return os.path.exists(out) and all(os.path.getmtime(out) >= os.path.getmtime(s) for s in srcs)
+
+
 def build(force: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
-        return LIB
-    tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
-           "-fexcess-precision=standard", "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    """liboracle.so, and the C self-test program linked against it."""
+    if force or not _fresh(LIB, SRC):
+        tmp = LIB + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+               "-fexcess-precision=standard", "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, LIB)
+    if force or not _fresh(SELFTEST, SELFTEST_SRC, LIB):
+        tmp = SELFTEST + ".tmp.%d" % os.getpid()
+        cmd = ["gcc", "-O1", "-std=c11", "-fno-fast-math", "-ffp-contract=off", "-Wall", "-Wextra", "-Werror",
+               "-o", tmp, SELFTEST_SRC, "-L", HERE, "-loracle", "-Wl,-rpath," + HERE, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, SELFTEST)
     return LIB
 
 

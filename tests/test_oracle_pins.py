@@ -752,3 +752,23 @@ def test_sharded_integer_sums_are_exact(sizes, op):
     got = orc.all_reduce_sharded(xs, sizes, op, "none", 256)
     for r in range(W):
         assert np.array_equal(got[r], want.astype(np.float32)), r
+
+
+# ------------------------------------------------------------ C self-test
+
+def test_oracle_c_selftest():
+    """oracle/selftest.c checks the oracle from C, with no Python in between:
+    the README's four-rank demo for every codec, the codec size ratios and the
+    OFP8 table values (the golden fixtures), and the block-scale rule's
+    closed forms."""
+    import os
+    import subprocess
+    from oracle import build as ob
+    ob.build()
+    golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    out = subprocess.run([ob.SELFTEST] + [os.path.join(golden, f) for f in
+                                          ("demo_four_ranks.txt", "codec_sizes.txt", "ofp8_values.txt")],
+                         capture_output=True, text=True, timeout=60)
+    lines = out.stdout.strip().splitlines()
+    assert out.returncode == 0 and not [l for l in lines if not l.startswith("ok ")], out.stdout + out.stderr
+    assert len(lines) == 16

@@ -153,8 +153,11 @@ int gb_island_size(const gb_ctx *ctx, int island);
 int gb_island_first_rank(const gb_ctx *ctx, int island); /* = the island's leader */
 int gb_island_of_rank(const gb_ctx *ctx, int rank);
 
-/* Grow the context's staging so that collectives on up to n elements of
- * `dtype` with `codec` / `block` need no further allocation.  Enqueues
+/* Grow the context's staging so that the single-buffer collectives
+ * (gb_all_reduce, gb_all_reduce_ef, gb_reduce_scatter, gb_all_gather,
+ * gb_broadcast) on up to n elements of `dtype` with `codec` / `block`, under
+ * the policy set when it is called, need no further allocation.  The
+ * bucket-set calls and gb_all_reduce_host may still grow it.  Enqueues
  * nothing. */
 gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int block);
 

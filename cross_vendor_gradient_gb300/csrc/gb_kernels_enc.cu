@@ -246,44 +246,44 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
                 encode_store<CODEC, BLOCK, false>(payload, a.scales_off, tile, lane, n, full[h], v, nullptr);
             }
         }
-        return;
-    }
-    for (uint32_t tile = warp0; tile < a.tiles; tile += stride) {
-        const uint64_t base = (uint64_t)tile * kTile;
-        const bool full = base + kTile <= n;
-        float v[8];
-        island_sum<T, KT>(a, r0, K, base, lane, full, v);
-        if constexpr (EF) {
-            float *res = a.residual[isl];
-            float r[8], dec[8];
-            if (full) {
-                const U8x32 x = ld_rw_v8(res + base + 8 * lane);
+    } else {
+        for (uint32_t tile = warp0; tile < a.tiles; tile += stride) {
+            const uint64_t base = (uint64_t)tile * kTile;
+            const bool full = base + kTile <= n;
+            float v[8];
+            island_sum<T, KT>(a, r0, K, base, lane, full, v);
+            if constexpr (EF) {
+                float *res = a.residual[isl];
+                float r[8], dec[8];
+                if (full) {
+                    const U8x32 x = ld_rw_v8(res + base + 8 * lane);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) r[k] = __uint_as_float(x.w[k]);
-            } else {
+                    for (int k = 0; k < 8; ++k) r[k] = __uint_as_float(x.w[k]);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t j = base + lane_elem(lane, k);
-                    r[k] = j < n ? res[j] : 0.0f;
+                    for (int k = 0; k < 8; ++k) {
+                        const uint64_t j = base + lane_elem(lane, k);
+                        r[k] = j < n ? res[j] : 0.0f;
+                    }
                 }
-            }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], r[k]);
-            encode_store<CODEC, BLOCK, true>(payload, a.scales_off, tile, lane, n, full, v, dec);
-            if (full) {
-                uint32_t w[8];
+                for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], r[k]);
+                encode_store<CODEC, BLOCK, true>(payload, a.scales_off, tile, lane, n, full, v, dec);
+                if (full) {
+                    uint32_t w[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__fsub_rn(v[k], dec[k]));
-                st_v8(res + base + 8 * lane, w);
-            } else {
+                    for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__fsub_rn(v[k], dec[k]));
+                    st_v8(res + base + 8 * lane, w);
+                } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t j = base + lane_elem(lane, k);
-                    if (j < n) res[j] = __fsub_rn(v[k], dec[k]);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint64_t j = base + lane_elem(lane, k);
+                        if (j < n) res[j] = __fsub_rn(v[k], dec[k]);
+                    }
                 }
+            } else {
+                encode_store<CODEC, BLOCK, false>(payload, a.scales_off, tile, lane, n, full, v, nullptr);
             }
-        } else {
-            encode_store<CODEC, BLOCK, false>(payload, a.scales_off, tile, lane, n, full, v, nullptr);
         }
     }
 }

@@ -68,7 +68,9 @@ def parse():
     p.add_argument("--roofline-only", action="store_true",
                    help="only the per-kernel timed regions (kernels inside one-hop steps, and back to "
                         "back); for profiling")
-    p.add_argument("--sweep", action="store_true", help="payload sweep rows (one JSON line each)")
+    p.add_argument("--sweep", action="store_true", help="payload sweep rows only (one JSON line each)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="leave the payload sweep out of the default bench line")
     p.add_argument("--collective", default="all_reduce",
                    choices=["all_reduce", "reduce_scatter", "all_gather", "broadcast"],
                    help="the collective one step runs (all_reduce: the default bench line)")
@@ -206,32 +208,54 @@ def dataclasses_replace_f32(w):
     return dataclasses.replace(w, dtype="f32")
 
 
+def stream_set_count(set_bytes):
+    """Input sets cycled by kernel_stream: together at least 4 x L2 when a
+    set is large (at least 5, at most 8 GiB in all), else 16 sets."""
+    return max(5, min(-(-(4 * L2_BYTES) // set_bytes), 16 if set_bytes * 16 < 4 * L2_BYTES else 1 << 30,
+                      (8 << 30) // set_bytes))
+
+
+def make_sets(pristine, I, P, S, ef=False):
+    """S distinct input sets (copies of the rank buffers), output buffers,
+    payloads of P bytes per island and, with error feedback, residuals."""
+    import torch
+    n = pristine[0].numel()
+    dev = pristine[0].device
+    return {"S": S,
+            "ins": [[p.clone() for p in pristine] for _ in range(S)],
+            "outs": [[torch.empty_like(p) for p in pristine] for _ in range(S)],
+            "pays": [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)],
+            "res": [[torch.zeros(n, dtype=torch.float32, device=dev) for _ in range(I)] for _ in range(S)]
+            if ef else None}
+
+
 def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, batches,
-                  names=("k_reduce_encode", "k_decode_bcast"), ef=False):
+                  names=("k_reduce_encode", "k_decode_bcast"), ef=False, sets=None):
     """Timed region 3: each kernel launched back to back, as the fused halves
     of the path (gb_island_reduce_compress, gb_decompress_island_broadcast),
     with the same grid as in a step.  S distinct input sets, outputs and
     payloads (together at least 4 x L2 when a set is large, else 16 sets) are
-    cycled.  A batch starts from a clean L2 (256 MiB read) after a ~0.4 ms
-    GPU spin, so the host has queued the whole batch before its first event;
-    each kernel's first launch of the batch is untimed and CUDA events on the
-    launching stream bracket the other S - 1.  So no launch finds its inputs
-    in L2, and every timed launch also writes back what its predecessor left
-    dirty there: the steady state of a stream of buckets.  Returns per-launch
-    milliseconds of both kernels.  ef: the encode carries error feedback
-    (gb_island_reduce_compress_ef, one float32 residual per island and set)."""
+    cycled.  Each batch (S encodes, then S decodes) starts from a clean L2
+    (256 MiB read) after a ~0.4 ms GPU spin, so the host has queued the whole
+    batch before its first event; each kernel's first launch of the batch is
+    untimed and CUDA events on the launching stream bracket the other S - 1.
+    So no launch finds its inputs in L2: the decode batch starts after the
+    payloads have been evicted, as payloads landed by the bridge's copies
+    are read from HBM in a step.  Every timed launch also writes back what
+    its predecessor left dirty in L2: the steady state of a stream of
+    buckets.  Returns per-launch milliseconds of both kernels.  ef: the
+    encode carries error feedback (gb_island_reduce_compress_ef, one float32
+    residual per island and set).  sets: prebuilt make_sets() buffers (their
+    payloads at least P bytes), reused across calls."""
     import torch
     W = len(pristine)
     n = pristine[0].numel()
     b = pristine[0].element_size()
     set_bytes = W * n * b + I * P + (I * n * 4 if ef else 0)
-    S = max(5, min(-(-(4 * L2_BYTES) // set_bytes), 16 if set_bytes * 16 < 4 * L2_BYTES else 1 << 30,
-                   (8 << 30) // set_bytes))
-    dev = pristine[0].device
-    ins = [[p.clone() for p in pristine] for _ in range(S)]
-    outs = [[torch.empty_like(p) for p in pristine] for _ in range(S)]
-    pays = [[torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)] for _ in range(S)]
-    res = [[torch.zeros(n, dtype=torch.float32, device=dev) for _ in range(I)] for _ in range(S)] if ef else None
+    if sets is None:
+        sets = make_sets(pristine, I, P, stream_set_count(set_bytes), ef)
+    S = sets["S"]
+    ins, outs, pays, res = sets["ins"], sets["outs"], sets["pays"], sets["res"]
     # every leader's row holds the same I payloads: the call decodes them
     # once and writes all ranks, as the decode in a step does
     rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
@@ -250,6 +274,8 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
                     e[0].record(stream)
             if e:
                 e[1].record(stream)
+            clean.amax()  # evict the payloads: the decodes read them from HBM
+            torch.cuda._sleep(800_000)
             for q in range(S):
                 ctx.decompress_island_broadcast(rows[q], op, codec, block, outs[q], stream=stream)
                 if e and q == 0:
@@ -260,6 +286,27 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
     return {"sets": S, "timed_launches_per_batch": S - 1, "batches": batches, "set_bytes": set_bytes,
             names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
             names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
+
+
+def pinned_link(dev, stream, big=256 << 20):
+    """Pinned copy bandwidth (the bridge's roofline): the best of five
+    256 MiB cudaMemcpyAsync copies each way, CUDA events on the stream."""
+    import torch
+    hbuf = torch.empty(big, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(big, dtype=torch.uint8, device=dev)
+    link = {}
+    with torch.cuda.stream(stream):
+        for name, (dst, src) in (("d2h_gbs", (hbuf, dbuf)), ("h2d_gbs", (dbuf, hbuf))):
+            best = 0.0
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                dst.copy_(src, non_blocking=True)
+                e1.record(stream)
+                e1.synchronize()
+                best = max(best, big / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+            link[name] = best
+    return link
 
 
 def run_gb(args, world, rank, local, pg):
@@ -302,23 +349,7 @@ def run_gb(args, world, rank, local, pg):
     chunk_bytes = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
     ctx.reserve(n, tdt, codec, w.block)
 
-    # pinned copy bandwidth (bridge roofline), one large copy each way
-    big = 256 << 20
-    hbuf = torch.empty(big, dtype=torch.uint8, pin_memory=True)
-    dbuf = torch.empty(big, dtype=torch.uint8, device=dev)
-    link = {}
-    with torch.cuda.stream(stream):
-        for name, (dst, src) in (("d2h_gbs", (hbuf, dbuf)), ("h2d_gbs", (dbuf, hbuf))):
-            best = 0.0
-            for _ in range(5):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                dst.copy_(src, non_blocking=True)
-                e1.record(stream)
-                e1.synchronize()
-                best = max(best, big / (e0.elapsed_time(e1) * 1e-3) / 1e9)
-            link[name] = best
-    del hbuf, dbuf
+    link = pinned_link(dev, stream)
 
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -374,6 +405,15 @@ def run_gb(args, world, rank, local, pg):
     Kr = args.steps if args.roofline_only else min(K, 500)
     ctx.set_pipeline(0, False)
     ctx.set_sharded_bridge(False)
+    # the same one-hop steps without phase marks first: the difference is
+    # what the marks' CUDA events cost the step
+    with torch.cuda.stream(stream):
+        for i in range(Wm):
+            step(i, False)
+        for i in range(Kr):
+            step(i, True)
+    torch.cuda.synchronize()
+    nomark_ms = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Kr)]))
     ctx.set_phase_timing(Kr)
     with torch.cuda.stream(stream):
         for i in range(Wm):
@@ -440,6 +480,17 @@ def run_gb(args, world, rank, local, pg):
         e2e_ms = max_over_ranks(pg, float(np.mean(e_ms)), dev if pg is not None else None)
     ctx.close()
 
+    # the metric's curve: the payload sweep, on the default line at N = 1
+    sweep = None
+    if (not args.roofline_only and not args.no_sweep and world == 1 and args.workload == "c2"
+            and not (args.dtype or args.op or args.islands or args.block or args.n or args.codec or args.ef
+                     or args.sharded or args.no_graphs or args.chunk_kib is not None)):
+        del pristine, bufs
+        torch.cuda.empty_cache()
+        t0 = time.perf_counter()
+        rows = sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps=min(K, 20))
+        sweep = sweep_line_object(rows, peak, peak_kind, link_peak, time.perf_counter() - t0)
+
     value = world * n * b / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
@@ -471,7 +522,8 @@ def run_gb(args, world, rank, local, pg):
            if ks else {}),
         "kernels_ms": {names[0]: k1_ms, "bridge_hop": bridge_ms, names[1]: k2_ms,
                        "region": "timed region 2: one bridge hop per call, CUDA events around each phase",
-                       "step_ms_with_marks": plain_ms},
+                       "step_ms_with_marks": plain_ms, "step_ms_without_marks": nomark_ms,
+                       "marks_cost_ms": plain_ms - nomark_ms},
         "kernels_hbm_frac": {names[0]: k1_bytes / (k1_ms * 1e-3) / 1e9 / peak,
                              names[1]: k2_bytes / (k2_ms * 1e-3) / 1e9 / peak},
         "bridge": {"bytes_per_step": link_bytes, "ms": bridge_ms,
@@ -485,6 +537,7 @@ def run_gb(args, world, rank, local, pg):
         "timed_wall_s": t_wall,
         "clocks": clk,
         **({"host_call_us": host_us} if host_us else {}),
+        **({"sweep": sweep} if sweep else {}),
     }
     return line, w, xs, codec
 
@@ -721,34 +774,76 @@ def run_buckets_bench(args, world, rank, local, pg):
     }
 
 
-def run_sweep(args, local):
-    """Payload sweep (workload c3): 4 KiB .. 256 MiB of float32 per rank at
-    2 islands x 2 ranks, codecs none / bf16 / e4m3; one JSON line per row.
-    Per row: the step as run by default (pipelined graph, no marks) for the
-    algorithm GB/s; one-hop steps with phase marks for the kernels inside a
-    step and the bridge's fraction of pinned copy bandwidth; and each kernel
-    back to back (kernel_stream) for the HBM roofline fractions.
-    L2 is flushed (write then clean read) before every timed step."""
+SWEEP_COLUMNS = ["bytes_per_rank", "codec", "steps", "ms_per_step", "algbw_gbs", "encode_frac", "decode_frac",
+                 "encode_frac_in_step", "decode_frac_in_step", "bridge_gbs", "bridge_frac", "floor_ms"]
+
+
+def op_floor_ms(ctx, bufs, I, P, codec, block, op, stream, flush, clean, reps=50):
+    """The sum of a one-chunk step's operations, each timed on its own on the
+    device (CUDA events around it, L2 flushed before it as before a step,
+    after a spin so the host is ahead): the encode launch, the bridge's
+    device -> host and host -> device copies of the step's sizes, the decode
+    launch; minus one event pair per extra measurement (each one carries the
+    cost of its own two events).  Host buffers are pinned.  Returns (floor,
+    parts) in milliseconds."""
+    import torch
+    dev = bufs[0].device
+    nbytes = I * P
+    hb = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    pays = [torch.empty(P, dtype=torch.uint8, device=dev) for _ in range(I)]
+    rows = [pays[j] for g in range(I) for j in range(I)]
+
+    def each(fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            fn()
+            torch.cuda.synchronize()
+            torch.cuda._sleep(20_000_000)
+            for a, b in evs:
+                flush.zero_()
+                clean.amax()
+                a.record(stream)
+                fn()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in evs]))
+
+    parts = {"events": each(lambda: None),
+             "encode": each(lambda: ctx.island_reduce_compress(bufs, codec, block, pays, stream=stream)),
+             "copies": each(lambda: (hb.copy_(db, non_blocking=True), db.copy_(hb, non_blocking=True))),
+             "decode": each(lambda: ctx.decompress_island_broadcast(rows, op, codec, block, bufs, stream=stream))}
+    return parts["encode"] + parts["copies"] + parts["decode"] - 2 * parts["events"], parts
+
+
+def sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps, emit=None):
+    """The payload sweep (workload c3): 4 KiB .. 256 MiB of float32 per rank
+    at 2 islands x 2 ranks, U(-1, 1), SUM, codecs none / bf16 / e4m3.  Per
+    row: the step as a user runs it (pipelined policy, graph replay, no phase
+    marks; L2 flushed before each timed step) for the algorithm GB/s; each
+    kernel back to back over distinct input sets (kernel_stream) for the HBM
+    roofline fractions; one-hop steps with phase marks for the kernels inside
+    a step and the bridge against pinned copy bandwidth; and, up to 1 MiB,
+    the sum of the step's operations timed one by one (op_floor_ms).  Rank
+    buffers are drawn on the device (torch.Generator seeded per rank).
+    Returns compact rows (SWEEP_COLUMNS); emit(row_dict) gets each row's
+    details as it is measured."""
     import torch
     from cross_vendor_gradient_gb300 import Context, payload_bytes
     from cross_vendor_gradient_gb300 import workloads as wl
-    from cross_vendor_gradient_gb300 import build as gbuild
-
-    gbuild.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
     w = wl.WORKLOADS["c3"]
     W, I = w.world_size, len(w.island_sizes)
     peak, peak_kind = measured_peaks()
-    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
     codecs = [args.codec] if args.codec else list(w.codecs)
+    chunk = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
+    rows = []
     for lg in wl.SWEEP_LOG2:
         n = 1 << lg
         pristine = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), dev, torch.float32) for r in range(W)]
         bufs = [p.clone() for p in pristine]
-        K = max(5, min(args.steps, int(4e9 // (n * 4 * W))))
+        K = max(5, min(max_steps, int(4e9 // (n * 4 * W))))
+        Pmax = max(payload_bytes(c, w.block, n) for c in codecs)
+        sets = make_sets(pristine, I, Pmax, stream_set_count(W * n * 4 + I * Pmax))
         for codec in codecs:
             ctx = Context(w.island_sizes)
             ctx.reserve(n, torch.float32, codec, w.block)
@@ -770,38 +865,65 @@ def run_sweep(args, local):
                 torch.cuda.synchronize()
                 return float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(count)])) if timed else 0.0
 
-            chunk = 2 << 20 if args.chunk_kib is None else args.chunk_kib << 10
             ctx.set_pipeline(chunk, True)
-            steps(max(3, args.warmup), False)
+            steps(3, False)
             ms = steps(K, True)
             ctx.set_pipeline(0, False)
             ctx.set_phase_timing(K)
-            steps(3, False)
+            steps(2, False)
             plain = steps(K, True)
             ph = np.array([ctx.phase_times(a) for a in range(K)])
             ctx.set_phase_timing(0)
             k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
             P = payload_bytes(codec, w.block, n)
             b1, b2 = alg_bytes(W, I, n, 4, P)
-            ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, 2,
-                               max(3, min(20, int(2e9 // (n * 4 * W)))))
+            ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, 1,
+                               max(3, min(10, int(2e9 // (n * 4 * W)))), sets=sets)
+            floor = parts = None
+            if n * 4 <= (1 << 20):
+                floor, parts = op_floor_ms(ctx, bufs, I, P, codec, w.block, w.op, stream, flush, clean)
             ctx.close()
             s1, s2 = ks["k_reduce_encode"], ks["k_decode_bcast"]
-            print(json.dumps({
-                "metric": METRIC, "sweep_row": True, "workload": "c3", "codec": codec, "n": n,
-                "bytes_per_rank": 4 * n, "value": 4 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-                "steps": K, "one_hop_ms_per_step": plain,
-                "hbm_frac": {"k_reduce_encode": b1 / (s1 * 1e-3) / 1e9 / peak,
-                             "k_decode_bcast": b2 / (s2 * 1e-3) / 1e9 / peak, "peak_gbs": peak,
-                             "peak_kind": peak_kind,
-                             "region": "each kernel back to back over %d distinct input sets" % ks["sets"]},
-                "kernels_stream_ms": {"k_reduce_encode": s1, "k_decode_bcast": s2},
-                "in_step_hbm_frac": {"k_reduce_encode": b1 / (k1 * 1e-3) / 1e9 / peak,
-                                     "k_decode_bcast": b2 / (k2 * 1e-3) / 1e9 / peak},
-                "kernels_ms": {"k_reduce_encode": k1, "bridge_hop": br, "k_decode_bcast": k2},
-                "bridge_gbs": (I * P + I * (I - 1) * P) / (br * 1e-3) / 1e9 if br > 0 else None,
-            }), flush=True)
-        del pristine, bufs
+            link_bytes = I * P + I * (I - 1) * P
+            bridge = link_bytes / (br * 1e-3) / 1e9 if br > 0 else None
+            row = [4 * n, codec, K, ms, 4 * n / (ms * 1e-3) / 1e9, b1 / (s1 * 1e-3) / 1e9 / peak,
+                   b2 / (s2 * 1e-3) / 1e9 / peak, b1 / (k1 * 1e-3) / 1e9 / peak, b2 / (k2 * 1e-3) / 1e9 / peak,
+                   bridge, bridge / link_peak if bridge else None, floor]
+            rows.append([float('%.6g' % v) if isinstance(v, float) else v for v in row])
+            if emit:
+                emit({"metric": METRIC, "sweep_row": True, "workload": "c3", "codec": codec, "n": n,
+                      "bytes_per_rank": 4 * n, "value": row[4], "unit": "GB/s", "ms_per_step": ms, "steps": K,
+                      "one_hop_ms_per_step": plain,
+                      "hbm_frac": {"k_reduce_encode": row[5], "k_decode_bcast": row[6], "peak_gbs": peak,
+                                   "peak_kind": peak_kind,
+                                   "region": "each kernel back to back over %d distinct input sets" % ks["sets"]},
+                      "kernels_stream_ms": {"k_reduce_encode": s1, "k_decode_bcast": s2},
+                      "in_step_hbm_frac": {"k_reduce_encode": row[7], "k_decode_bcast": row[8]},
+                      "kernels_ms": {"k_reduce_encode": k1, "bridge_hop": br, "k_decode_bcast": k2},
+                      "bridge_gbs": bridge, "bridge_frac": row[10],
+                      **({"floor_ms": floor, "floor_parts_ms": parts} if floor is not None else {})})
+        del pristine, bufs, sets
+        torch.cuda.empty_cache()
+    return rows
+
+
+def sweep_line_object(rows, peak, peak_kind, link_peak, wall_s):
+    """The sweep as one compact object of the bench line."""
+    return {"workload": "c3: 4 simulated ranks as islands [2, 2], float32 U(-1, 1) per rank, SUM, "
+                        "4 KiB .. 256 MiB per rank in powers of two, codecs none / bf16 / e4m3 block 256",
+            "columns": SWEEP_COLUMNS, "rows": rows,
+            "notes": {"ms_per_step": "the step as a user runs it (pipelined policy, CUDA graph replay), L2 flushed "
+                                     "before each timed step, CUDA events around the step",
+                      "algbw_gbs": "bytes of one rank buffer / step time",
+                      "encode_frac, decode_frac": "algorithmic HBM bytes / back-to-back launch time / %.1f GB/s "
+                                                  "(%s HBM copy peak)" % (peak, peak_kind),
+                      "*_in_step": "the same kernels inside one-hop steps with CUDA events around each phase",
+                      "bridge_gbs, bridge_frac": "one-hop device->host + host->device bytes / bridge time, and "
+                                                 "its fraction of min(D2H, H2D) pinned copy bandwidth %.1f GB/s"
+                                                 % link_peak,
+                      "floor_ms": "rows up to 1 MiB: encode + copies + decode, each timed alone after an L2 "
+                                  "flush, minus the extra event pairs"},
+            "wall_s": wall_s}
 
 
 def run_reference(args, world, rank, pg):
@@ -984,7 +1106,17 @@ def main():
         return
     if args.sweep:
         if rank == 0:
-            run_sweep(args, local)
+            import torch
+            from cross_vendor_gradient_gb300 import build as gbuild
+            gbuild.build()
+            torch.cuda.set_device(local)
+            dev = torch.device("cuda", local)
+            stream = torch.cuda.Stream(device=dev)
+            flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+            clean = torch.zeros(FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
+            link = pinned_link(dev, stream)
+            sweep_rows(args, dev, stream, flush, clean, min(link["d2h_gbs"], link["h2d_gbs"]), args.steps,
+                       emit=lambda d: print(json.dumps(d), flush=True))
         if pg is not None:
             pg.destroy_process_group()
         return

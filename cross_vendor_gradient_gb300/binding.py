@@ -33,6 +33,7 @@ GB_MAX_ISLANDS = 8
 GB_N_PHASES = 3
 GB_INJECT_BRIDGE = 1
 GB_INJECT_ALLOC = 2
+GB_INJECT_OTHER_DEVICE = 3
 GB_NOALLOC_DEVICE_BYTES = 64 << 20
 GB_NOALLOC_HOST_BYTES = 32 << 20
 

@@ -839,7 +839,8 @@ gb_status gb_phase_times(gb_ctx *c, int age, float *ms) {
 gb_status gb_last_phase_times(gb_ctx *c, float *ms) { return gb_phase_times(c, 0, ms); }
 
 gb_status gb_debug_inject(gb_ctx *c, int what) {
-    if (!c || (what != 0 && what != GB_INJECT_BRIDGE && what != GB_INJECT_ALLOC)) return GB_ERR_INVALID_ARG;
+    if (!c || (what != 0 && what != GB_INJECT_BRIDGE && what != GB_INJECT_ALLOC && what != GB_INJECT_OTHER_DEVICE))
+        return GB_ERR_INVALID_ARG;
     c->inject = what;
     return GB_OK;
 }

@@ -165,6 +165,7 @@ gb_status check_codec(gb_ctx *c, int codec, int block);
 gb_status check_n(gb_ctx *c, size_t n);
 gb_status check_dev_bufs(gb_ctx *c, const void *const *bufs, int count, const char *name);
 gb_status check_dev_ptr(gb_ctx *c, const void *p, const char *name);
+int seen_device(gb_ctx *c, int dev);
 gb_status bind(gb_ctx *c);
 gb_status begin(gb_ctx *c, cudaStream_t s);
 gb_status end(gb_ctx *c, cudaStream_t s);

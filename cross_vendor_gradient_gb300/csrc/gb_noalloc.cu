@@ -16,14 +16,9 @@
 //     for the host, like the pageable default of the pages' bridge).
 // It produces the same bits as gb_all_reduce (same kernels, same payload
 // layout per island, same island order).
-#include <cstring>
 #include <mutex>
 
-#include <cuda_runtime.h>
-
-#include "gb.h"
-#include "gb_device.cuh"
-#include "gb_kernels.cuh"
+#include "gb_internal.cuh"
 
 namespace {
 
@@ -53,66 +48,61 @@ gb_status scratch_address(int dev, unsigned char **out) {
     return GB_OK;
 }
 
-size_t payload_bytes_of(int codec, int block, size_t n) {
-    switch (codec) {
-    case GB_CODEC_NONE: return 4 * n;
-    case GB_CODEC_BF16: return 2 * n;
-    default: return gb::round_up(n, 16) + 4 * ((n + block - 1) / block);
-    }
-}
-
-bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
+// The host slots hold I payload slots and the device array I * I: the
+// device bound keeps I * slot <= GB_NOALLOC_DEVICE_BYTES / I, within the host
+// array for every I >= 2, so one size check covers both.
+static_assert(2ull * GB_NOALLOC_HOST_BYTES >= GB_NOALLOC_DEVICE_BYTES, "host slots smaller than the device bound");
 
 }  // namespace
 
 extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, size_t n,
                                            gb_dtype dtype, gb_op op, gb_codec codec, int block,
                                            gb_stream stream) {
-    // ---- validation: the same rules as gb_all_reduce, plus the size limit
-    if (!ctx) return GB_ERR_INVALID_ARG;
-    if (gb_context_status(ctx) != GB_OK) return GB_ERR_CONTEXT_FAILED;
-    if (dtype != GB_F32 && dtype != GB_BF16) return GB_ERR_UNSUPPORTED_DTYPE;
-    if (op != GB_SUM && op != GB_AVG) return GB_ERR_UNSUPPORTED_OP;
-    if (gb_payload_bytes(codec, block, 1) == 0) return GB_ERR_UNSUPPORTED_CODEC;
-    const int I = gb_n_islands(ctx), W = gb_world_size(ctx);
-    if (!rank_bufs) return GB_ERR_INVALID_ARG;
-    for (int r = 0; r < W; ++r) {
-        if (!rank_bufs[r]) return GB_ERR_INVALID_ARG;
-        if (!aligned32(rank_bufs[r])) return GB_ERR_MISALIGNED;
-    }
+    // ---- validation: the checks of gb_all_reduce (arguments first, the
+    // device after them), restricted to the codec path, plus the size limit
+    using namespace gbrt;
+    GB_TRY(check_ctx(ctx));
+    GB_TRY(check_codec_dtype(ctx, dtype));
+    if (op != GB_SUM && op != GB_AVG) return set_msg(ctx, GB_ERR_UNSUPPORTED_OP, "noalloc all_reduce takes SUM / AVG");
+    GB_TRY(check_codec(ctx, codec, block));
+    GB_TRY(check_n(ctx, n));
+    const int I = ctx->I, W = ctx->W;
+    GB_TRY(check_dev_bufs(ctx, (const void *const *)rank_bufs, W, "rank_bufs"));
     if (n == 0) return GB_OK;
     const int eff = I == 1 ? GB_CODEC_NONE : (int)codec;
-    const int blk = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? block : 256;
-    const size_t P = payload_bytes_of(eff, blk, n);
-    const size_t slot = gb::round_up(P, 256);
+    const int blk = is_fp8(eff) ? block : 256;
+    const size_t P = payload_bytes(eff, blk, n);
+    const size_t slot = round_up(P, 256);
     // own payloads (I slots), then each leader's received payloads (I - 1 slots each)
-    if (n > (size_t)GB_NOALLOC_DEVICE_BYTES || slot > GB_NOALLOC_DEVICE_BYTES / ((size_t)I * I) ||
-        (I > 1 && slot > GB_NOALLOC_HOST_BYTES / (size_t)I))
-        return GB_ERR_TOO_LARGE;
+    if (slot > GB_NOALLOC_DEVICE_BYTES / ((size_t)I * I))
+        return set_msg(ctx, GB_ERR_TOO_LARGE, "%d x %d payload slots of %zu bytes exceed the fixed %u bytes", I, I,
+                       slot, (unsigned)GB_NOALLOC_DEVICE_BYTES);
 
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        return GB_ERR_NO_DEVICE;
+        return set_msg(ctx, GB_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
     }
+    dev = seen_device(ctx, dev);
+    if (ctx->device >= 0 && dev != ctx->device)
+        return set_msg(ctx, GB_ERR_INVALID_ARG, "context is bound to device %d, current device is %d", ctx->device,
+                       dev);
     unsigned char *scratch = nullptr;
-    gb_status st = scratch_address(dev, &scratch);
-    if (st != GB_OK) return st;
+    if (scratch_address(dev, &scratch) != GB_OK)
+        return set_msg(ctx, GB_ERR_CUDA, "cudaGetSymbolAddress of the fixed staging array failed");
     cudaStream_t s = (cudaStream_t)stream;
-    int first[GB_MAX_ISLANDS + 1];
-    for (int i = 0; i < I; ++i) first[i] = gb_island_first_rank(ctx, i);
-    first[I] = W;
 
     // ---- island reduce + encode into the own-payload slots
     gb::ReduceEncodeArgs ra;
     memset(&ra, 0, sizeof ra);
     for (int r = 0; r < W; ++r) ra.src[r] = rank_bufs[r];
     for (int i = 0; i < I; ++i) ra.payload[i] = scratch + (size_t)i * slot;
-    for (int i = 0; i <= I; ++i) ra.first[i] = first[i];
+    for (int i = 0; i <= I; ++i) ra.first[i] = ctx->first[i];
     ra.n_islands = I;
     ra.n = n;
     ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
-    ra.scales_off = (eff == GB_CODEC_E4M3 || eff == GB_CODEC_E5M2) ? gb::round_up(n, 16) : P;
+    ra.scales_off = is_fp8(eff) ? round_up(n, 16) : P;
     if (gb::launch_reduce_encode(ra, dtype, eff, blk, s) != cudaSuccess) return GB_ERR_CUDA;
 
     // ---- bridge hop through the host slots: own slots out, others' in
@@ -138,7 +128,7 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
     memset(&da, 0, sizeof da);
     for (int r = 0; r < W; ++r) {
         da.dst[r] = rank_bufs[r];
-        da.group_of_rank[r] = gb_island_of_rank(ctx, r);
+        da.group_of_rank[r] = ctx->island_of[r];
     }
     const void *received[GB_MAX_ISLANDS];
     for (int j = 0; j < I; ++j) {

@@ -105,6 +105,16 @@ gb_status check_dev_ptr(gb_ctx *c, const void *p, const char *name) {
 }
 
 
+// The current device `dev` as this call sees it: GB_INJECT_OTHER_DEVICE
+// makes one call of a bound context see another device (a test of the
+// mismatch refusal that needs no second GPU); unbound, the injection is
+// dropped.
+int seen_device(gb_ctx *c, int dev) {
+    if (c->inject != GB_INJECT_OTHER_DEVICE) return dev;
+    c->inject = 0;
+    return c->device >= 0 ? c->device + 1 : dev;
+}
+
 // Bind the context to the current device on first use (creates its streams
 // and events there).
 gb_status bind(gb_ctx *c) {
@@ -114,6 +124,7 @@ gb_status bind(gb_ctx *c) {
         cudaGetLastError();
         return set_msg(c, GB_ERR_NO_DEVICE, "no CUDA device: %s", cudaGetErrorString(e));
     }
+    dev = seen_device(c, dev);
     if (c->device < 0) {
         if ((e = cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming)) != cudaSuccess)
             return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);

@@ -464,9 +464,14 @@ gb_status gb_last_phase_times(gb_ctx *ctx, float *ms /* [GB_N_PHASES] */);
  *     copies (the call returns GB_ERR_BRIDGE, no rank buffer is written,
  *     the context becomes failed);
  *   GB_INJECT_ALLOC: the next staging allocation fails (GB_ERR_ALLOC, the
- *     context becomes failed). */
+ *     context becomes failed);
+ *   GB_INJECT_OTHER_DEVICE: the next call of a context already bound to a
+ *     device sees a current device other than that one, as a caller that
+ *     switched devices would (GB_ERR_INVALID_ARG with nothing enqueued; not
+ *     sticky).  Without a bound device it has no effect and is dropped. */
 #define GB_INJECT_BRIDGE 1
 #define GB_INJECT_ALLOC 2
+#define GB_INJECT_OTHER_DEVICE 3
 gb_status gb_debug_inject(gb_ctx *ctx, int what);
 
 /* ------------------------------------------- all_reduce without allocation
@@ -488,10 +493,14 @@ gb_status gb_debug_inject(gb_ctx *ctx, int what);
  *     calling thread until the first kernel and the copy have finished.
  * Limits: with I islands and P = gb_payload_bytes(codec, block, n) (the
  * float32 sum, 4n, when I == 1), I * I * round_up(P, 256) must fit the
- * device array and I * round_up(P, 256) the host array; larger calls return
- * GB_ERR_TOO_LARGE with nothing enqueued.  It covers the codec path only
- * (float32 / bfloat16 rank buffers, SUM / AVG); other arguments are checked
- * as in gb_all_reduce.
+ * device array; larger calls return GB_ERR_TOO_LARGE with nothing enqueued.
+ * (The host array holds I * round_up(P, 256), which that bound already keeps
+ * within GB_NOALLOC_HOST_BYTES for every I >= 2.)  It covers the codec path
+ * only (float32 / bfloat16 rank buffers, SUM / AVG); the other arguments are
+ * checked as in gb_all_reduce, the device included: a context already bound
+ * to a device (by an earlier call of another entry point) refuses a call
+ * made with another device current (GB_ERR_INVALID_ARG), and an unbound
+ * context takes the current device without being bound by this call.
  * Sharing: every call in the process uses the same two arrays, which keep
  * the last call's contents; nothing in them needs to start at zero (each
  * call reads only what it wrote).  Calls that overlap on the GPU -- from

@@ -162,6 +162,23 @@ def test_argument_errors_need_no_device():
         assert B.gb_context_status(ctx) == B.GB_OK
         assert B.gb_last_error(ctx) == B.GB_ERR_MISALIGNED  # the last refused call: the misaligned bucket set
         assert B.gb_debug_inject(ctx, 77) == B.GB_ERR_INVALID_ARG
+        # the fixed-buffer all_reduce checks its arguments the same way, before any device call
+        na = B.gb_all_reduce_noalloc
+        assert na(0, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        assert na(ctx, fake, 10, B.GB_F64, 0, 0, 256) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert na(ctx, fake, 10, 0, B.GB_MAX, 0, 256) == B.GB_ERR_UNSUPPORTED_OP
+        assert na(ctx, fake, 10, 0, 0, 2, 64) == B.GB_ERR_UNSUPPORTED_CODEC
+        assert na(ctx, fake[:3] + [0], 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        assert na(ctx, fake[:3] + [0x10008], 10, 0, 0, 0, 256) == B.GB_ERR_MISALIGNED
+        assert na(ctx, fake, 1 << 39, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
+        # 2 x 2 slots of 4n bytes beyond the fixed array: refused from the sizes alone
+        assert na(ctx, fake, B.GB_NOALLOC_DEVICE_BYTES // 16 + 256, 0, 0, 0, 256) == B.GB_ERR_TOO_LARGE
+        assert "exceed" in B.gb_last_error_message(ctx)
+        assert na(ctx, fake, 0, 0, 0, 2, 256) == B.GB_OK
+        # the device-mismatch hook is accepted; on an unbound context it is dropped
+        assert B.gb_debug_inject(ctx, B.GB_INJECT_OTHER_DEVICE) == B.GB_OK
+        assert B.gb_debug_inject(ctx, 0) == B.GB_OK
+        assert B.gb_context_status(ctx) == B.GB_OK
     finally:
         B.gb_destroy(ctx)
 

@@ -54,6 +54,23 @@ def test_default_line_contract():
     assert d["gpu_launches"] == 20 * 8  # 4 chunks x (encode + decode) per graph-replayed step
     c = d["clocks"]
     assert c["sm_mhz"] > 0 and isinstance(c["reasons"], list)
+    k = d["kernels_ms"]  # one-hop steps with and without the phase marks' events
+    assert k["step_ms_with_marks"] > 0 and k["step_ms_without_marks"] > 0
+    # the metric's curve: 17 payload sizes x 3 codecs of the c3 sweep
+    sw = d["sweep"]
+    cols = sw["columns"]
+    assert cols[:5] == ["bytes_per_rank", "codec", "steps", "ms_per_step", "algbw_gbs"]
+    rows = [dict(zip(cols, row)) for row in sw["rows"]]
+    assert len(rows) == 51
+    assert sorted({r["bytes_per_rank"] for r in rows}) == [4096 << k for k in range(17)]
+    for size in {r["bytes_per_rank"] for r in rows}:
+        assert sorted(r["codec"] for r in rows if r["bytes_per_rank"] == size) == ["bf16", "e4m3", "none"]
+    for r in rows:
+        assert r["ms_per_step"] > 0 and r["steps"] >= 5
+        assert abs(r["algbw_gbs"] - r["bytes_per_rank"] / (r["ms_per_step"] * 1e-3) / 1e9) < 1e-3 * r["algbw_gbs"]
+        assert 0 < r["encode_frac"] < 1.3 and 0 < r["decode_frac"] < 1.3
+        assert 0 < r["bridge_frac"] < 1.3
+        assert (r["floor_ms"] is not None) == (r["bytes_per_rank"] <= 1 << 20)
 
 
 def test_reference_arm_contract():

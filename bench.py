@@ -229,24 +229,55 @@ def make_sets(pristine, I, P, S, ef=False):
             if ef else None}
 
 
+def b2b_ms(stream, clean, warm, batches, S, launch):
+    """Back-to-back launches, in steady state.  launch(q) enqueues one launch
+    on input set q.  Each batch starts from a clean L2 (a 256 MiB read) after
+    a ~0.4 ms GPU spin, so the host has queued the whole batch before its
+    first event.  A CUDA event between two launches takes away the second
+    one's programmatic early start, so the events sit after launch 0 and
+    after the batch's last launch, and two batch lengths are timed: S
+    launches (S - 1 after the first event) and 2 launches (1 after it).
+    Their difference is S - 2 launches of a long run of back-to-back
+    launches, without the start-up gap that follows the first event.
+    Returns milliseconds per launch: (steady, with the gap) where `with the
+    gap` is the long batch's window divided by S - 1."""
+    import torch
+    ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(batches)]
+    with torch.cuda.stream(stream):
+        for it in range(warm + batches):
+            e = ea[it - warm] if it >= warm else None
+            for count, (i0, i1) in ((S, (0, 1)), (2, (2, 3))):
+                clean.amax()
+                torch.cuda._sleep(800_000)
+                for q in range(count):
+                    launch(q)
+                    if e and q == 0:
+                        e[i0].record(stream)
+                if e:
+                    e[i1].record(stream)
+    torch.cuda.synchronize()
+    long_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ea]))
+    short_ms = float(np.mean([e[2].elapsed_time(e[3]) for e in ea]))
+    return (long_ms - short_ms) / (S - 2), long_ms / (S - 1)
+
+
 def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, batches,
-                  names=("k_reduce_encode", "k_decode_bcast"), ef=False, sets=None):
-    """Timed region 3: each kernel launched back to back, as the fused halves
-    of the path (gb_island_reduce_compress, gb_decompress_island_broadcast),
-    with the same grid as in a step.  S distinct input sets, outputs and
-    payloads (together at least 4 x L2 when a set is large, else 16 sets) are
-    cycled.  Each batch (S encodes, then S decodes) starts from a clean L2
-    (256 MiB read) after a ~0.4 ms GPU spin, so the host has queued the whole
-    batch before its first event; each kernel's first launch of the batch is
-    untimed and CUDA events on the launching stream bracket the other S - 1.
-    So no launch finds its inputs in L2: the decode batch starts after the
-    payloads have been evicted, as payloads landed by the bridge's copies
-    are read from HBM in a step.  Every timed launch also writes back what
-    its predecessor left dirty in L2: the steady state of a stream of
-    buckets.  Returns per-launch milliseconds of both kernels.  ef: the
-    encode carries error feedback (gb_island_reduce_compress_ef, one float32
-    residual per island and set).  sets: prebuilt make_sets() buffers (their
-    payloads at least P bytes), reused across calls."""
+                  names=("k_reduce_encode", "k_decode_bcast"), ef=False, sets=None, scatter=False):
+    """Timed region 3: each kernel launched back to back (b2b_ms), as the
+    fused halves of the path (gb_island_reduce_compress_op, then
+    gb_decompress_island_broadcast, or gb_decompress_scatter for
+    reduce_scatter), with the same grid as in a step.  S distinct input
+    sets, outputs and payloads (together at least 4 x L2 when a set is
+    large, else 16 sets) are cycled, so no launch finds its inputs in L2:
+    the decode batch starts after the payloads have been evicted, as
+    payloads landed by the bridge's copies are read from HBM in a step.
+    Every timed launch also writes back what its predecessor left dirty in
+    L2: the steady state of a stream of buckets.  Returns per-launch
+    milliseconds of both kernels.  ef: the encode carries error feedback
+    (gb_island_reduce_compress_ef, one float32 residual per island and
+    set).  sets: prebuilt make_sets() buffers (their payloads at least P
+    bytes), reused across calls.  The op selects the codec path or the exact
+    path (MAX / MIN, other dtypes)."""
     import torch
     W = len(pristine)
     n = pristine[0].numel()
@@ -256,36 +287,28 @@ def kernel_stream(ctx, pristine, I, P, codec, block, op, stream, clean, warm, ba
         sets = make_sets(pristine, I, P, stream_set_count(set_bytes), ef)
     S = sets["S"]
     ins, outs, pays, res = sets["ins"], sets["outs"], sets["pays"], sets["res"]
+    if scatter:
+        outs = [[o[: n // W] for o in row] for row in outs]
     # every leader's row holds the same I payloads: the call decodes them
     # once and writes all ranks, as the decode in a step does
     rows = [[pays[q][j] for g in range(I) for j in range(I)] for q in range(S)]
-    ea = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(batches)]
-    with torch.cuda.stream(stream):
-        for it in range(warm + batches):
-            e = ea[it - warm] if it >= warm else None
-            clean.amax()
-            torch.cuda._sleep(800_000)
-            for q in range(S):
-                if ef:
-                    ctx.island_reduce_compress_ef(ins[q], res[q], codec, block, pays[q], stream=stream)
-                else:
-                    ctx.island_reduce_compress(ins[q], codec, block, pays[q], stream=stream)
-                if e and q == 0:
-                    e[0].record(stream)
-            if e:
-                e[1].record(stream)
-            clean.amax()  # evict the payloads: the decodes read them from HBM
-            torch.cuda._sleep(800_000)
-            for q in range(S):
-                ctx.decompress_island_broadcast(rows[q], op, codec, block, outs[q], stream=stream)
-                if e and q == 0:
-                    e[2].record(stream)
-            if e:
-                e[3].record(stream)
-    torch.cuda.synchronize()
-    return {"sets": S, "timed_launches_per_batch": S - 1, "batches": batches, "set_bytes": set_bytes,
-            names[0]: float(np.mean([e[0].elapsed_time(e[1]) for e in ea])) / (S - 1),
-            names[1]: float(np.mean([e[2].elapsed_time(e[3]) for e in ea])) / (S - 1)}
+
+    def enc(q):
+        if ef:
+            ctx.island_reduce_compress_ef(ins[q], res[q], codec, block, pays[q], stream=stream)
+        else:
+            ctx.island_reduce_compress_op(ins[q], op, codec, block, pays[q], stream=stream)
+
+    def dec(q):
+        if scatter:
+            ctx.decompress_scatter(rows[q], n, op, codec, block, outs[q], stream=stream)
+        else:
+            ctx.decompress_island_broadcast(rows[q], op, codec, block, outs[q], stream=stream)
+
+    t1, g1 = b2b_ms(stream, clean, warm, batches, S, enc)
+    t2, g2 = b2b_ms(stream, clean, warm, batches, S, dec)  # the payloads were written by the encodes
+    return {"sets": S, "timed_launches_per_batch": S - 2, "batches": batches, "set_bytes": set_bytes,
+            names[0]: t1, names[1]: t2, "with_first_gap": {names[0]: g1, names[1]: g2}}
 
 
 def pinned_link(dev, stream, big=256 << 20):
@@ -444,15 +467,16 @@ def run_gb(args, world, rank, local, pg):
 
     # ---- timed region 3: each kernel back to back (see kernel_stream)
     ks = None
-    if not exact and I > 1:
+    if I > 1:  # the codec path's kernels, or the exact path's (MAX / MIN, other dtypes)
         ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, Wm, max(3, min(Kr, 50)),
                            names, ef=ef)
         S, set_bytes = ks["sets"], ks["set_bytes"]
     if ks:
         r1, r2 = ks[names[0]], ks[names[1]]
         region = ("timed region 3: each kernel launched back to back over %d input sets (%.0f MB each, "
-                  "distinct, from a clean L2); CUDA events around the last %d launches of each batch"
-                  % (S, set_bytes / 1e6, S - 1))
+                  "distinct, from a clean L2); CUDA events after the first and the last launch of batches of "
+                  "%d and of 2 launches, the difference over %d launches"
+                  % (S, set_bytes / 1e6, S, S - 2))
     else:
         r1, r2 = k1_ms, k2_ms
         region = "timed region 2: one bridge hop per call, CUDA events around each phase"
@@ -580,7 +604,7 @@ def host_call_us(ctx, bufs, pristine, op, codec, block, stream, calls=200):
     return out
 
 
-KERNEL_SOURCES = ("gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_device.cuh", "gb_kernels.cuh")
+KERNEL_SOURCES = ("gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_kernels_exact.cu", "gb_device.cuh", "gb_kernels.cuh")
 
 
 def kernel_source_sha():
@@ -630,7 +654,7 @@ def run_buckets_bench(args, world, rank, local, pg):
     # reduce_scatter slices of whole 8-element vectors: buckets padded to 8 * W elements
     _, _, bn = bucket_plan(numels, w.elem_bytes, wl.BUCKET_CAP_BYTES, 8 * W if rs_ag else 1)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-    pristine = [[wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 1000 * bi, dev, tdt) for r in range(W)]
+    pristine = [[wl.draw_device(w.dist, nb, wl.bucket_seed(w.cid, bi, r), dev, tdt) for r in range(W)]
                 for bi, nb in enumerate(bn)]
     bufs = [[x.clone() for x in row] for row in pristine]
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -977,10 +1001,11 @@ def run_collective(args, world, rank, local, pg):
     reduce_scatter: n elements per rank in, n / W out (the codec applies);
     all_gather: n / W in, n out (exact); broadcast: n in place from rank 0
     (exact).  value = n * b / step time (bytes of one full rank buffer).  The
-    kernels' HBM fractions come from one-hop calls with phase marks, with the
-    algorithmic bytes of each collective: reduce_scatter encode W*n*b + I*P,
-    decode I*P + n*b; all_gather copy W*m*b read + W*W*m*b written (m = n /
-    W); broadcast copy n*b read + (W - 1)*n*b written."""
+    kernels' HBM fractions come from their launches back to back (the
+    roofline; timed region 3) and from one-hop calls with phase marks, with
+    the algorithmic bytes of each collective: reduce_scatter encode
+    W*n*b + I*P, decode I*P + n*b; all_gather copy W*m*b read + W*W*m*b
+    written (m = n / W); broadcast copy n*b read + (W - 1)*n*b written."""
     import torch
     from cross_vendor_gradient_gb300 import Context, kernel_launch_count, payload_bytes
     from cross_vendor_gradient_gb300 import workloads as wl
@@ -1053,7 +1078,7 @@ def run_collective(args, world, rank, local, pg):
     steps(3, False)
     one_hop = steps(Kr, True)
     ph = np.array([ctx.phase_times(a) for a in range(Kr)])
-    ctx.close()
+    ctx.set_phase_timing(0)
     k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
     P = payload_bytes(codec, w.block, n) if coll == "reduce_scatter" else m * b
     if coll == "reduce_scatter":
@@ -1065,8 +1090,40 @@ def run_collective(args, world, rank, local, pg):
     else:
         kern = [("k_copy", n * b + (W - 1) * n * b, k2)]
         link = n * b + (I - 1) * n * b
+
+    # ---- timed region 3: the collective's kernels back to back.
+    # reduce_scatter: the fused halves (encode, then the slice decode);
+    # all_gather / broadcast: the copy kernel alone, as the whole call of a
+    # one-island context over the same W ranks (no bridge, nothing else
+    # launched), algorithmic bytes W*m*b + W*W*m*b and n*b + (W-1)*n*b.
+    Kb = max(3, min(K, 20))
+    if coll == "reduce_scatter":
+        ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, 1, Kb,
+                           ("k_reduce_encode", "k_decode_bcast (slices)"), scatter=True)
+        b2b = [(k, nb, ks[k]) for k, nb, _ in kern]
+        sets_used = ks["sets"]
+    else:
+        one = Context((W,))
+        set_bytes = (W * m * b + W * n * b) if coll == "all_gather" else W * n * b
+        S = stream_set_count(set_bytes)
+        srcs = [[p.clone() for p in pristine] for _ in range(S)]
+        dsts = [[torch.empty(n, dtype=torch.float32, device=dev) for _ in range(W)] for _ in range(S)] \
+            if coll == "all_gather" else None
+
+        def launch(q):
+            if coll == "all_gather":
+                one.all_gather(srcs[q], dsts[q], stream=stream)
+            else:
+                one.broadcast(srcs[q], 0, stream=stream)
+
+        t, _ = b2b_ms(stream, clean, 1, Kb, S, launch)
+        one.close()
+        b2b = [("k_copy (one island of %d ranks)" % W, kern[0][1], t)]
+        sets_used = S
+        del srcs, dsts
+    ctx.close()
     peak, peak_kind = measured_peaks()
-    dom = max(kern, key=lambda t: t[2])
+    dom = max(b2b, key=lambda t: t[2])
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
     return {
         "metric": "%s algorithm GB/s and %% of GB300 HBM roofline" % coll, "value": world * n * b / (ms * 1e-3) / 1e9,
@@ -1086,8 +1143,12 @@ def run_collective(args, world, rank, local, pg):
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_launch": dom[1],
                      "avg_launch_ms": dom[2], "traffic": None,
-                     "region": "one bridge hop per call, CUDA events around each phase"},
-        "kernels": [{"kernel": k, "alg_bytes": nb, "ms": t, "hbm_frac": nb / (t * 1e-3) / 1e9 / peak}
+                     "region": "timed region 3: back to back over %d distinct input sets from a clean L2"
+                               % sets_used},
+        "kernels_stream": [{"kernel": k, "alg_bytes": nb, "ms": t, "hbm_frac": nb / (t * 1e-3) / 1e9 / peak}
+                           for k, nb, t in b2b],
+        "kernels": [{"kernel": k, "alg_bytes": nb, "ms": t, "hbm_frac": nb / (t * 1e-3) / 1e9 / peak,
+                     "region": "one bridge hop per call, CUDA events around each phase"}
                     for k, nb, t in kern],
         "bridge": {"bytes_per_step": link, "ms": br, "achieved_gbs": link / (br * 1e-3) / 1e9 if br > 0 else None},
         "one_hop_ms_per_step": one_hop, "gpu_launches": int(launches), "clocks": clk,

@@ -50,6 +50,13 @@ def payload_bytes(codec, block, n):
     return B.gb_payload_bytes(_codec(codec), block, n)
 
 
+def island_payload_bytes(dtype, op, codec, block, n):
+    """Bytes of one island's payload for any dtype and op (the exact path's
+    fold, or the codec's payload)."""
+    dt = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    return B.gb_island_payload_bytes(dt, _op(op), _codec(codec), block, n)
+
+
 def payload_scales_offset(codec, block, n):
     return B.gb_payload_scales_offset(_codec(codec), block, n)
 
@@ -248,6 +255,27 @@ class Context:
         self._check(B.gb_decompress_island_broadcast(self.handle, [p.data_ptr() for p in payloads],
                                                      tensors[0].numel(), dt, _op(op), _codec(codec), block,
                                                      [t.data_ptr() for t in tensors], _stream(stream)))
+
+    def island_reduce_compress_op(self, tensors, op, codec, block, payloads, stream=None):
+        """The first fused half for every dtype and op: the codec path's
+        encode, or the exact path's island fold (payloads of
+        island_payload_bytes bytes)."""
+        dt = _dtype(tensors)
+        self._check(B.gb_island_reduce_compress_op(self.handle, [t.data_ptr() for t in tensors],
+                                                   tensors[0].numel(), dt, _op(op), _codec(codec), block,
+                                                   [p.data_ptr() for p in payloads], _stream(stream)))
+
+    def decompress_scatter(self, payloads, n, op, codec, block, outputs, stream=None):
+        """reduce_scatter's second half: outputs[r] (n / W elements) receives
+        slice r of the decoded total.  payloads: I tensors (every leader holds
+        the same ones) or I * I."""
+        dt = _dtype(outputs)
+        I = len(self.island_sizes)
+        if len(payloads) == I and I > 1:
+            payloads = [p for _ in range(I) for p in payloads]
+        self._check(B.gb_decompress_scatter(self.handle, [p.data_ptr() for p in payloads], n, dt, _op(op),
+                                            _codec(codec), block, [t.data_ptr() for t in outputs],
+                                            _stream(stream)))
 
     # -------------------------------------------------------------- timing
     def set_phase_timing(self, capacity):

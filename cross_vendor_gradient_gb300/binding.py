@@ -67,6 +67,9 @@ SIGNATURES = {
     "gb_island_reduce_compress": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
     "gb_island_reduce_compress_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _P(_vp), _vp]),
     "gb_decompress_island_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
+    "gb_island_payload_bytes": (_sz, [_i, _i, _i, _i, _sz]),
+    "gb_island_reduce_compress_op": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
+    "gb_decompress_scatter": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _P(_vp), _vp]),
     "gb_all_reduce": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_all_reduce_ef": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
     "gb_reduce_scatter": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _i, _i, _i, _vp]),
@@ -217,6 +220,19 @@ def gb_island_reduce_compress_ef(ctx, rank_bufs, residuals, n, dtype, codec, blo
 def gb_decompress_island_broadcast(ctx, payloads, n, dtype, op, codec, block, rank_bufs, stream=0):
     return lib().gb_decompress_island_broadcast(ctx, _ptrs(payloads), n, dtype, op, codec, block,
                                                 _ptrs(rank_bufs), stream)
+
+
+def gb_island_payload_bytes(dtype, op, codec, block, n):
+    return lib().gb_island_payload_bytes(dtype, op, codec, block, n)
+
+
+def gb_island_reduce_compress_op(ctx, rank_bufs, n, dtype, op, codec, block, payloads, stream=0):
+    return lib().gb_island_reduce_compress_op(ctx, _ptrs(rank_bufs), n, dtype, op, codec, block, _ptrs(payloads),
+                                              stream)
+
+
+def gb_decompress_scatter(ctx, payloads, n, dtype, op, codec, block, out, stream=0):
+    return lib().gb_decompress_scatter(ctx, _ptrs(payloads), n, dtype, op, codec, block, _ptrs(out), stream)
 
 
 def gb_all_reduce(ctx, rank_bufs, n, dtype, op, codec, block, stream=0):

@@ -153,7 +153,7 @@ gb_status gb_island_reduce(gb_ctx *c, int island, const void *const *rank_bufs, 
     const int K = c->size[island];
     GB_TRY(check_codec_dtype(c, dtype));
     GB_TRY(check_n(c, n));
-    GB_TRY(check_dev_bufs(c, rank_bufs, K, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, rank_bufs, K, "rank_bufs"));
     GB_TRY(check_dev_ptr(c, island_sum, "island_sum"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
@@ -224,7 +224,7 @@ gb_status gb_island_broadcast(gb_ctx *c, int island, const float *total, size_t 
     if (op != GB_SUM && op != GB_AVG) return set_msg(c, GB_ERR_UNSUPPORTED_OP, "island broadcast takes SUM / AVG");
     GB_TRY(check_n(c, n));
     GB_TRY(check_dev_ptr(c, total, "total"));
-    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, K, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)rank_bufs, K, "rank_bufs"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
     gb::DecodeBcastArgs da;
@@ -256,7 +256,7 @@ static gb_status island_reduce_compress(gb_ctx *c, const void *const *rank_bufs,
     GB_TRY(check_codec_dtype(c, dtype));
     GB_TRY(check_codec(c, codec, block));
     GB_TRY(check_n(c, n));
-    GB_TRY(check_dev_bufs(c, rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, rank_bufs, c->W, "rank_bufs"));
     GB_TRY(check_dev_bufs(c, (const void *const *)payloads, c->I, "payloads"));
     if (res) GB_TRY(check_dev_bufs(c, (const void *const *)res, c->I, "residuals"));
     if (n == 0) return GB_OK;
@@ -288,24 +288,25 @@ gb_status gb_island_reduce_compress_ef(gb_ctx *c, const void *const *rank_bufs, 
     return island_reduce_compress(c, rank_bufs, residuals, n, dtype, codec, block, payloads, stream);
 }
 
-gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype,
-                                         gb_op op, gb_codec codec, int block, void *const *rank_bufs,
-                                         gb_stream stream) {
+// The second half of the fused pair: decode (or fold) the payloads, add them
+// in island order, divide for AVG, and write every rank (rs == 0) or rank
+// r's slice of n / W elements (rs == 1).
+static gb_status decompress_to_ranks(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype, gb_op op,
+                                     gb_codec codec, int block, void *const *dst, int rs, gb_stream stream) {
     GB_TRY(check_ctx(c));
-    GB_TRY(check_codec_dtype(c, dtype));
-    if (op != GB_SUM && op != GB_AVG)
-        return set_msg(c, GB_ERR_UNSUPPORTED_OP, "decompress + island broadcast takes SUM / AVG");
-    GB_TRY(check_codec(c, codec, block));
-    GB_TRY(check_n(c, n));
+    GB_TRY(check_collective(c, n, dtype, op, codec, block));
     GB_TRY(check_dev_bufs(c, payloads, c->I * c->I, "payloads"));
-    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)dst, c->W, rs ? "out" : "rank_bufs"));
+    if (rs && n % (size_t)c->W)
+        return set_msg(c, GB_ERR_INVALID_ARG, "n = %zu is not a multiple of W = %d", n, c->W);
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
+    const bool exact = is_exact(dtype, op);
     const int blk = is_fp8(codec) ? block : 256;
     gb::DecodeBcastArgs da;
     memset(&da, 0, sizeof da);
     for (int r = 0; r < c->W; ++r) {
-        da.dst[r] = rank_bufs[r];
+        da.dst[r] = dst[r];
         da.group_of_rank[r] = c->island_of[r];
     }
     bool same_rows = true;  // every leader holds the same pointers: decode once
@@ -320,24 +321,78 @@ gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads,
         da.n_groups = c->I;
         da.n_src = c->I;
     }
+    if (rs) {  // grid unit r (first[n_groups] = W of them): rank r's slice, from row group_of_rank[r]
+        const uint64_t m = n / (uint64_t)c->W;
+        for (int r = 0; r < c->W; ++r) {
+            da.rs_src[r] = (uint64_t)r * m;
+            da.rs_len[r] = m;
+        }
+        da.rs = 1;
+        const uint64_t ve = exact ? 16 / elem_bytes(dtype) : 8;
+        da.vec = (m % ve) == 0;
+        da.tiles = (uint32_t)((m + gb::kTile - 1) / gb::kTile);
+    } else {
+        da.rs = 0;
+        da.vec = 1;
+        da.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
+    }
     da.avg = op == GB_AVG;
     da.world = (float)c->W;
     da.world_pow2 = (c->W & (c->W - 1)) == 0;
     da.inv_world = 1.0f / (float)c->W;
     da.n = n;
-    da.scales_off = scales_offset(codec, n);
-    da.rs = 0;
-    da.vec = 1;
-    da.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
-    return check_launch(c, gb::launch_decode_bcast(da, dtype, codec, blk, (cudaStream_t)stream),
-                        "decompress + island broadcast");
+    da.scales_off = exact ? 0 : scales_offset(codec, n);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (exact) return check_launch(c, gb::launch_exact_combine(da, dtype, op, s), "fold + broadcast");
+    return check_launch(c, gb::launch_decode_bcast(da, dtype, codec, blk, s), "decompress + island broadcast");
+}
+
+gb_status gb_decompress_island_broadcast(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype,
+                                         gb_op op, gb_codec codec, int block, void *const *rank_bufs,
+                                         gb_stream stream) {
+    return decompress_to_ranks(c, payloads, n, dtype, op, codec, block, rank_bufs, 0, stream);
+}
+
+gb_status gb_decompress_scatter(gb_ctx *c, const void *const *payloads, size_t n, gb_dtype dtype, gb_op op,
+                                gb_codec codec, int block, void *const *out, gb_stream stream) {
+    return decompress_to_ranks(c, payloads, n, dtype, op, codec, block, out, 1, stream);
+}
+
+size_t gb_island_payload_bytes(gb_dtype dtype, gb_op op, gb_codec codec, int block, size_t n) {
+    if (dtype < GB_F32 || dtype > GB_I64 || op < GB_SUM || op > GB_MIN || !codec_ok(codec, block)) return 0;
+    if (op == GB_AVG && !is_float_dtype(dtype)) return 0;
+    if ((dtype == GB_F16 || dtype == GB_F64) && (op == GB_SUM || op == GB_AVG) && codec != GB_CODEC_NONE) return 0;
+    if (is_exact(dtype, op)) return n * gb::exact_payload_elem_bytes(dtype, op);
+    return payload_bytes(codec, block, n);
+}
+
+gb_status gb_island_reduce_compress_op(gb_ctx *c, const void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                       gb_op op, gb_codec codec, int block, void *const *payloads,
+                                       gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_collective(c, n, dtype, op, codec, block));
+    if (!is_exact(dtype, op))
+        return island_reduce_compress(c, rank_bufs, nullptr, n, dtype, codec, block, payloads, stream);
+    GB_TRY(check_rank_bufs(c, rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_dev_bufs(c, (const void *const *)payloads, c->I, "payloads"));
+    if (n == 0) return GB_OK;
+    GB_TRY(bind(c));
+    gb::ReduceEncodeArgs ra;
+    memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < c->W; ++r) ra.src[r] = rank_bufs[r];
+    for (int i = 0; i < c->I; ++i) ra.payload[i] = payloads[i];
+    for (int i = 0; i <= c->I; ++i) ra.first[i] = c->first[i];
+    ra.n_islands = c->I;
+    ra.n = n;
+    ra.tiles = (uint32_t)((n + gb::kTile - 1) / gb::kTile);
+    return check_launch(c, gb::launch_exact_reduce(ra, dtype, op, (cudaStream_t)stream), "island fold");
 }
 
 gb_status gb_all_reduce(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dtype, gb_op op,
                         gb_codec codec, int block, gb_stream stream) {
     GB_TRY(check_ctx(c));
     GB_TRY(check_collective(c, n, dtype, op, codec, block));
-    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
     return run_rbb(c, (const void *const *)rank_bufs, rank_bufs, n, dtype, op, codec, block,
@@ -350,7 +405,7 @@ gb_status gb_all_reduce_ef(gb_ctx *c, void *const *rank_bufs, float *const *resi
     GB_TRY(check_collective(c, n, dtype, op, codec, block));
     if (is_exact(dtype, op))
         return set_msg(c, GB_ERR_UNSUPPORTED_OP, "error feedback applies to float32 / bfloat16 SUM / AVG");
-    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
     GB_TRY(check_dev_bufs(c, (const void *const *)residuals, c->I, "residuals"));
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
@@ -362,8 +417,8 @@ gb_status gb_reduce_scatter(gb_ctx *c, const void *const *in, void *const *out, 
                             gb_dtype dtype, gb_op op, gb_codec codec, int block, gb_stream stream) {
     GB_TRY(check_ctx(c));
     GB_TRY(check_collective(c, n_in, dtype, op, codec, block));
-    GB_TRY(check_dev_bufs(c, in, c->W, "in"));
-    GB_TRY(check_dev_bufs(c, (const void *const *)out, c->W, "out"));
+    GB_TRY(check_rank_bufs(c, in, c->W, "in"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)out, c->W, "out"));
     if (n_in % (size_t)c->W)
         return set_msg(c, GB_ERR_INVALID_ARG, "n_in = %zu is not a multiple of W = %d", n_in, c->W);
     if (n_in == 0) return GB_OK;
@@ -376,15 +431,17 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
     GB_TRY(check_ctx(c));
     GB_TRY(check_dtype(c, dtype));
     GB_TRY(check_n(c, n_in));
-    GB_TRY(check_dev_bufs(c, in, c->W, "in"));
-    GB_TRY(check_dev_bufs(c, (const void *const *)out, c->W, "out"));
+    GB_TRY(check_rank_bufs(c, in, c->W, "in"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)out, c->W, "out"));
     if (n_in == 0) return GB_OK;
     GB_TRY(bind(c));
     cudaStream_t s = (cudaStream_t)stream;
     const int W = c->W, I = c->I;
     const size_t mb = n_in * elem_bytes(dtype);
-    if (I > 1) GB_TRY(grow_host(c, (size_t)W * mb));
-    GB_TRY(begin(c, s));
+    if (I > 1) {  // one island touches no staging: nothing to order against other calls
+        GB_TRY(grow_host(c, (size_t)W * mb));
+        GB_TRY(begin(c, s));
+    }
     const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
     GB_TRY(mark(c, mm, 0, s));
     GB_TRY(mark(c, mm, 1, s));
@@ -461,7 +518,7 @@ gb_status gb_all_gather(gb_ctx *c, const void *const *in, void *const *out, size
     }
     GB_TRY(mark(c, mm, 5, s));
     commit_marks(c, 1, I > 1);
-    return end(c, s);
+    return I > 1 ? end(c, s) : GB_OK;
 }
 
 gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dtype, int src,
@@ -469,7 +526,7 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
     GB_TRY(check_ctx(c));
     GB_TRY(check_dtype(c, dtype));
     GB_TRY(check_n(c, n));
-    GB_TRY(check_dev_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(c, (const void *const *)rank_bufs, c->W, "rank_bufs"));
     if (src < 0 || src >= c->W) return set_msg(c, GB_ERR_INVALID_ARG, "src %d", src);
     if (n == 0) return GB_OK;
     GB_TRY(bind(c));
@@ -477,8 +534,10 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
     const int I = c->I;
     const int si = c->island_of[src];
     const size_t nb = n * elem_bytes(dtype);
-    if (I > 1) GB_TRY(grow_host(c, nb));
-    GB_TRY(begin(c, s));
+    if (I > 1) {  // one island touches no staging: nothing to order against other calls
+        GB_TRY(grow_host(c, nb));
+        GB_TRY(begin(c, s));
+    }
     const int mm = c->tcap > 0 ? kMarkDirect : kMarkOff;
     GB_TRY(mark(c, mm, 0, s));
     GB_TRY(mark(c, mm, 1, s));
@@ -545,7 +604,7 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
     GB_TRY(check_launch(c, gb::launch_copy(a, s), "broadcast copy"));
     GB_TRY(mark(c, mm, 5, s));
     commit_marks(c, 1, I > 1);
-    return end(c, s);
+    return I > 1 ? end(c, s) : GB_OK;
 }
 
 gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dtype dtype, gb_op op,
@@ -677,7 +736,7 @@ static gb_status all_reduce_buckets(gb_ctx *c, int n_buckets, void *const *bucke
     for (int b = 0; b < n_buckets; ++b) {
         GB_TRY(check_n(c, bucket_numel[b]));
         if (bucket_numel[b] == 0) continue;  // an empty bucket's pointers are never used
-        GB_TRY(check_dev_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
+        GB_TRY(check_rank_bufs(c, (const void *const *)(bucket_bufs + (size_t)b * c->W), c->W, "bucket_bufs"));
         if (res)
             GB_TRY(check_dev_bufs(c, (const void *const *)(res + (size_t)b * c->I), c->I, "residuals"));
     }
@@ -726,8 +785,8 @@ gb_status gb_reduce_scatter_buckets(gb_ctx *c, int n_buckets, const void *const 
         if (bucket_numel[b] % (size_t)c->W)
             return set_msg(c, GB_ERR_INVALID_ARG, "bucket %d: %zu elements is not a multiple of W = %d", b,
                            bucket_numel[b], c->W);
-        GB_TRY(check_dev_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
-        GB_TRY(check_dev_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
+        GB_TRY(check_rank_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
+        GB_TRY(check_rank_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
         total += bucket_numel[b];
     }
     if (total == 0) return GB_OK;
@@ -754,8 +813,8 @@ gb_status gb_all_gather_buckets(gb_ctx *c, int n_buckets, const void *const *in_
         GB_TRY(check_n(c, bucket_numel_in[b]));
         GB_TRY(check_n(c, bucket_numel_in[b] * (size_t)c->W));
         if (bucket_numel_in[b] == 0) continue;
-        GB_TRY(check_dev_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
-        GB_TRY(check_dev_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
+        GB_TRY(check_rank_bufs(c, in_bufs + (size_t)b * c->W, c->W, "in_bufs"));
+        GB_TRY(check_rank_bufs(c, (const void *const *)(out_bufs + (size_t)b * c->W), c->W, "out_bufs"));
         total += bucket_numel_in[b];
         const size_t mb = bucket_numel_in[b] * elem_bytes(dtype);
         if (mb > mb_max) mb_max = mb;

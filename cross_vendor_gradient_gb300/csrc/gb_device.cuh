@@ -112,6 +112,37 @@ __device__ __forceinline__ void st_u2(void *p, uint2 v) {
     asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// A lane's 8 float32 elements of a rank buffer: one 32-byte access, or,
+// when a rank buffer of the launch is only 16-byte aligned (A16), two
+// 16-byte accesses at the same addresses (the warp still covers the same
+// contiguous 1 KiB).
+template <bool A16>
+__device__ __forceinline__ U8x32 ld_stream_f32x8(const void *p) {
+    if constexpr (A16) {
+        const uint4 lo = ld_stream_u4(p), hi = ld_stream_u4((const unsigned char *)p + 16);
+        return U8x32{{lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w}};
+    } else {
+        return ld_stream_v8(p);
+    }
+}
+template <bool A16>
+__device__ __forceinline__ void st_stream_f32x8(void *p, const uint32_t w[8]) {
+    if constexpr (A16) {
+        st_stream_u4(p, make_uint4(w[0], w[1], w[2], w[3]));
+        st_stream_u4((unsigned char *)p + 16, make_uint4(w[4], w[5], w[6], w[7]));
+    } else {
+        st_stream_v8(p, w);
+    }
+}
+
+// Whether any of the first `count` buffers is 16-byte but not 32-byte
+// aligned (host side; rank buffers must be 16-byte aligned).
+inline bool any_a16(const void *const *p, int count) {
+    for (int i = 0; i < count; ++i)
+        if (((uintptr_t)p[i] & 31u) != 0) return true;
+    return false;
+}
+
 // ------------------------------------------------------------ conversions
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) { return __uint_as_float(h16 << 16); }
 

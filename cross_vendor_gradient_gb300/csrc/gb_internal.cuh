@@ -129,6 +129,7 @@ enum { kMarkOff = 0, kMarkDirect = 1, kMarkCapture = 2 };
 // Shape of one reduce-bridge-broadcast: the element range is cut into C
 // chunks of whole 256-element tiles (so whole codec blocks); every chunk's
 // payload parts have a fixed stride `part`.  C == 1 is the plain policy.
+// chunk_range gives chunk ch's first element and length.
 struct Plan {
     int I = 0, W = 0;
     uint64_t n = 0;
@@ -136,12 +137,18 @@ struct Plan {
     gb_op op = GB_SUM;
     int eff = GB_CODEC_NONE, blk = 256, rs = 0;
     size_t eb = 4, cb = 4;
-    uint64_t chunk = 0;
+    uint64_t chunk = 0;  // the longest chunk (the part stride holds it)
     int C = 1;
+    uint64_t off[kMaxChunks + 1] = {};  // chunk ch is elements [off[ch], off[ch + 1])
     int links = 1;  // copy stream pairs the chunks' bridge copies are spread over
     size_t part = 0;
     size_t dev_bytes = 0, host_bytes = 0;
 };
+
+inline void chunk_range(const Plan &p, int ch, uint64_t *e0, uint64_t *m) {
+    *e0 = p.off[ch];
+    *m = p.off[ch + 1] - p.off[ch];
+}
 
 // One chunk of a bucket set's pipeline (enqueue_buckets): bucket b,
 // elements [e0, e0 + m).
@@ -164,6 +171,7 @@ bool codec_ok(int codec, int block);
 gb_status check_codec(gb_ctx *c, int codec, int block);
 gb_status check_n(gb_ctx *c, size_t n);
 gb_status check_dev_bufs(gb_ctx *c, const void *const *bufs, int count, const char *name);
+gb_status check_rank_bufs(gb_ctx *c, const void *const *bufs, int count, const char *name);
 gb_status check_dev_ptr(gb_ctx *c, const void *p, const char *name);
 int seen_device(gb_ctx *c, int dev);
 gb_status bind(gb_ctx *c);

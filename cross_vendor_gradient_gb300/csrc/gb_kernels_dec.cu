@@ -123,8 +123,9 @@ __device__ __forceinline__ void decode_lane(const void *payload, uint64_t scales
 }
 
 // Write this lane's 8 float32 results to a rank buffer of type T (bf16:
-// round to nearest even), streaming.
-template <typename T>
+// round to nearest even), streaming (A16: float32 rank buffers only
+// 16-byte aligned).
+template <typename T, bool A16>
 __device__ __forceinline__ void store_rank(void *p, uint64_t lbase, int lane, uint64_t limit, bool full,
                                            const float t[8]) {
     if constexpr (sizeof(T) == 4) {
@@ -133,7 +134,7 @@ __device__ __forceinline__ void store_rank(void *p, uint64_t lbase, int lane, ui
             uint32_t w[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(t[k]);
-            st_stream_v8(f + lbase + 8 * lane, w);
+            st_stream_f32x8<A16>(f + lbase + 8 * lane, w);
         } else {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -157,7 +158,7 @@ __device__ __forceinline__ void store_rank(void *p, uint64_t lbase, int lane, ui
 }
 
 // AVG and the stores of one tile's totals to ranks r_lo .. r_hi - 1.
-template <typename T>
+template <typename T, bool A16>
 __device__ __forceinline__ void finish_tile(const DecodeBcastArgs &a, int r_lo, int r_hi, uint64_t lbase, int lane,
                                             uint64_t limit, bool full, float t[8]) {
     if (a.avg) {
@@ -171,11 +172,13 @@ __device__ __forceinline__ void finish_tile(const DecodeBcastArgs &a, int r_lo, 
             for (int k = 0; k < 8; ++k) t[k] = __fdiv_rn(t[k], a.world);
         }
     }
-    for (int r = r_lo; r < r_hi; ++r) store_rank<T>(a.dst[r], lbase, lane, limit, full, t);
+    for (int r = r_lo; r < r_hi; ++r) store_rank<T, A16>(a.dst[r], lbase, lane, limit, full, t);
 }
 
 // NS > 0: exactly NS payloads (loads unrolled); NS == 0: a.n_src of them.
-template <typename T, int CODEC, int BLOCK, int NS>
+// A16: some float32 rank buffer is only 16-byte aligned (launched with
+// NS == 0).
+template <typename T, int CODEC, int BLOCK, int NS, bool A16 = false>
 __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ DecodeBcastArgs a) {
     const int u = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ De
 #pragma unroll
                 for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[k]);  // island order
             }
-            finish_tile<T>(a, r_lo, r_hi, (uint64_t)tile * kTile, lane, limit, true, t);
+            finish_tile<T, A16>(a, r_lo, r_hi, (uint64_t)tile * kTile, lane, limit, true, t);
 #pragma unroll
             for (int q = 0; q < NS; ++q) cur[q] = nx[q];
             tile = nxt;
@@ -254,7 +257,54 @@ __global__ void __launch_bounds__(256) k_decode_bcast(const __grid_constant__ De
                     for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[q][k]);
                 }
         }
-        finish_tile<T>(a, r_lo, r_hi, lbase, lane, limit, full, t);
+        finish_tile<T, A16>(a, r_lo, r_hi, lbase, lane, limit, full, t);
+    }
+}
+
+// reduce_scatter's decode (grid y = rank r): rank r's slice only, one
+// output per tile.  A warp writes 1 KiB per tile here against 4 KiB in the
+// all_reduce decode, so the work per warp is small and the grid holds about
+// one tile per warp: the next-tile prefetch of k_decode_bcast buys nothing
+// and its registers cost occupancy (40 against 32 per thread, 6 against 8
+// resident blocks per SM).  The NS payloads of a full tile are all loaded
+// before the first decode.
+template <typename T, int CODEC, int BLOCK, int NS, bool A16 = false>
+__global__ void __launch_bounds__(256, (NS > 0 && !A16) ? 8 : 1) k_decode_slices(const __grid_constant__ DecodeBcastArgs a) {
+    const int u = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int g = a.group_of_rank[u];
+    const uint64_t gofs = a.rs_src[u], limit = a.rs_len[u];
+    const int nsrc = NS > 0 ? NS : a.n_src;
+    const uint32_t wpb = blockDim.x >> 5;
+    const uint32_t stride = gridDim.x * wpb;
+    const uint32_t nfull = a.vec ? (uint32_t)(limit / kTile) : 0u;
+    for (uint32_t tile = blockIdx.x * wpb + (threadIdx.x >> 5) + wait_prior_grid(); tile < a.tiles; tile += stride) {
+        const uint64_t lbase = (uint64_t)tile * kTile;
+        float t[8];
+        if (NS > 0 && tile < nfull) {
+            RawLane<CODEC> r[NS > 0 ? NS : 1];
+#pragma unroll
+            for (int q = 0; q < NS; ++q) load_raw<CODEC, BLOCK>(a.payload[g][q], a.scales_off, gofs + lbase, lane, r[q]);
+            decode_raw<CODEC>(r[0], t);
+#pragma unroll
+            for (int q = 1; q < NS; ++q) {
+                float d[8];
+                decode_raw<CODEC>(r[q], d);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[k]);  // island order
+            }
+            finish_tile<T, A16>(a, u, u + 1, lbase, lane, limit, true, t);
+        } else {
+            const bool full = tile < nfull;
+            decode_lane<CODEC, BLOCK>(a.payload[g][0], a.scales_off, gofs + lbase, lbase, limit, lane, full, t);
+            for (int j = 1; j < nsrc; ++j) {
+                float d[8];
+                decode_lane<CODEC, BLOCK>(a.payload[g][j], a.scales_off, gofs + lbase, lbase, limit, lane, full, d);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) t[k] = __fadd_rn(t[k], d[k]);
+            }
+            finish_tile<T, A16>(a, u, u + 1, lbase, lane, limit, full, t);
+        }
     }
 }
 
@@ -277,32 +327,39 @@ __global__ void __launch_bounds__(256) k_decompress_acc(const __grid_constant__ 
     }
 }
 
+// Grid row j copies job j.  With 16-byte vectors a thread moves kCopyU of
+// them per step, spaced a grid apart (each load and store instruction of a
+// warp covers 512 contiguous bytes), all loaded before the first store.
+constexpr int kCopyU = 4;
+
 __global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a) {
-    const uint64_t tid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x + wait_prior_grid();
+    const int j = blockIdx.y;
+    const unsigned char *s = a.src[j];
+    const int d_lo = a.dst_lo[j], d_hi = a.dst_hi[j];
+    const uint64_t off = a.dst_off[j];
     const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x + wait_prior_grid();
     if (a.vec) {
         const uint64_t chunks = a.bytes / 16;
-        const uint64_t total = chunks * (uint64_t)a.n_jobs;
-        for (uint64_t c = tid; c < total; c += nth) {
-            const int j = (int)(c / chunks);
-            const uint64_t off = (c - (uint64_t)j * chunks) * 16;
-            const unsigned char *s = a.src[j] + off;
-            const uint4 x = ld_stream_u4(s);
-            for (int d = a.dst_lo[j]; d < a.dst_hi[j]; ++d) {
-                unsigned char *p = a.dst[d] + a.dst_off[j] + off;
-                if (p != s) st_stream_u4(p, x);
+        for (; t < chunks; t += kCopyU * nth) {
+            uint4 x[kCopyU];
+#pragma unroll
+            for (int u = 0; u < kCopyU; ++u)
+                if (t + u * nth < chunks) x[u] = ld_stream_u4(s + 16 * (t + u * nth));
+            for (int d = d_lo; d < d_hi; ++d) {
+                unsigned char *p = a.dst[d] + off;
+                if (p == s) continue;  // the source itself (a leader's received block)
+#pragma unroll
+                for (int u = 0; u < kCopyU; ++u)
+                    if (t + u * nth < chunks) st_stream_u4(p + 16 * (t + u * nth), x[u]);
             }
         }
     } else {
-        const uint64_t total = a.bytes * (uint64_t)a.n_jobs;
-        for (uint64_t c = tid; c < total; c += nth) {
-            const int j = (int)(c / a.bytes);
-            const uint64_t off = c - (uint64_t)j * a.bytes;
-            const unsigned char *s = a.src[j] + off;
-            const unsigned char x = *s;
-            for (int d = a.dst_lo[j]; d < a.dst_hi[j]; ++d) {
-                unsigned char *p = a.dst[d] + a.dst_off[j] + off;
-                if (p != s) *p = x;
+        for (; t < a.bytes; t += nth) {
+            const unsigned char x = s[t];
+            for (int d = d_lo; d < d_hi; ++d) {
+                unsigned char *p = a.dst[d] + off;
+                if (p != s) p[t] = x;
             }
         }
     }
@@ -313,6 +370,16 @@ __global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a
 template <typename T, int CODEC, int BLOCK>
 static cudaError_t dispatch_ns(const DecodeBcastArgs &a, cudaStream_t s) {
     const unsigned units = a.rs ? (unsigned)a.first[a.n_groups] : (unsigned)a.n_groups;
+    const bool a16 = sizeof(T) == 4 && any_a16((const void *const *)a.dst, a.first[a.n_groups]);
+    if (a.rs) {
+        if (a16) return launch_grid<k_decode_slices<T, CODEC, BLOCK, 0, true>>(a.tiles, units, a, s);
+        switch (a.n_src) {
+        case 1: return launch_grid<k_decode_slices<T, CODEC, BLOCK, 1>>(a.tiles, units, a, s);
+        case 2: return launch_grid<k_decode_slices<T, CODEC, BLOCK, 2>>(a.tiles, units, a, s);
+        default: return launch_grid<k_decode_slices<T, CODEC, BLOCK, 0>>(a.tiles, units, a, s);
+        }
+    }
+    if (a16) return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 0, true>>(a.tiles, units, a, s);
     switch (a.n_src) {
     case 1: return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 1>>(a.tiles, units, a, s);
     case 2: return launch_grid<k_decode_bcast<T, CODEC, BLOCK, 2>>(a.tiles, units, a, s);
@@ -353,10 +420,10 @@ cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, 
 }
 
 cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s) {
-    const uint64_t units = a.vec ? a.bytes / 16 : a.bytes;
-    const uint64_t threads = units * (uint64_t)a.n_jobs;
-    // launch_grid counts 8 warps of 32 threads per block: pass threads / 32 as "tiles"
-    return launch_grid<k_copy>((threads + 31) / 32, 1, a, s);
+    // threads per job: one per kCopyU 16-byte vectors, or one per byte;
+    // launch_grid counts 8 warps of 32 threads per block, so it is given warps
+    const uint64_t threads = a.vec ? (a.bytes / 16 + kCopyU - 1) / kCopyU : a.bytes;
+    return launch_grid<k_copy>((threads + 31) / 32, (unsigned)a.n_jobs, a, s);
 }
 
 }  // namespace gb

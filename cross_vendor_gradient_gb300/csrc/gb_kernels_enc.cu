@@ -21,13 +21,14 @@ namespace gb {
 
 using bf16 = __nv_bfloat16;
 
-// This lane's 8 elements of rank buffer `p` in tile `base`, as float32.
-template <typename T>
+// This lane's 8 elements of rank buffer `p` in tile `base`, as float32
+// (A16: float32 rank buffers only 16-byte aligned).
+template <typename T, bool A16>
 __device__ __forceinline__ void load_rank(const void *p, uint64_t base, int lane, uint64_t n, bool full,
                                           float v[8]) {
     if constexpr (sizeof(T) == 4) {
         if (full) {
-            const U8x32 x = ld_stream_v8((const float *)p + base + 8 * lane);
+            const U8x32 x = ld_stream_f32x8<A16>((const float *)p + base + 8 * lane);
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = __uint_as_float(x.w[k]);
         } else {
@@ -155,13 +156,13 @@ __device__ __forceinline__ void encode_store(unsigned char *payload, uint64_t sc
 // The island sum of this lane's 8 elements of the tile at `base` (ascending
 // rank order).  KT > 0: exactly KT ranks, all loads issued before the first
 // add; KT == 0: K ranks, four ranks' loads in flight at a time.
-template <typename T, int KT>
+template <typename T, int KT, bool A16>
 __device__ __forceinline__ void island_sum(const ReduceEncodeArgs &a, int r0, int K, uint64_t base, int lane,
                                            bool full, float v[8]) {
     if constexpr (KT > 0) {
         float w[KT][8];
 #pragma unroll
-        for (int q = 0; q < KT; ++q) load_rank<T>(a.src[r0 + q], base, lane, a.n, full, w[q]);
+        for (int q = 0; q < KT; ++q) load_rank<T, A16>(a.src[r0 + q], base, lane, a.n, full, w[q]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[k] = w[0][k];
 #pragma unroll
@@ -169,12 +170,12 @@ __device__ __forceinline__ void island_sum(const ReduceEncodeArgs &a, int r0, in
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = __fadd_rn(v[k], w[q][k]);
     } else {
-        load_rank<T>(a.src[r0], base, lane, a.n, full, v);
+        load_rank<T, A16>(a.src[r0], base, lane, a.n, full, v);
         for (int q0 = 1; q0 < K; q0 += 4) {
             float w[4][8];
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-                if (q0 + u < K) load_rank<T>(a.src[r0 + q0 + u], base, lane, a.n, full, w[u]);
+                if (q0 + u < K) load_rank<T, A16>(a.src[r0 + q0 + u], base, lane, a.n, full, w[u]);
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 if (q0 + u < K) {
@@ -195,8 +196,9 @@ constexpr int kTilesPerStep = (sizeof(T) == 2 && KT > 0 && !EF) ? 2 : 1;
 
 // KT > 0: every island has KT ranks (loads unrolled); KT == 0: any sizes.
 // EF: error feedback -- encode s + r and keep r = (s + r) - dec(codes) in
-// the island's residual buffer (float32, n elements).
-template <typename T, int CODEC, int BLOCK, int KT, bool EF>
+// the island's residual buffer (float32, n elements).  A16: some float32
+// rank buffer is only 16-byte aligned (launched with KT == 0).
+template <typename T, int CODEC, int BLOCK, int KT, bool EF, bool A16 = false>
 __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ ReduceEncodeArgs a) {
     const int isl = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
                         }
                     }
                 } else {
-                    island_sum<T, KT>(a, r0, K, base, lane, false, v);
+                    island_sum<T, KT, A16>(a, r0, K, base, lane, false, v);
                 }
                 encode_store<CODEC, BLOCK, false>(payload, a.scales_off, tile, lane, n, full[h], v, nullptr);
             }
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(256) k_reduce_encode(const __grid_constant__ R
             const uint64_t base = (uint64_t)tile * kTile;
             const bool full = base + kTile <= n;
             float v[8];
-            island_sum<T, KT>(a, r0, K, base, lane, full, v);
+            island_sum<T, KT, A16>(a, r0, K, base, lane, full, v);
             if constexpr (EF) {
                 float *res = a.residual[isl];
                 float r[8], dec[8];
@@ -297,6 +299,8 @@ static cudaError_t dispatch_k(const ReduceEncodeArgs &a, cudaStream_t s) {
     // the grid counts warp steps: tiles, or tile pairs (kTilesPerStep)
     constexpr int P = kTilesPerStep<T, 1, EF>;
     const uint64_t steps = (a.tiles + P - 1) / P;
+    if (sizeof(T) == 4 && any_a16(a.src + a.first[0], a.first[a.n_islands] - a.first[0]))
+        return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 0, EF, true>>(a.tiles, units, a, s);
     switch (K) {
     case 1: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 1, EF>>(steps, units, a, s);
     case 2: return launch_grid<k_reduce_encode<T, CODEC, BLOCK, 2, EF>>(steps, units, a, s);

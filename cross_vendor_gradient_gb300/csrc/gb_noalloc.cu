@@ -67,7 +67,7 @@ extern "C" gb_status gb_all_reduce_noalloc(gb_ctx *ctx, void *const *rank_bufs, 
     GB_TRY(check_codec(ctx, codec, block));
     GB_TRY(check_n(ctx, n));
     const int I = ctx->I, W = ctx->W;
-    GB_TRY(check_dev_bufs(ctx, (const void *const *)rank_bufs, W, "rank_bufs"));
+    GB_TRY(check_rank_bufs(ctx, (const void *const *)rank_bufs, W, "rank_bufs"));
     if (n == 0) return GB_OK;
     const int eff = I == 1 ? GB_CODEC_NONE : (int)codec;
     const int blk = is_fp8(eff) ? block : 256;

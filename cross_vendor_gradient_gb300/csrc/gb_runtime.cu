@@ -43,7 +43,8 @@ bool is_float_dtype(int d) { return d == GB_F32 || d == GB_BF16 || d == GB_F16 |
 // MAX / MIN, and every dtype but float32 / bfloat16, take the exact path.
 bool is_exact(int dtype, int op) { return op == GB_MAX || op == GB_MIN || (dtype != GB_F32 && dtype != GB_BF16); }
 
-// The kernels move float32 data with 32-byte vector accesses.
+// Payloads, island sums, accumulators and residuals: the kernels move their
+// float32 data with 32-byte vector accesses.
 bool aligned32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
 
 gb_status check_ctx(gb_ctx *c) {
@@ -94,6 +95,19 @@ gb_status check_dev_bufs(gb_ctx *c, const void *const *bufs, int count, const ch
     for (int r = 0; r < count; ++r) {
         if (!bufs[r]) return set_msg(c, GB_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
         if (!aligned32(bufs[r])) return set_msg(c, GB_ERR_MISALIGNED, "%s[%d] not 32-byte aligned", name, r);
+    }
+    return GB_OK;
+}
+
+// Rank buffers (the collectives' inputs and outputs): 16-byte aligned.  The
+// kernels move float32 rank data with 32-byte accesses when every rank
+// buffer of a launch is 32-byte aligned, else with two 16-byte accesses.
+gb_status check_rank_bufs(gb_ctx *c, const void *const *bufs, int count, const char *name) {
+    if (!bufs) return set_msg(c, GB_ERR_INVALID_ARG, "%s is NULL", name);
+    for (int r = 0; r < count; ++r) {
+        if (!bufs[r]) return set_msg(c, GB_ERR_INVALID_ARG, "%s[%d] is NULL", name, r);
+        if (((uintptr_t)bufs[r] & 15u) != 0)
+            return set_msg(c, GB_ERR_MISALIGNED, "%s[%d] not 16-byte aligned", name, r);
     }
     return GB_OK;
 }
@@ -345,6 +359,7 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         if (ch < n) p.chunk = ch;
     }
     p.C = (int)((n + p.chunk - 1) / p.chunk);
+    for (int ch = 0; ch <= p.C; ++ch) p.off[ch] = (uint64_t)ch * p.chunk < n ? (uint64_t)ch * p.chunk : n;
     if (sharded_ok && !rs && c->sharded && c->I > 1 && k > 1) p.links = p.C < kMaxLinks ? p.C : kMaxLinks;
     p.part = round_up(part_bytes(p, p.chunk), 256);
     // received parts: two islands share one mirror of the host slots (leader
@@ -420,8 +435,8 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
     // 1. island reduce + encode, chunk by chunk
     GB_TRY(mark(c, markmode, 0, s));
     for (int ch = 0; ch < p.C; ++ch) {
-        const uint64_t e0 = (uint64_t)ch * p.chunk;
-        const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+        uint64_t e0, m;
+        chunk_range(p, ch, &e0, &m);
         gb::ReduceEncodeArgs ra;
         memset(&ra, 0, sizeof ra);
         for (int r = 0; r < p.W; ++r) ra.src[r] = (const unsigned char *)in[r] + e0 * p.eb;
@@ -449,8 +464,8 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         auto link_h = [&](int ch) { const int l = ch % p.links; return l ? c->lsh[l] : c->sh; };
         cudaStream_t D = s, H = s;
         for (int ch = 0; ch < p.C; ++ch) {
-            const uint64_t e0 = (uint64_t)ch * p.chunk;
-            const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+            uint64_t e0, m;
+            chunk_range(p, ch, &e0, &m);
             const size_t pb = part_bytes(p, m);
             if (multi) {
                 D = link_d(ch);
@@ -490,8 +505,8 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
 
     // 3. decode + accumulate + broadcast, chunk by chunk
     for (int ch = 0; ch < p.C; ++ch) {
-        const uint64_t e0 = (uint64_t)ch * p.chunk;
-        const uint64_t m = (p.n - e0) < p.chunk ? (p.n - e0) : p.chunk;
+        uint64_t e0, m;
+        chunk_range(p, ch, &e0, &m);
         if (multi) GB_TRY(wait_on(c, s, c->ev_h2d[ch]));
         GB_TRY(mark(c, markmode, 4 + 2 * ch, s));
         gb::DecodeBcastArgs da;
@@ -583,10 +598,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
         return base + (((size_t)g * p.C + ch) * I + j) * p.part;
     };
     auto hslot = [&](int ch, int j) { return c->h_stage + ((size_t)ch * I + j) * p.part; };
-    auto range = [&](int ch, uint64_t *e0, uint64_t *m) {
-        *e0 = (uint64_t)ch * p.chunk;
-        *m = (p.n - *e0) < p.chunk ? (p.n - *e0) : p.chunk;
-    };
+    auto range = [&](int ch, uint64_t *e0, uint64_t *m) { chunk_range(p, ch, e0, m); };
     cudaStream_t D = c->sd, H = c->sh;
     if (c->inject == GB_INJECT_BRIDGE) {
         c->inject = 0;

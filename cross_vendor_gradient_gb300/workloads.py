@@ -6,8 +6,10 @@ bucket planning): it only describes the workloads and draws their inputs, so
 that the CUDA path and the oracle can be fed the same bytes.
 
 Seeds: rank r of workload c draws from ``numpy.random.PCG64(1000 * c + r)``
-(host) or from a ``torch.Generator`` seeded the same way on the target device
-(large workloads, generated where they are used).
+(host: the small workloads and the oracle-checked sizes) or from a
+``torch.Generator`` seeded the same way on the target device (the payload
+sweep, and large buffers, generated where they are used); bucket b of a
+bucketed workload draws on the device with seed bucket_seed(c, b, r).
 """
 from dataclasses import dataclass, field
 
@@ -92,6 +94,12 @@ SWEEP_LOG2 = tuple(range(10, 27))  # 2^10 .. 2^26 float32 elements per rank
 
 def seed_of(cid: int, rank: int) -> int:
     return 1000 * cid + rank
+
+
+def bucket_seed(cid: int, bucket: int, rank: int) -> int:
+    """Seed of rank `rank`'s buffer of bucket `bucket` in a bucketed workload
+    (the benchmark and the tests draw the same buckets)."""
+    return 1_000_000 * cid + 1000 * bucket + rank
 
 
 # ---------------------------------------------------------------- host side

@@ -19,11 +19,16 @@
  *
  * Conventions for every call below:
  *   - Pointers named *_bufs / rank_bufs / in / out are arrays of W (or K_i)
- *     DEVICE pointers, in global rank order, each 32-byte aligned (the
- *     kernels move float32 data with 32-byte vector accesses; cudaMalloc
- *     and torch allocations are; GB_ERR_MISALIGNED otherwise).  Every other
- *     device buffer argument must be 32-byte aligned too.  The caller owns
- *     them.
+ *     DEVICE pointers, in global rank order, each 16-byte aligned (the
+ *     all_reduce alignment rule of the torch-mojo-backend page,
+ *     "Distributed training", Limitations), so that a gradient view
+ *     inside a bucket may start at any multiple of 16 bytes.  The kernels
+ *     move float32 rank data with 32-byte accesses when every rank buffer of
+ *     a launch is 32-byte aligned, else with two 16-byte accesses.  Every
+ *     other device buffer argument (payloads, island sums, accumulators,
+ *     totals, error-feedback residuals) must be 32-byte aligned (cudaMalloc
+ *     and torch allocations are).  GB_ERR_MISALIGNED otherwise.  The caller
+ *     owns them.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
  *     call validates all of its arguments first and returns an error with
  *     nothing enqueued; otherwise it enqueues its work on `stream` and returns
@@ -69,7 +74,8 @@ typedef enum {
                                   /* not take (MAX / MIN where only SUM / AVG apply)      */
     GB_ERR_UNSUPPORTED_CODEC = 4, /* unknown codec, fp8 block not 128 / 256, or a codec   */
                                   /* on float16 / float64 SUM / AVG                       */
-    GB_ERR_MISALIGNED = 5,        /* a device buffer not 32-byte aligned                  */
+    GB_ERR_MISALIGNED = 5,        /* a rank buffer not 16-byte aligned, or another device */
+                                  /* buffer not 32-byte aligned                           */
     GB_ERR_ALLOC = 6,             /* pinned or device staging allocation failed (sticky)  */
     GB_ERR_CUDA = 7,              /* a CUDA runtime call failed (sticky)                  */
     GB_ERR_BRIDGE = 8,            /* the bridge hop failed (sticky)                       */
@@ -236,8 +242,8 @@ size_t gb_payload_scales_offset(gb_codec codec, int block, size_t n);
 
 /* island_sum[j] = ((x_0[j] + x_1[j]) + ...) + x_{K-1}[j] in float32, over the
  * K = gb_island_size(ctx, island) buffers of `rank_bufs` (that island's
- * ranks, in rank order).  island_sum: n float32, device, 32-byte aligned,
- * must not overlap the inputs. */
+ * ranks, in rank order, 16-byte aligned).  island_sum: n float32, device,
+ * 32-byte aligned, must not overlap the inputs. */
 gb_status gb_island_reduce(gb_ctx *ctx, int island, const void *const *rank_bufs, size_t n,
                            gb_dtype dtype, float *island_sum, gb_stream stream);
 
@@ -272,7 +278,7 @@ gb_status gb_island_broadcast(gb_ctx *ctx, int island, const float *total, size_
  * with `codec` and `block`, in the layout of gb_payload_bytes (codes, then
  * the fp8 scales at gb_payload_scales_offset).  The codec is applied as
  * given, with one island too (gb_all_reduce skips it there: no bridge).
- * rank_bufs: W device buffers of n elements, 32-byte aligned, read only.
+ * rank_bufs: W device buffers of n elements, 16-byte aligned, read only.
  * payloads: I device buffers of gb_payload_bytes(codec, block, n) bytes,
  * 32-byte aligned, owned by the caller.  dtype F32 or BF16.  One kernel
  * launch for all islands, stream-ordered on `stream`.
@@ -298,10 +304,48 @@ gb_status gb_island_reduce_compress_ef(gb_ctx *ctx, const void *const *rank_bufs
                                        gb_dtype dtype, gb_codec codec, int block, void *const *payloads,
                                        gb_stream stream);
 /* The second half, decode + accumulate + broadcast (described with
- * gb_island_reduce_compress above). */
+ * gb_island_reduce_compress above).  It also takes the exact path's
+ * payloads (the dtypes and ops of gb_island_reduce_compress_op; codec as
+ * for gb_all_reduce): every rank of island g receives the fold of
+ * payloads[g * I + 0 .. I - 1] in island order (AVG divided by W), rounded
+ * to dtype. */
 gb_status gb_decompress_island_broadcast(gb_ctx *ctx, const void *const *payloads, size_t n, gb_dtype dtype,
                                          gb_op op, gb_codec codec, int block, void *const *rank_bufs,
                                          gb_stream stream);
+
+/* The fused halves for every dtype and op gb_all_reduce takes (gpubridge
+ * README, API table, all_reduce row and the supported dtypes; "Bridge
+ * compression": MAX / MIN and integer dtypes stay exact).
+ *
+ * gb_island_payload_bytes: bytes of one island's payload for n elements --
+ * gb_payload_bytes(codec, block, n) on the codec path (float32 / bfloat16
+ * SUM / AVG); otherwise the exact path's island fold: n elements of the
+ * dtype, or n float32 sums for float16 / bfloat16 SUM / AVG.  0 for a
+ * combination gb_all_reduce refuses.
+ *
+ * gb_island_reduce_compress_op: gb_island_reduce_compress with an op.  On
+ * the codec path it is that call; otherwise payloads[i] receives the fold
+ * of island i's ranks in ascending rank order (MAX / MIN: among equal values
+ * the lower rank's is kept; integer SUM wraps; float16 / bfloat16 sums in
+ * float32, float64 in float64), the codec ignored (float16 / float64 SUM /
+ * AVG take GB_CODEC_NONE only).  payloads: I device buffers of
+ * gb_island_payload_bytes bytes, 32-byte aligned.  One kernel launch.
+ *
+ * gb_decompress_scatter: reduce_scatter's second half (API table,
+ * reduce_scatter_tensor row): out[r] (n / W elements, device, 16-byte
+ * aligned, not overlapping the payloads) receives elements
+ * [r * n / W, (r + 1) * n / W) of what gb_decompress_island_broadcast would
+ * write into every rank from the same payloads (payloads: I * I pointers as
+ * there).  n must be a multiple of W.  One kernel launch.
+ *
+ * Errors as for gb_all_reduce / gb_reduce_scatter; n == 0 is a no-op.
+ * Neither call allocates. */
+size_t gb_island_payload_bytes(gb_dtype dtype, gb_op op, gb_codec codec, int block, size_t n);
+gb_status gb_island_reduce_compress_op(gb_ctx *ctx, const void *const *rank_bufs, size_t n, gb_dtype dtype,
+                                       gb_op op, gb_codec codec, int block, void *const *payloads,
+                                       gb_stream stream);
+gb_status gb_decompress_scatter(gb_ctx *ctx, const void *const *payloads, size_t n, gb_dtype dtype, gb_op op,
+                                gb_codec codec, int block, void *const *out, gb_stream stream);
 
 /* ------------------------------------------------------------ collectives */
 

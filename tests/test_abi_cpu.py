@@ -125,7 +125,8 @@ def test_argument_errors_need_no_device():
         assert B.gb_all_reduce(ctx, fake, 10, 0, 0, 5, 256) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_all_reduce(ctx, fake[:3] + [0], 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG
         assert B.gb_all_reduce(ctx, fake[:3] + [0x10008], 10, 0, 0, 0, 256) == B.GB_ERR_MISALIGNED
-        assert B.gb_all_reduce(ctx, fake[:3] + [0x10010], 10, 1, 0, 0, 256) == B.GB_ERR_MISALIGNED
+        assert B.gb_all_reduce(ctx, fake[:3] + [0x10004], 10, 1, 0, 0, 256) == B.GB_ERR_MISALIGNED
+        assert "16-byte" in B.gb_last_error_message(ctx)
         assert B.gb_reduce_scatter(ctx, fake, fake, 10, 0, 0, 0, 256) == B.GB_ERR_INVALID_ARG  # 10 % 4
         assert B.gb_broadcast(ctx, fake, 10, 0, 4) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce(ctx, 2, fake, 10, 0, fake[0]) == B.GB_ERR_INVALID_ARG
@@ -138,7 +139,28 @@ def test_argument_errors_need_no_device():
         assert B.gb_island_reduce_compress(ctx, fake, 10, 0, 2, 256, [pl[0], 0]) == B.GB_ERR_INVALID_ARG
         assert B.gb_island_reduce_compress(ctx, fake, 10, 0, 2, 256, [pl[0], pl[1] + 16]) == B.GB_ERR_MISALIGNED
         pl4 = pl + pl[::-1]  # every leader's row
-        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, B.GB_MAX, 2, 256, fake) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, B.GB_I32, B.GB_AVG, 0, 256, fake) == \
+            B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_decompress_island_broadcast(ctx, pl4, 10, B.GB_F16, B.GB_SUM, 2, 256, fake) == \
+            B.GB_ERR_UNSUPPORTED_CODEC
+        # the halves for every dtype and op, and reduce_scatter's second half
+        assert B.gb_island_reduce_compress_op(ctx, fake, 10, B.GB_I8, B.GB_AVG, 0, 256, pl) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_island_reduce_compress_op(ctx, fake, 10, 9, 0, 0, 256, pl) == B.GB_ERR_UNSUPPORTED_DTYPE
+        assert B.gb_island_reduce_compress_op(ctx, fake, 10, B.GB_F64, B.GB_AVG, 1, 256, pl) == \
+            B.GB_ERR_UNSUPPORTED_CODEC
+        assert B.gb_island_reduce_compress_op(ctx, fake, 10, B.GB_I32, B.GB_MAX, 0, 256, [pl[0], 0]) == \
+            B.GB_ERR_INVALID_ARG
+        assert B.gb_island_reduce_compress_op(ctx, fake, 0, B.GB_I32, B.GB_MAX, 0, 256, pl) == B.GB_OK
+        assert B.gb_decompress_scatter(ctx, pl4, 10, 0, 0, 2, 256, fake) == B.GB_ERR_INVALID_ARG  # 10 % 4
+        assert B.gb_decompress_scatter(ctx, pl4, 12, B.GB_U8, B.GB_AVG, 0, 256, fake) == B.GB_ERR_UNSUPPORTED_OP
+        assert B.gb_decompress_scatter(ctx, pl4, 12, 0, 0, 2, 256, fake[:3] + [0x10008]) == B.GB_ERR_MISALIGNED
+        assert B.gb_decompress_scatter(ctx, pl4, 0, 0, 0, 2, 256, fake) == B.GB_OK
+        assert B.gb_island_payload_bytes(B.GB_F32, B.GB_SUM, 2, 256, 1024) == B.gb_payload_bytes(2, 256, 1024)
+        assert B.gb_island_payload_bytes(B.GB_BF16, B.GB_MAX, 2, 256, 1024) == 2048
+        assert B.gb_island_payload_bytes(B.GB_F16, B.GB_AVG, 0, 256, 1024) == 4096
+        assert B.gb_island_payload_bytes(B.GB_I64, B.GB_SUM, 0, 256, 3) == 24
+        assert B.gb_island_payload_bytes(B.GB_I64, B.GB_AVG, 0, 256, 3) == 0
+        assert B.gb_island_payload_bytes(B.GB_F32, B.GB_SUM, 2, 64, 3) == 0
         assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, 0, 7, 256, fake) == B.GB_ERR_UNSUPPORTED_CODEC
         assert B.gb_decompress_island_broadcast(ctx, pl4, 10, 0, 0, 2, 256, fake[:3] + [0]) == B.GB_ERR_INVALID_ARG
         assert B.gb_decompress_island_broadcast(ctx, pl4[:3] + [0], 10, 0, 0, 2, 256, fake) == B.GB_ERR_INVALID_ARG

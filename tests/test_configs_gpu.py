@@ -102,26 +102,24 @@ def test_c3_payload_sweep(codec):
     with Context(w.island_sizes) as ctx:
         for lg in wl.SWEEP_LOG2:
             n = 1 << lg
-            if lg <= 20:
-                xs = wl.host_rank_inputs(w, n=n)
-                want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
-                bufs = [to_dev(x) for x in xs]
+            # the benchmark's inputs: drawn on the device, seed_of(c3, r)
+            ins = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), "cuda", torch.float32)
+                   for r in range(w.world_size)]
+            bufs = [x.clone() for x in ins]
+            for _ in range(2):  # direct, then captured (the benchmark's pipelined policy)
+                for b, x in zip(bufs, ins):
+                    b.copy_(x)
                 ctx.all_reduce(bufs, w.op, codec, w.block)
-                torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            if lg <= 20:  # every element
+                xs = [to_host(x) for x in ins]
+                want = orc.all_reduce(xs, w.island_sizes, w.op, codec, w.block)
                 for r in range(w.world_size):
                     assert_bits_equal(to_host(bufs[r]), want[r], "c3 %s n=2^%d rank %d" % (codec, lg, r))
             else:
-                ins = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), "cuda", torch.float32)
-                       for r in range(w.world_size)]
-                bufs = [x.clone() for x in ins]
-                for _ in range(2):  # direct, then captured
-                    for b, x in zip(bufs, ins):
-                        b.copy_(x)
-                    ctx.all_reduce(bufs, w.op, codec, w.block)
-                torch.cuda.synchronize()
                 ranks_identical(bufs)
                 check_sampled(ins, bufs, w.island_sizes, w.op, codec, w.block, n, 48, lg, "c3 %s n=2^%d" % (codec, lg))
-                del ins, bufs
+            del ins, bufs
 
 
 def _bucketed(w, pad):
@@ -138,7 +136,7 @@ def test_c4_gpt2_small_buckets():
     with Context(w.island_sizes) as ctx:
         ins, bufs = [], []
         for b, nb in enumerate(bn):
-            row = [wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 100 * b, "cuda", torch.bfloat16)
+            row = [wl.draw_device(w.dist, nb, wl.bucket_seed(w.cid, b, r), "cuda", torch.bfloat16)
                    for r in range(w.world_size)]
             ins.append(row)
             bufs.append([x.clone() for x in row])
@@ -164,13 +162,13 @@ def test_c5_llama_buckets_and_rs_ag():
     with Context(w.island_sizes) as ctx:
         ins, bufs = [], []
         for b, nb in enumerate(bn):
-            row = [wl.draw_device(w.dist, nb, wl.seed_of(w.cid, r) + 1000 * b, "cuda", torch.bfloat16)
+            row = [wl.draw_device(w.dist, nb, wl.bucket_seed(w.cid, b, r), "cuda", torch.bfloat16)
                    for r in range(W)]
             ins.append(row)
             bufs.append([x.clone() for x in row])
         ctx.all_reduce_buckets(bufs, w.op, codec, w.block)
         torch.cuda.synchronize()
-        for b in range(0, len(bn), 7):
+        for b in range(len(bn)):  # every bucket: chunk boundaries differ between bucket sizes
             check_sampled(ins[b], bufs[b], w.island_sizes, w.op, codec, w.block, bn[b], 8, b, "c5 bucket %d" % b)
         # reduce_scatter then all_gather over the same inputs equals the all_reduce, everywhere
         for b, nb in enumerate(bn):

@@ -327,11 +327,25 @@ __global__ void __launch_bounds__(256) k_decompress_acc(const __grid_constant__ 
     }
 }
 
-// Grid row j copies job j.  With 16-byte vectors a thread moves kCopyU of
-// them per step, spaced a grid apart (each load and store instruction of a
-// warp covers 512 contiguous bytes), all loaded before the first store.
-constexpr int kCopyU = 4;
+// Grid row j copies job j.  With vectors (VB = 16 or 32 bytes, when every
+// address and the length are multiples of VB) a thread moves 64 bytes per
+// step as 64 / VB vectors spaced a grid apart (each warp instruction covers
+// 32 * VB contiguous bytes), all loaded before the first store.  32-byte
+// vectors halve the store instructions, which otherwise fill the
+// load/store queue (ncu: lg_throttle stalls).
+template <int VB> struct CopyVec;
+template <> struct CopyVec<16> {
+    uint4 x;
+    __device__ __forceinline__ void ld(const unsigned char *p) { x = ld_stream_u4(p); }
+    __device__ __forceinline__ void st(unsigned char *p) const { st_stream_u4(p, x); }
+};
+template <> struct CopyVec<32> {
+    U8x32 x;
+    __device__ __forceinline__ void ld(const unsigned char *p) { x = ld_stream_v8(p); }
+    __device__ __forceinline__ void st(unsigned char *p) const { st_stream_v8(p, x.w); }
+};
 
+template <int VB>
 __global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a) {
     const int j = blockIdx.y;
     const unsigned char *s = a.src[j];
@@ -339,19 +353,20 @@ __global__ void __launch_bounds__(256) k_copy(const __grid_constant__ CopyArgs a
     const uint64_t off = a.dst_off[j];
     const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
     uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x + wait_prior_grid();
-    if (a.vec) {
-        const uint64_t chunks = a.bytes / 16;
-        for (; t < chunks; t += kCopyU * nth) {
-            uint4 x[kCopyU];
+    if constexpr (VB > 0) {
+        constexpr int U = 64 / VB;
+        const uint64_t chunks = a.bytes / VB;
+        for (; t < chunks; t += U * nth) {
+            CopyVec<VB> x[U];
 #pragma unroll
-            for (int u = 0; u < kCopyU; ++u)
-                if (t + u * nth < chunks) x[u] = ld_stream_u4(s + 16 * (t + u * nth));
+            for (int u = 0; u < U; ++u)
+                if (t + u * nth < chunks) x[u].ld(s + VB * (t + u * nth));
             for (int d = d_lo; d < d_hi; ++d) {
                 unsigned char *p = a.dst[d] + off;
                 if (p == s) continue;  // the source itself (a leader's received block)
 #pragma unroll
-                for (int u = 0; u < kCopyU; ++u)
-                    if (t + u * nth < chunks) st_stream_u4(p + 16 * (t + u * nth), x[u]);
+                for (int u = 0; u < U; ++u)
+                    if (t + u * nth < chunks) x[u].st(p + VB * (t + u * nth));
             }
         }
     } else {
@@ -420,10 +435,16 @@ cudaError_t launch_decompress_accumulate(const DecompressAccArgs &a, int codec, 
 }
 
 cudaError_t launch_copy(const CopyArgs &a, cudaStream_t s) {
-    // threads per job: one per kCopyU 16-byte vectors, or one per byte;
     // launch_grid counts 8 warps of 32 threads per block, so it is given warps
-    const uint64_t threads = a.vec ? (a.bytes / 16 + kCopyU - 1) / kCopyU : a.bytes;
-    return launch_grid<k_copy>((threads + 31) / 32, (unsigned)a.n_jobs, a, s);
+    bool v32 = a.vec && a.bytes % 32 == 0;
+    for (int j = 0; v32 && j < a.n_jobs; ++j) {
+        v32 = ((uintptr_t)a.src[j] & 31u) == 0 && a.dst_off[j] % 32 == 0;
+        for (int d = a.dst_lo[j]; v32 && d < a.dst_hi[j]; ++d) v32 = ((uintptr_t)a.dst[d] & 31u) == 0;
+    }
+    // 64 bytes per thread: warps = bytes / (64 * 32)
+    if (v32 || a.vec) return (v32 ? launch_grid<k_copy<32>, CopyArgs> : launch_grid<k_copy<16>, CopyArgs>)(
+                          (a.bytes + 2047) / 2048, (unsigned)a.n_jobs, a, s);
+    return launch_grid<k_copy<0>>((a.bytes + 31) / 32, (unsigned)a.n_jobs, a, s);
 }
 
 }  // namespace gb

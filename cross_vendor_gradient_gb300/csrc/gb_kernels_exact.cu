@@ -119,7 +119,42 @@ __device__ __forceinline__ V16<T> load16(const T *p) {
 }
 
 // --------------------------------------------------------------- kernels
-template <typename T, int OP>
+// The fold of KT rank vectors (16 bytes of T each, ascending rank) into the
+// payload vector out (NPO 16-byte words of P).
+template <typename T, int OP, int KT, int NPO>
+__device__ __forceinline__ void fold_ranks_raw(const uint4 (&raw)[KT], uint4 (&out)[NPO]) {
+    using A = typename Ex<T>::A;
+    using P = PayloadT<T, OP>;
+    constexpr int N = V16<T>::N;
+    if constexpr (kByteSimd<T>) {
+        uint4 acc = raw[0];
+#pragma unroll
+        for (int q = 1; q < KT; ++q)
+            acc = make_uint4(fold4<T, OP>(acc.x, raw[q].x), fold4<T, OP>(acc.y, raw[q].y),
+                             fold4<T, OP>(acc.z, raw[q].z), fold4<T, OP>(acc.w, raw[q].w));
+        out[0] = acc;
+    } else {
+        A s[N];
+#pragma unroll
+        for (int q = 0; q < KT; ++q) {
+            T x[N];
+            memcpy(x, &raw[q], 16);
+#pragma unroll
+            for (int k = 0; k < N; ++k) s[k] = q == 0 ? Ex<T>::widen(x[k]) : fold<OP>(s[k], Ex<T>::widen(x[k]));
+        }
+        P o[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) o[k] = to_payload<T, OP>(s[k]);
+        memcpy(out, o, sizeof o);
+    }
+}
+
+// KT > 0: every island has KT ranks.  Then a thread takes kFoldU full
+// vectors per step, spaced a grid apart, and issues all KT * kFoldU rank
+// loads before the first fold; the rest, and KT == 0, take the loop below.
+constexpr int kFoldU = 2;
+
+template <typename T, int OP, int KT>
 __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ ReduceEncodeArgs a) {
     using A = typename Ex<T>::A;
     using P = PayloadT<T, OP>;
@@ -129,8 +164,27 @@ __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ Re
     const int K = a.first[isl + 1] - r0;
     P *out = (P *)a.payload[isl];
     const uint64_t nvec = (a.n + N - 1) / N;
-    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid(); vi < nvec;
-         vi += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid();
+    if constexpr (KT > 0) {
+        constexpr int NPO = (int)(sizeof(P) * N / 16);
+        const uint64_t nfull = a.n / N;
+        for (; vi + (kFoldU - 1) * nth < nfull; vi += kFoldU * nth) {
+            uint4 raw[kFoldU][KT];
+#pragma unroll
+            for (int v = 0; v < kFoldU; ++v)
+#pragma unroll
+                for (int q = 0; q < KT; ++q) raw[v][q] = ld_u4((const T *)a.src[r0 + q] + (vi + v * nth) * N);
+#pragma unroll
+            for (int v = 0; v < kFoldU; ++v) {
+                uint4 o[NPO];
+                fold_ranks_raw<T, OP, KT, NPO>(raw[v], o);
+#pragma unroll
+                for (int i = 0; i < NPO; ++i) st_u4((unsigned char *)(out + (vi + v * nth) * N) + 16 * i, o[i]);
+            }
+        }
+    }
+    for (; vi < nvec; vi += nth) {
         const uint64_t j0 = vi * N;
         const int cnt = (a.n - j0) < (uint64_t)N ? (int)(a.n - j0) : N;
         if constexpr (kByteSimd<T>) {
@@ -190,7 +244,57 @@ __global__ void __launch_bounds__(256) k_exact_reduce(const __grid_constant__ Re
     }
 }
 
-template <typename T, int OP>
+// The fold of NS payload vectors (raw bits of N payload elements each, NP
+// 16-byte words, island order), AVG applied, narrowed to 16 bytes of T.
+template <typename T, int OP, int NS, int NP>
+__device__ __forceinline__ uint4 combine_raw(const uint4 (&raw)[NS][NP], const DecodeBcastArgs &a) {
+    using A = typename Ex<T>::A;
+    using P = PayloadT<T, OP>;
+    constexpr int N = V16<T>::N;
+    if constexpr (kByteSimd<T> && OP != GB_AVG) {
+        uint4 acc = raw[0][0];
+#pragma unroll
+        for (int q = 1; q < NS; ++q)
+            acc = make_uint4(fold4<T, OP>(acc.x, raw[q][0].x), fold4<T, OP>(acc.y, raw[q][0].y),
+                             fold4<T, OP>(acc.z, raw[q][0].z), fold4<T, OP>(acc.w, raw[q][0].w));
+        return acc;
+    } else {
+        A t[N];
+#pragma unroll
+        for (int q = 0; q < NS; ++q) {
+            P x[N];
+            memcpy(x, raw[q], sizeof x);
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                const A v = to_acc<T, OP>(x[k]);
+                t[k] = (q == 0) ? v : fold<OP>(t[k], v);
+            }
+        }
+        if constexpr (OP == GB_AVG) {
+#pragma unroll
+            for (int k = 0; k < N; ++k) {
+                if constexpr (sizeof(A) == 8)
+                    t[k] = __ddiv_rn(t[k], (double)a.world);
+                else
+                    t[k] = a.world_pow2 ? __fmul_rn(t[k], a.inv_world) : __fdiv_rn(t[k], a.world);
+            }
+        }
+        T o[N];
+#pragma unroll
+        for (int k = 0; k < N; ++k) o[k] = Ex<T>::narrow(t[k]);
+        uint4 w;
+        memcpy(&w, o, 16);
+        return w;
+    }
+}
+
+// NS > 0: exactly NS payloads.  Then a thread takes kCombineU full vectors
+// per step, spaced a grid apart, and issues all their payload loads before
+// the first fold (the codec decode keeps as many bytes in flight per lane);
+// the rest, and NS == 0, take the element-wise-capable loop below.
+constexpr int kCombineU = 2;
+
+template <typename T, int OP, int NS>
 __global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ DecodeBcastArgs a) {
     using A = typename Ex<T>::A;
     using P = PayloadT<T, OP>;
@@ -212,8 +316,29 @@ __global__ void __launch_bounds__(256) k_exact_combine(const __grid_constant__ D
         limit = a.n;
     }
     const uint64_t nvec = (limit + N - 1) / N;
-    for (uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid(); vi < nvec;
-         vi += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t nth = (uint64_t)gridDim.x * blockDim.x;
+    uint64_t vi = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x + wait_prior_grid();
+    if constexpr (NS > 0) {
+        constexpr int NP = (int)(sizeof(P) * N / 16);
+        const uint64_t nfull = a.vec ? limit / N : 0;
+        for (; vi + (kCombineU - 1) * nth < nfull; vi += kCombineU * nth) {
+            uint4 raw[kCombineU][NS][NP];
+#pragma unroll
+            for (int v = 0; v < kCombineU; ++v)
+#pragma unroll
+                for (int q = 0; q < NS; ++q)
+#pragma unroll
+                    for (int i = 0; i < NP; ++i)
+                        raw[v][q][i] = ld_u4((const unsigned char *)((const P *)a.payload[g][q] + gofs +
+                                                                   (vi + v * nth) * N) + 16 * i);
+#pragma unroll
+            for (int v = 0; v < kCombineU; ++v) {
+                const uint4 w = combine_raw<T, OP, NS, NP>(raw[v], a);
+                for (int r = r_lo; r < r_hi; ++r) st_stream_u4((T *)a.dst[r] + (vi + v * nth) * N, w);
+            }
+        }
+    }
+    for (; vi < nvec; vi += nth) {
         const uint64_t l0 = vi * N;
         const int cnt = (limit - l0) < (uint64_t)N ? (int)(limit - l0) : N;
         const bool full = a.vec && cnt == N;
@@ -284,7 +409,16 @@ static cudaError_t launch_pair(bool combine, const void *args, cudaStream_t s) {
     constexpr int N = V16<T>::N;
     if (!combine) {
         const ReduceEncodeArgs &a = *(const ReduceEncodeArgs *)args;
-        return launch_vec<k_exact_reduce<T, OP>>((a.n + N - 1) / N, (unsigned)a.n_islands, a, s);
+        int K = a.first[1] - a.first[0];
+        for (int i = 1; i < a.n_islands; ++i)
+            if (a.first[i + 1] - a.first[i] != K) K = 0;
+        const uint64_t vecs = (a.n + N - 1) / N, per_u = (vecs + kFoldU - 1) / kFoldU;
+        switch (K) {
+        case 1: return launch_vec<k_exact_reduce<T, OP, 1>>(per_u, (unsigned)a.n_islands, a, s);
+        case 2: return launch_vec<k_exact_reduce<T, OP, 2>>(per_u, (unsigned)a.n_islands, a, s);
+        case 4: return launch_vec<k_exact_reduce<T, OP, 4>>(per_u, (unsigned)a.n_islands, a, s);
+        default: return launch_vec<k_exact_reduce<T, OP, 0>>(vecs, (unsigned)a.n_islands, a, s);
+        }
     }
     const DecodeBcastArgs &a = *(const DecodeBcastArgs *)args;
     const unsigned units = a.rs ? (unsigned)a.first[a.n_groups] : (unsigned)a.n_groups;
@@ -294,7 +428,13 @@ static cudaError_t launch_pair(bool combine, const void *args, cudaStream_t s) {
         for (unsigned u = 0; u < units; ++u)
             if (a.rs_len[u] > limit) limit = a.rs_len[u];
     }
-    return launch_vec<k_exact_combine<T, OP>>((limit + N - 1) / N, units, a, s);
+    // one thread per kCombineU vectors when the payload count is unrolled
+    const uint64_t vecs = (limit + N - 1) / N;
+    switch (a.n_src) {
+    case 1: return launch_vec<k_exact_combine<T, OP, 1>>((vecs + kCombineU - 1) / kCombineU, units, a, s);
+    case 2: return launch_vec<k_exact_combine<T, OP, 2>>((vecs + kCombineU - 1) / kCombineU, units, a, s);
+    default: return launch_vec<k_exact_combine<T, OP, 0>>(vecs, units, a, s);
+    }
 }
 
 template <typename T>

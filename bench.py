@@ -799,10 +799,11 @@ def run_buckets_bench(args, world, rank, local, pg):
 
 
 SWEEP_COLUMNS = ["bytes_per_rank", "codec", "steps", "ms_per_step", "algbw_gbs", "encode_frac", "decode_frac",
-                 "encode_frac_in_step", "decode_frac_in_step", "bridge_gbs", "bridge_frac", "floor_ms"]
+                 "encode_frac_in_step", "decode_frac_in_step", "bridge_gbs", "bridge_frac", "floor_ms",
+                 "ms_median"]
 
 
-def op_floor_ms(ctx, bufs, I, P, codec, block, op, stream, flush, clean, reps=50):
+def op_floor_ms(ctx, bufs, I, P, codec, block, op, stream, flush, clean, reps=100):
     """The sum of a one-chunk step's operations, each timed on its own on the
     device (CUDA events around it, L2 flushed before it as before a step,
     after a spin so the host is ahead): the encode launch, the bridge's
@@ -865,7 +866,8 @@ def sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps, emit=None)
         n = 1 << lg
         pristine = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), dev, torch.float32) for r in range(W)]
         bufs = [p.clone() for p in pristine]
-        K = max(5, min(max_steps, int(4e9 // (n * 4 * W))))
+        # up to 1 MiB a step is a few tens of microseconds: 50 of them, for the comparison with the floor
+        K = 50 if n * 4 <= (1 << 20) else max(5, min(max_steps, int(4e9 // (n * 4 * W))))
         Pmax = max(payload_bytes(c, w.block, n) for c in codecs)
         sets = make_sets(pristine, I, Pmax, stream_set_count(W * n * 4 + I * Pmax))
         for codec in codecs:
@@ -892,6 +894,7 @@ def sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps, emit=None)
             ctx.set_pipeline(chunk, True)
             steps(3, False)
             ms = steps(K, True)
+            ms_median = float(np.median([ev0[i].elapsed_time(ev1[i]) for i in range(K)]))
             ctx.set_pipeline(0, False)
             ctx.set_phase_timing(K)
             steps(2, False)
@@ -912,7 +915,7 @@ def sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps, emit=None)
             bridge = link_bytes / (br * 1e-3) / 1e9 if br > 0 else None
             row = [4 * n, codec, K, ms, 4 * n / (ms * 1e-3) / 1e9, b1 / (s1 * 1e-3) / 1e9 / peak,
                    b2 / (s2 * 1e-3) / 1e9 / peak, b1 / (k1 * 1e-3) / 1e9 / peak, b2 / (k2 * 1e-3) / 1e9 / peak,
-                   bridge, bridge / link_peak if bridge else None, floor]
+                   bridge, bridge / link_peak if bridge else None, floor, ms_median]
             rows.append([float('%.6g' % v) if isinstance(v, float) else v for v in row])
             if emit:
                 emit({"metric": METRIC, "sweep_row": True, "workload": "c3", "codec": codec, "n": n,
@@ -946,7 +949,8 @@ def sweep_line_object(rows, peak, peak_kind, link_peak, wall_s):
                                                  "its fraction of min(D2H, H2D) pinned copy bandwidth %.1f GB/s"
                                                  % link_peak,
                       "floor_ms": "rows up to 1 MiB: encode + copies + decode, each timed alone after an L2 "
-                                  "flush, minus the extra event pairs"},
+                                  "flush (median of 100), minus the extra event pairs",
+                      "ms_median": "the median step, beside the mean ms_per_step"},
             "wall_s": wall_s}
 
 

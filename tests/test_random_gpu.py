@@ -1,0 +1,120 @@
+"""Seeded random cases against the oracle, bit for bit: random island layouts,
+lengths, dtypes, ops, codecs, pipeline chunk sizes and rank-view offsets (16
+or 32 bytes into the allocation), through all_reduce, reduce_scatter,
+all_gather and broadcast, each call made twice on the same buffers (the
+second replays a graph where the policy captures one).  Each case is
+reproducible from its index."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from cross_vendor_gradient_gb300 import Context
+from cross_vendor_gradient_gb300 import workloads as wl
+from tests.gpu_util import assert_bits_equal, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+TORCH = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "f64": torch.float64,
+         "i8": torch.int8, "u8": torch.uint8, "i32": torch.int32, "i64": torch.int64}
+CODECS = [("none", 256), ("bf16", 256), ("e4m3", 256), ("e4m3", 128), ("e5m2", 128), ("e5m2", 256)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+
+
+def case(seed):
+    rng = np.random.default_rng(10_000 + seed)
+    I = int(rng.integers(1, 5))
+    sizes = tuple(int(v) for v in rng.integers(1, 5, I))
+    W = sum(sizes)
+    if seed % 2 == 0:  # the codec path: float32 / bfloat16 SUM / AVG
+        dtype = str(rng.choice(["f32", "bf16"]))
+        op = str(rng.choice(["sum", "avg"]))
+        codec, block = CODECS[int(rng.integers(0, len(CODECS)))]
+    else:  # the exact path
+        dtype = str(rng.choice(list(TORCH)))
+        ops = (["max", "min"] if dtype in ("f32", "bf16") else
+               ["sum", "max", "min"] + (["avg"] if dtype in ("f16", "f64") else []))
+        op = str(rng.choice(ops))
+        codec, block = "none", 256
+    m = int(rng.integers(1, 20_000))
+    n = m * W
+    chunk = int(rng.choice([0, 1024, 4096, 65536, 2 << 20]))
+    offs = [int(rng.choice([16, 32])) for _ in range(W)]
+    return sizes, dtype, op, codec, block, n, chunk, offs
+
+
+def draw(dtype, n, seed):
+    rng = np.random.default_rng(seed)
+    if dtype == "f32":
+        return (rng.standard_normal(n) * 1e-2).astype(np.float32)
+    if dtype == "bf16":
+        return wl.to_bf16_bits((rng.standard_normal(n) * 1e-2).astype(np.float32))
+    if dtype in ("f16", "f64"):
+        return (rng.standard_normal(n) * 10).astype(np.float16 if dtype == "f16" else np.float64)
+    npdt = {"i8": np.int8, "u8": np.uint8, "i32": np.int32, "i64": np.int64}[dtype]
+    info = np.iinfo(npdt)
+    return rng.integers(info.min, info.max, n, dtype=npdt, endpoint=True)
+
+
+class View:
+    def __init__(self, count, tdt, off):
+        es = torch.empty(0, dtype=tdt).element_size()
+        self.nbytes, self.lo = count * es, 256 + off
+        self.raw = torch.full((self.lo + self.nbytes + 256,), 0x3C, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[self.lo:self.lo + self.nbytes].view(tdt)
+
+    def intact(self):
+        return bool(torch.all(self.raw[:self.lo] == 0x3C)) and bool(torch.all(self.raw[self.lo + self.nbytes:] == 0x3C))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_case_matches_oracle(seed):
+    sizes, dtype, op, codec, block, n, chunk, offs = case(seed)
+    W = sum(sizes)
+    tdt = TORCH[dtype]
+    xs = [draw(dtype, n, 100 * seed + r) for r in range(W)]
+    what = "seed %d: %s %s %s %s/%d n=%d chunk=%d" % (seed, sizes, dtype, op, codec, block, n, chunk)
+    with Context(sizes) as ctx:
+        ctx.set_pipeline(chunk, True)
+        ranks = [View(n, tdt, o) for o in offs]
+        want = orc.all_reduce(xs, sizes, op, codec, block)
+        for call in range(2):
+            for v, x in zip(ranks, xs):
+                v.t.copy_(to_dev(x))
+            ctx.all_reduce([v.t for v in ranks], op, codec, block)
+            torch.cuda.synchronize()
+            for r in range(W):
+                assert_bits_equal(to_host(ranks[r].t), want[r], "AR %s call %d rank %d" % (what, call, r))
+        # reduce_scatter then all_gather over the same ranks
+        m = n // W
+        ins = [View(n, tdt, o) for o in offs]
+        outs = [View(m, tdt, o) for o in reversed(offs)]
+        for v, x in zip(ins, xs):
+            v.t.copy_(to_dev(x))
+        ctx.reduce_scatter([v.t for v in ins], [o.t for o in outs], op, codec, block)
+        torch.cuda.synchronize()
+        want = orc.reduce_scatter(xs, sizes, op, codec, block)
+        for r in range(W):
+            assert_bits_equal(to_host(outs[r].t), want[r], "RS %s rank %d" % (what, r))
+        gat = [View(n, tdt, o) for o in offs]
+        ctx.all_gather([o.t for o in outs], [g.t for g in gat])
+        torch.cuda.synchronize()
+        want_ag = orc.all_gather([to_host(o.t) for o in outs])
+        for r in range(W):
+            assert_bits_equal(to_host(gat[r].t), want_ag[r], "AG %s rank %d" % (what, r))
+        src = seed % W
+        bc = [View(n, tdt, o) for o in offs]
+        for v, x in zip(bc, xs):
+            v.t.copy_(to_dev(x))
+        ctx.broadcast([v.t for v in bc], src)
+        torch.cuda.synchronize()
+        for r in range(W):
+            assert_bits_equal(to_host(bc[r].t), xs[src], "BC %s rank %d" % (what, r))
+        for v in ranks + bc:
+            assert v.intact(), what

@@ -198,3 +198,29 @@ def test_noalloc_size_limits():
         torch.cuda.synchronize()
         for r in range(3):
             assert_bits_equal(to_host(over[r]), xs[r], "refused call wrote rank %d" % r)
+
+
+def test_noalloc_takes_16_byte_views():
+    """Rank buffers that start 16 bytes into their allocations (views inside
+    a flat bucket): the same bits as gb_all_reduce on the same views, and
+    the bytes around each view untouched."""
+    sizes, n = (2, 2), 65_536 + 24
+    xs = _inputs(sizes, n, "f32", 95)
+    with Context(sizes) as ctx:
+        raws, views, refs = [], [], []
+        for x in xs:
+            raw = torch.full((n + 16,), -7.0, device="cuda")
+            v = raw[4:4 + n]  # 16 bytes in
+            assert v.data_ptr() % 32 == 16
+            v.copy_(to_dev(x))
+            raws.append(raw)
+            views.append(v)
+            refs.append(to_dev(x))
+        st = B.gb_all_reduce_noalloc(ctx.handle, [t.data_ptr() for t in views], n, B.GB_F32, B.GB_AVG,
+                                     B.GB_CODEC_E4M3, 256, torch.cuda.current_stream().cuda_stream)
+        assert st == B.GB_OK, B.gb_status_string(st)
+        ctx.all_reduce(refs, "avg", "e4m3", 256)
+        torch.cuda.synchronize()
+        for r in range(4):
+            assert_bits_equal(to_host(views[r]), to_host(refs[r]), "rank %d" % r)
+            assert bool(torch.all(raws[r][:4] == -7.0)) and bool(torch.all(raws[r][4 + n:] == -7.0)), r

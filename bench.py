@@ -607,13 +607,22 @@ def host_call_us(ctx, bufs, pristine, op, codec, block, stream, calls=200):
 KERNEL_SOURCES = ("gb_kernels_enc.cu", "gb_kernels_dec.cu", "gb_kernels_exact.cu", "gb_device.cuh", "gb_kernels.cuh")
 
 
+def _code_only(text):
+    """C++ source without its comments and blank lines: what the compiler sees."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_sha():
-    """sha256[:16] over the kernel sources (the key of a recorded capture)."""
+    """sha256[:16] over the kernel sources' code, comments left out (the key
+    of a recorded capture: a comment edit does not change what was profiled)."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "cross_vendor_gradient_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "cross_vendor_gradient_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -10,12 +10,14 @@
 // How: the host passes the payloads once, as one output group holding all
 // W ranks (every leader would compute the same bits), so each payload is
 // read and decoded once.  One warp per 256-element tile per output unit
-// (grid y: a group of ranks, or one rank for reduce_scatter), 8 contiguous
-// elements per lane; the payloads of a tile are all loaded before the first add
-// (compile-time count for 1 or 2 islands), and for those counts the loads of
-// the warp's next tile are issued before the current one is decoded and
-// stored; the result leaves as one 32-byte (float32) or 16-byte (bf16)
-// streaming store per lane per rank.
+// (grid y: a group of ranks; reduce_scatter has its own kernel, one grid
+// row per rank's slice), 8 contiguous elements per lane; the payloads of a
+// tile are all loaded before the first add (compile-time count for 1 or 2
+// islands), and for those counts the loads of the warp's next tile are
+// issued before the current one is decoded and stored; the result leaves as
+// one 32-byte (float32; two 16-byte halves when a rank buffer is only
+// 16-byte aligned) or 16-byte (bf16) streaming store per lane per rank.
+// The exact copies (all_gather, broadcast) take one grid row per copy job.
 #include <atomic>
 #include <cuda_runtime.h>
 

@@ -8,7 +8,9 @@
 // for SUM / AVG, the dtype itself for MAX / MIN, whose result is always one
 // of the inputs); float64 in float64; integers wrap modulo 2^bits for SUM.
 // MAX keeps the earlier value unless a later one is strictly greater (MIN:
-// strictly less).  Each thread moves 16 bytes of rank data per step.
+// strictly less).  Threads move 16-byte vectors: two per step, with every
+// operand's load issued before the first fold, when the rank (payload)
+// count is a compile-time 1, 2 or 4 (1 or 2); one per step otherwise.
 #include <cstring>
 #include <type_traits>
 

@@ -1,5 +1,6 @@
 """The committed ncu summaries belong to the kernel sources as they stand:
-every summary under profiles/ names the sources' hash it was captured from,
+every summary under profiles/ names the hash of the sources' code (comments
+left out) it was captured from,
 and the recorded DRAM traffic that bench.py reports is keyed by the same
 hash.  A kernel change without a new capture fails here (and bench.py would
 report no traffic)."""
@@ -27,3 +28,10 @@ def test_recorded_traffic_is_for_the_current_kernels():
     for kernel in ("k_decode_bcast", "k_reduce_encode"):
         t = bench.traffic_from_profiles(kernel)
         assert t is not None and t > 0, kernel
+
+
+def test_the_capture_key_ignores_comments_only():
+    import bench
+    code = "int f(int x) {\n    return x + 1;  // one more\n}\n/* a note\n   over lines */\n"
+    assert bench._code_only(code) == bench._code_only(code.replace("one more", "plus one").replace("note", "remark"))
+    assert bench._code_only(code) != bench._code_only(code.replace("x + 1", "x + 2"))

@@ -18,12 +18,13 @@ be written back during the step); neither is inside the step's CUDA events.
 Reported: algorithm GB/s (bytes of one rank buffer / step time, summed over
 replicas), the dominant kernel's HBM roofline fraction from live CUDA event
 durations (each kernel launched back to back over input sets cycled so that
-none is in L2; the per-kernel durations inside a step, with a CUDA event
-around every phase, are reported beside it), the bridge hop against measured
-pinned copy bandwidth, the
-same metric end to end through gb_all_reduce_host with pinned host buffers,
-and the oracle timed on the host cores (``--impl reference`` times only the
-oracle).  Multi-GPU: one independent replica per GPU (the path has no
+none is in L2, in steady state; the per-kernel durations inside a step, with
+a CUDA event around every phase, are reported beside it), the bridge hop
+against measured pinned copy bandwidth, the same metric end to end through
+gb_all_reduce_host with pinned host buffers, the oracle timed on the host
+cores (``--impl reference`` times only the oracle), and, on one GPU, the
+metric's curve: the 4 KiB .. 256 MiB payload sweep x codec as a compact
+`sweep` object.  Multi-GPU: one independent replica per GPU (the path has no
 exchange between GPUs), max time over ranks.
 """
 import argparse
@@ -769,8 +770,17 @@ def run_buckets_bench(args, world, rank, local, pg):
             step(i, True, per_bucket=True)
     torch.cuda.synchronize()
     ph = np.array([ctx.phase_times(a) for a in range(Kr * len(bn))])  # newest first
-    ctx.close()
+    ctx.set_phase_timing(0)
+    # timed region 3 on the set's largest bucket within the 25 MiB cap (the
+    # shape most of the set's kernels have): each kernel back to back
     b = w.elem_bytes
+    bi = max((i for i, nb in enumerate(bn) if nb * b <= wl.BUCKET_CAP_BYTES), key=lambda i: bn[i])
+    Pb = payload_bytes(codec, w.block, bn[bi])
+    ks = kernel_stream(ctx, pristine[bi], I, Pb, codec, w.block, w.op, stream, clean, 2, 5, ef=ef)
+    ctx.close()
+    kb1, kb2 = alg_bytes(W, I, bn[bi], b, Pb)
+    if ef:
+        kb1 += 2 * I * bn[bi] * 4
     per_rank = sum(bn) * b
     bytes1 = bytes2 = 0
     for nb in bn:
@@ -783,7 +793,8 @@ def run_buckets_bench(args, world, rank, local, pg):
     t1 = float(np.sum(ph[:, 0])) / Kr
     t2 = float(np.sum(ph[:, 2])) / Kr
     peak, peak_kind = measured_peaks()
-    dom = ("k_reduce_encode", bytes1, t1) if t1 >= t2 else ("k_decode_bcast", bytes2, t2)
+    s1, s2 = ks["k_reduce_encode"], ks["k_decode_bcast"]
+    dom = ("k_reduce_encode", kb1, s1) if s1 >= s2 else ("k_decode_bcast", kb2, s2)
     achieved = dom[1] / (dom[2] * 1e-3) / 1e9
     return {
         "metric": METRIC, "value": world * per_rank / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": world,
@@ -799,9 +810,16 @@ def run_buckets_bench(args, world, rank, local, pg):
                              "cut evenly), one CUDA graph per step" % (chunk_bytes >> 10),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_step": dom[1],
-                     "kernel_ms_per_step": dom[2], "traffic": None,
-                     "region": "one hop per bucket, CUDA events around each kernel"},
+                     "unit": "GB/s", "frac": achieved / peak, "alg_bytes_per_launch": dom[1],
+                     "avg_launch_ms": dom[2], "traffic": None,
+                     "region": "timed region 3 on bucket %d (%d values per rank, the largest within the 25 MiB "
+                               "cap): each kernel back to back over %d input sets, steady state"
+                               % (bi, bn[bi], ks["sets"])},
+        "kernels_stream_ms": ks,
+        "kernels_in_step": {"k_reduce_encode_ms_per_step": t1, "k_decode_bcast_ms_per_step": t2,
+                            "k_reduce_encode_hbm_frac": bytes1 / (t1 * 1e-3) / 1e9 / peak,
+                            "k_decode_bcast_hbm_frac": bytes2 / (t2 * 1e-3) / 1e9 / peak,
+                            "region": "one hop per bucket over the whole set, CUDA events around each kernel"},
         "gpu_launches": int(launches), "clocks": clk,
         **({"rs_ag": rs_line} if rs_line else {}),
     }

@@ -101,3 +101,41 @@ def test_context_bound_to_its_device_and_destroy_waits():
     torch.cuda.synchronize()
     a = to_host(bufs[0])
     assert np.array_equal(a, to_host(bufs[2]))
+
+
+@pytest.mark.parametrize("call", ["all_reduce", "reduce_scatter", "all_gather", "broadcast", "halves"])
+def test_a_foreign_device_is_refused_before_anything_runs(call):
+    """A context bound to a device refuses a call made while another device
+    is current (simulated on one GPU with GB_INJECT_OTHER_DEVICE): an
+    argument error, nothing launched or written, the context still usable."""
+    ctx = Context((2, 2))
+    n = 4096
+    bufs = _bufs(4, n, 3)
+    ctx.all_reduce([b.clone() for b in bufs], "sum", "none", 256)  # binds the context
+    torch.cuda.synchronize()
+    before = [to_host(b).copy() for b in bufs]
+    outs = [torch.full((n * 4 if call == "all_gather" else n // 4,), 7.0, device="cuda") for _ in range(4)]
+    pays = [torch.zeros(2 * n, dtype=torch.uint8, device="cuda") for _ in range(2)]  # >= the E4M3 payload
+    launches = B.gb_kernel_launch_count()
+    ctx.debug_inject(B.GB_INJECT_OTHER_DEVICE)
+    with pytest.raises(GbError) as e:
+        if call == "all_reduce":
+            ctx.all_reduce(bufs, "sum", "e4m3", 256)
+        elif call == "reduce_scatter":
+            ctx.reduce_scatter(bufs, outs, "sum", "bf16", 256)
+        elif call == "all_gather":
+            ctx.all_gather(bufs, outs)
+        elif call == "broadcast":
+            ctx.broadcast(bufs, 3)
+        else:
+            ctx.island_reduce_compress(bufs, "e4m3", 256, pays)
+    assert e.value.status == B.GB_ERR_INVALID_ARG
+    assert "device" in B.gb_last_error_message(ctx.handle)
+    assert B.gb_kernel_launch_count() == launches
+    torch.cuda.synchronize()
+    for r in range(4):
+        assert np.array_equal(to_host(bufs[r]), before[r])
+    assert ctx.status() == B.GB_OK
+    ctx.all_reduce(bufs, "sum", "none", 256)  # the next call runs
+    torch.cuda.synchronize()
+    ctx.close()

@@ -1,8 +1,10 @@
 """Seeded random cases against the oracle, bit for bit: random island layouts,
 lengths, dtypes, ops, codecs, pipeline chunk sizes and rank-view offsets (16
-or 32 bytes into the allocation), through all_reduce, reduce_scatter,
-all_gather and broadcast, each call made twice on the same buffers (the
-second replays a graph where the policy captures one).  Each case is
+or 32 bytes into the allocation), through all_reduce (twice on the same
+buffers: the second replays a graph where the policy captures one; every
+third case under the sharded-bridge policy), reduce_scatter, all_gather,
+broadcast, and the same inputs as a bucket set of three through the bucket
+all_reduce and reduce_scatter then all_gather of the set.  Each case is
 reproducible from its index."""
 import numpy as np
 import pytest
@@ -82,6 +84,7 @@ def test_random_case_matches_oracle(seed):
     what = "seed %d: %s %s %s %s/%d n=%d chunk=%d" % (seed, sizes, dtype, op, codec, block, n, chunk)
     with Context(sizes) as ctx:
         ctx.set_pipeline(chunk, True)
+        ctx.set_sharded_bridge(seed % 3 == 0)  # every third case under the sharded-bridge policy
         ranks = [View(n, tdt, o) for o in offs]
         want = orc.all_reduce(xs, sizes, op, codec, block)
         for call in range(2):
@@ -118,3 +121,31 @@ def test_random_case_matches_oracle(seed):
             assert_bits_equal(to_host(bc[r].t), xs[src], "BC %s rank %d" % (what, r))
         for v in ranks + bc:
             assert v.intact(), what
+        # the same inputs as a bucket set of three (bucket sizes multiples of W for reduce_scatter)
+        if n >= 3 * W:  # (the sharded policy, where on, stays on: bucket sets keep one link under it)
+            cut = [0, (n // 3) // W * W, (2 * n // 3) // W * W, n]
+            xb = [[x[cut[b]:cut[b + 1]].copy() for x in xs] for b in range(3)]
+            bk = [[View(cut[b + 1] - cut[b], tdt, o) for o in offs] for b in range(3)]
+            for row, xr in zip(bk, xb):
+                for v, x in zip(row, xr):
+                    v.t.copy_(to_dev(x))
+            ctx.all_reduce_buckets([[v.t for v in row] for row in bk], op, codec, block)
+            torch.cuda.synchronize()
+            for b in range(3):
+                want = orc.all_reduce(xb[b], sizes, op, codec, block)
+                for r in range(W):
+                    assert_bits_equal(to_host(bk[b][r].t), want[r], "buckets %s bucket %d rank %d" % (what, b, r))
+                    assert bk[b][r].intact(), what
+            rs = [[View((cut[b + 1] - cut[b]) // W, tdt, o) for o in offs] for b in range(3)]
+            for row, xr in zip(bk, xb):
+                for v, x in zip(row, xr):
+                    v.t.copy_(to_dev(x))
+            ctx.reduce_scatter_buckets([[v.t for v in row] for row in bk], [[v.t for v in row] for row in rs], op,
+                                       codec, block)
+            ctx.all_gather_buckets([[v.t for v in row] for row in rs], [[v.t for v in row] for row in bk])
+            torch.cuda.synchronize()
+            for b in range(3):
+                want = orc.all_reduce(xb[b], sizes, op, codec, block)  # RS then AG equals AR
+                for r in range(W):
+                    assert_bits_equal(to_host(bk[b][r].t), want[r], "RS+AG buckets %s bucket %d rank %d" % (
+                        what, b, r))

@@ -487,22 +487,33 @@ def run_gb(args, world, rank, local, pg):
     link_peak = min(link["d2h_gbs"], link["h2d_gbs"])
 
     # end to end through the host-buffer entry point (pinned host buffers)
-    e2e_ms, Ke = float("nan"), 0
+    # The W host rank buffers are the rows of one pinned [W, n] tensor (staged
+    # with 2D copies by gb_all_reduce_host_rows); the same step on W separate
+    # pinned tensors (gb_all_reduce_host, one copy per rank) is reported beside.
+    e2e_ms, sep_ms, Ke = float("nan"), float("nan"), 0
     if not args.roofline_only:
+        rows = torch.from_numpy(np.stack(xs) if xs[0].dtype == np.float32 else np.stack(xs).view(np.int16))
+        rows = rows.pin_memory()
+        if xs[0].dtype != np.float32:
+            rows = rows.view(torch.bfloat16)
         host = [torch.from_numpy(x.copy()).pin_memory() if x.dtype == np.float32 else
                 torch.from_numpy(x.view(np.int16).copy()).pin_memory().view(torch.bfloat16) for x in xs]
         Ke = max(10, min(200, K // 10))
-        e_ms = []
-        with torch.cuda.stream(stream):
-            for i in range(3 + Ke):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                ctx.all_reduce_host(host, w.op, codec, w.block, stream=stream)
-                e1.record(stream)
-                e1.synchronize()
-                if i >= 3:
-                    e_ms.append(e0.elapsed_time(e1))
-        e2e_ms = max_over_ranks(pg, float(np.mean(e_ms)), dev if pg is not None else None)
+
+        def e2e_mean(bufs):
+            e_ms = []
+            with torch.cuda.stream(stream):
+                for i in range(3 + Ke):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    ctx.all_reduce_host(bufs, w.op, codec, w.block, stream=stream)
+                    e1.record(stream)
+                    e1.synchronize()
+                    if i >= 3:
+                        e_ms.append(e0.elapsed_time(e1))
+            return float(np.mean(e_ms))
+        e2e_ms = max_over_ranks(pg, e2e_mean(rows), dev if pg is not None else None)
+        sep_ms = max_over_ranks(pg, e2e_mean(host), dev if pg is not None else None)
     ctx.close()
 
     # the metric's curve: the payload sweep, on the default line at N = 1
@@ -557,7 +568,9 @@ def run_gb(args, world, rank, local, pg):
                    if bridge_ms > 0 else None},
         "e2e": {"value": world * n * b / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "steps": Ke, "h2d_bytes_per_step": W * n * b, "d2h_bytes_per_step": W * n * b,
-                "api": "gb_all_reduce_host (pinned host rank buffers)"},
+                "api": "gb_all_reduce_host_rows (the W pinned host rank buffers as the rows of one [W, n] tensor)",
+                "separate_buffers": {"ms_per_step": sep_ms, "value": world * n * b / (sep_ms * 1e-3) / 1e9,
+                                     "api": "gb_all_reduce_host (W separate pinned host tensors)"}},
         "gpu_launches": int(launches),
         "timed_wall_s": t_wall,
         "clocks": clk,

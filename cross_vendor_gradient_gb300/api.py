@@ -46,6 +46,22 @@ def _dtype(tensors):
     return _DTYPES[dt]
 
 
+def _row_pitch(tensors):
+    """The byte distance between consecutive tensors when all of them lie in
+    one storage (one host allocation) at equal, ascending spacing of at
+    least one tensor's bytes; else None."""
+    if len(tensors) < 2:
+        return None
+    base = tensors[0].untyped_storage().data_ptr()
+    if any(t.untyped_storage().data_ptr() != base for t in tensors[1:]):
+        return None
+    nb = tensors[0].numel() * tensors[0].element_size()
+    pitch = tensors[1].data_ptr() - tensors[0].data_ptr()
+    if pitch < nb or any(t.data_ptr() != tensors[0].data_ptr() + r * pitch for r, t in enumerate(tensors)):
+        return None
+    return pitch
+
+
 def payload_bytes(codec, block, n):
     return B.gb_payload_bytes(_codec(codec), block, n)
 
@@ -161,10 +177,24 @@ class Context:
                                    src, _stream(stream)))
 
     def all_reduce_host(self, host_tensors, op="sum", codec="none", block=256, stream=None):
+        """host_tensors: W host tensors (pinned for asynchronous copies), or
+        one [W, n] host tensor whose rows are the ranks.  Rows of one
+        storage at equal, ascending spacing go through
+        gb_all_reduce_host_rows (2D staging copies); anything else through
+        gb_all_reduce_host."""
+        if isinstance(host_tensors, torch.Tensor):
+            if host_tensors.dim() != 2:
+                raise GbError(B.GB_ERR_INVALID_ARG, "a host tensor of ranks must be [W, n]")
+            host_tensors = list(host_tensors.unbind(0))
         dt = _dtype(host_tensors)
-        self._check(B.gb_all_reduce_host(self.handle, [t.data_ptr() for t in host_tensors],
-                                         host_tensors[0].numel(), dt, _op(op), _codec(codec), block,
-                                         _stream(stream)))
+        n = host_tensors[0].numel()
+        pitch = _row_pitch(host_tensors)
+        if pitch is not None:
+            self._check(B.gb_all_reduce_host_rows(self.handle, host_tensors[0].data_ptr(), pitch, n, dt, _op(op),
+                                                  _codec(codec), block, _stream(stream)))
+            return
+        self._check(B.gb_all_reduce_host(self.handle, [t.data_ptr() for t in host_tensors], n, dt, _op(op),
+                                         _codec(codec), block, _stream(stream)))
 
     def all_reduce_buckets(self, buckets, op="sum", codec="none", block=256, stream=None):
         """buckets: list of per-bucket lists of W flat tensors."""

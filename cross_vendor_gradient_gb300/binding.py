@@ -76,6 +76,7 @@ SIGNATURES = {
     "gb_all_gather": (_i, [_vp, _P(_vp), _P(_vp), _sz, _i, _vp]),
     "gb_broadcast": (_i, [_vp, _P(_vp), _sz, _i, _i, _vp]),
     "gb_all_reduce_host": (_i, [_vp, _P(_vp), _sz, _i, _i, _i, _i, _vp]),
+    "gb_all_reduce_host_rows": (_i, [_vp, _vp, _sz, _sz, _i, _i, _i, _i, _vp]),
     "gb_bucket_plan": (_i, [_P(_sz), _i, _sz, _sz, _sz, _P(_i), _P(_sz), _P(_sz), _i, _P(_i)]),
     "gb_all_reduce_buckets": (_i, [_vp, _i, _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
     "gb_all_reduce_buckets_ef": (_i, [_vp, _i, _P(_vp), _P(_vp), _P(_sz), _i, _i, _i, _i, _vp]),
@@ -257,6 +258,10 @@ def gb_broadcast(ctx, rank_bufs, n, dtype, src, stream=0):
 
 def gb_all_reduce_host(ctx, host_bufs, n, dtype, op, codec, block, stream=0):
     return lib().gb_all_reduce_host(ctx, _ptrs(host_bufs), n, dtype, op, codec, block, stream)
+
+
+def gb_all_reduce_host_rows(ctx, host, pitch, n, dtype, op, codec, block, stream=0):
+    return lib().gb_all_reduce_host_rows(ctx, host, pitch, n, dtype, op, codec, block, stream)
 
 
 def gb_bucket_plan(numel, elem_bytes, cap_bytes, pad_elems=1, max_buckets=None):

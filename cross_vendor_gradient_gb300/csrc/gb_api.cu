@@ -607,14 +607,12 @@ gb_status gb_broadcast(gb_ctx *c, void *const *rank_bufs, size_t n, gb_dtype dty
     return I > 1 ? end(c, s) : GB_OK;
 }
 
-gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dtype dtype, gb_op op,
-                             gb_codec codec, int block, gb_stream stream) {
-    GB_TRY(check_ctx(c));
-    GB_TRY(check_collective(c, n, dtype, op, codec, block));
-    if (!host_bufs) return set_msg(c, GB_ERR_INVALID_ARG, "host_bufs is NULL");
-    for (int r = 0; r < c->W; ++r)
-        if (!host_bufs[r]) return set_msg(c, GB_ERR_INVALID_ARG, "host_bufs[%d] is NULL", r);
-    if (n == 0) return GB_OK;
+// The body of gb_all_reduce_host and gb_all_reduce_host_rows, after their
+// argument checks.  row_pitch > 0: the host buffers are the rows of one host
+// allocation, row_pitch bytes apart, staged with 2D copies when the device
+// takes both pitches.
+static gb_status host_all_reduce(gb_ctx *c, void *const *host_bufs, size_t row_pitch, size_t n, gb_dtype dtype,
+                                 gb_op op, gb_codec codec, int block, gb_stream stream) {
     GB_TRY(bind(c));
     cudaStream_t s = (cudaStream_t)stream;
     const size_t nb = n * elem_bytes(dtype);
@@ -622,6 +620,7 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
     GB_TRY(grow_device(c, &c->d_ranks, &c->d_ranks_bytes, (size_t)c->W * stride));
     void *dev[GB_MAX_RANKS];
     for (int r = 0; r < c->W; ++r) dev[r] = c->d_ranks + (size_t)r * stride;
+    const size_t hpitch = row_pitch && row_pitch <= c->max_pitch && stride <= c->max_pitch ? row_pitch : 0;
     // chunks of half the pipeline chunk: here every chunk also carries W rank
     // buffers' worth of staging in and out, so the pipeline's fill and drain
     // weigh more (1 MiB beat 0.5, 0.75, 1.5 and 2 MiB on GB300).  The
@@ -634,7 +633,7 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
         GB_TRY(grow_host(c, p.host_bytes));
         GB_TRY(begin(c, s));
         if (!c->use_graphs) {
-            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, s));
+            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, stride, hpitch, s));
             return end(c, s);
         }
         GraphKey k;
@@ -645,6 +644,7 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
         }
         k.n = n;
         k.chunk = p.chunk;
+        k.host_pitch = hpitch;
         k.dtype = dtype;
         k.op = op;
         k.codec = p.eff;
@@ -656,14 +656,14 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
             ge = new_graph_slot(c);
             ge->key = k;
             ge->last_use = ++c->clock;
-            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, s));
+            GB_TRY(enqueue_host_pipeline(c, p, host_bufs, dev, stride, hpitch, s));
             return end(c, s);
         }
         ge->last_use = ++c->clock;
         if (!ge->exec) {
             cudaError_t e = cudaStreamBeginCapture(c->scap, cudaStreamCaptureModeThreadLocal);
             if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaStreamBeginCapture", e);
-            gb_status st = enqueue_host_pipeline(c, p, host_bufs, dev, c->scap);
+            gb_status st = enqueue_host_pipeline(c, p, host_bufs, dev, stride, hpitch, c->scap);
             cudaGraph_t g = nullptr;
             e = cudaStreamEndCapture(c->scap, &g);
             if (st != GB_OK) {
@@ -685,16 +685,39 @@ gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dty
         return end(c, s);
     }
     GB_TRY(begin(c, s));
-    for (int r = 0; r < c->W; ++r) {
-        cudaError_t e = cudaMemcpyAsync(dev[r], host_bufs[r], nb, cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "host -> device staging", e);
-    }
+    GB_TRY(stage_ranks(c, host_bufs, dev, stride, hpitch, 0, nb, cudaMemcpyHostToDevice, s));
     GB_TRY(run_rbb(c, (const void *const *)dev, dev, n, dtype, op, codec, block, s, 0));
-    for (int r = 0; r < c->W; ++r) {
-        cudaError_t e = cudaMemcpyAsync(host_bufs[r], dev[r], nb, cudaMemcpyDeviceToHost, s);
-        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "device -> host copy back", e);
-    }
+    GB_TRY(stage_ranks(c, host_bufs, dev, stride, hpitch, 0, nb, cudaMemcpyDeviceToHost, s));
     return end(c, s);
+}
+
+gb_status gb_all_reduce_host(gb_ctx *c, void *const *host_bufs, size_t n, gb_dtype dtype, gb_op op,
+                             gb_codec codec, int block, gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_collective(c, n, dtype, op, codec, block));
+    if (!host_bufs) return set_msg(c, GB_ERR_INVALID_ARG, "host_bufs is NULL");
+    for (int r = 0; r < c->W; ++r)
+        if (!host_bufs[r]) return set_msg(c, GB_ERR_INVALID_ARG, "host_bufs[%d] is NULL", r);
+    if (n == 0) return GB_OK;
+    return host_all_reduce(c, host_bufs, 0, n, dtype, op, codec, block, stream);
+}
+
+gb_status gb_all_reduce_host_rows(gb_ctx *c, void *host, size_t pitch, size_t n, gb_dtype dtype, gb_op op,
+                                  gb_codec codec, int block, gb_stream stream) {
+    GB_TRY(check_ctx(c));
+    GB_TRY(check_collective(c, n, dtype, op, codec, block));
+    if (!host) return set_msg(c, GB_ERR_INVALID_ARG, "host is NULL");
+    if (n == 0) return GB_OK;
+    const size_t nb = n * elem_bytes(dtype);
+    if (c->W > 1 && pitch < nb)
+        return set_msg(c, GB_ERR_INVALID_ARG, "pitch %zu is below a row's %zu bytes: the rows would overlap", pitch,
+                       nb);
+    if (c->W > 1 && pitch > (UINTPTR_MAX - (uintptr_t)host) / (size_t)(c->W - 1))
+        return set_msg(c, GB_ERR_INVALID_ARG, "pitch %zu puts the last row past the end of the address space",
+                       pitch);
+    void *rows[GB_MAX_RANKS];
+    for (int r = 0; r < c->W; ++r) rows[r] = (unsigned char *)host + (size_t)r * pitch;
+    return host_all_reduce(c, rows, c->W > 1 ? pitch : 0, n, dtype, op, codec, block, stream);
 }
 
 gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes_, size_t cap_bytes,

@@ -40,6 +40,7 @@ struct GraphKey {
     const void *host[GB_MAX_RANKS];  // gb_all_reduce_host: the host rank buffers
     const void *res[GB_MAX_ISLANDS];
     uint64_t n, chunk;
+    uint64_t host_pitch;  // gb_all_reduce_host_rows: 2D staging copies at this host pitch
     int dtype, op, codec, block, timed, links;
     const void *d_stage, *h_stage;
 };
@@ -73,6 +74,7 @@ struct gb_ctx {
     // device copies of host rank buffers (gb_all_reduce_host)
     unsigned char *d_ranks = nullptr;
     size_t d_ranks_bytes = 0;
+    size_t max_pitch = 0;  // cudaDevAttrMaxPitch of the bound device (2D copies)
     // ordering of staging reuse across calls
     cudaEvent_t done = nullptr;
     bool done_recorded = false;
@@ -203,7 +205,14 @@ gb_status record(gb_ctx *c, cudaEvent_t ev, cudaStream_t s);
 gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *const *out,
                       float *const *res, cudaStream_t s, int markmode, bool multi);
 gb_status ensure_links(gb_ctx *c, int L);
-gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, cudaStream_t s);
+// Rank staging of gb_all_reduce_host(_rows): `dev` is the context's rank
+// copies at `dpitch` bytes apart; hpitch > 0 says that the host buffers are
+// the rows of one host allocation, hpitch bytes apart: one 2D copy moves
+// every rank's bytes [off, off + bytes).
+gb_status stage_ranks(gb_ctx *c, void *const *host, void *const *dev, size_t dpitch, size_t hpitch, size_t off,
+                      size_t bytes, cudaMemcpyKind kind, cudaStream_t s);
+gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, size_t dpitch,
+                                size_t hpitch, cudaStream_t s);
 gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk> &work, const void *const *in,
                           void *const *out, const size_t *numel, int rs, float *const *res, cudaStream_t s);
 gb_status run_set_graph(gb_ctx *c, const std::vector<uint64_t> &key, int kernels,

@@ -160,6 +160,9 @@ gb_status bind(gb_ctx *c) {
                 return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
         for (int i = 0; i < kMarks; ++i)
             if ((e = cudaEventCreate(&c->cap_mark[i])) != cudaSuccess) return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
+        int mp = 0;
+        if (cudaDeviceGetAttribute(&mp, cudaDevAttrMaxPitch, dev) == cudaSuccess && mp > 0) c->max_pitch = (size_t)mp;
+        cudaGetLastError();
         c->device = dev;
     } else if (dev != c->device) {
         return set_msg(c, GB_ERR_INVALID_ARG, "context is bound to device %d, current device is %d",
@@ -583,13 +586,43 @@ gb_status ensure_links(gb_ctx *c, int L) {
     return GB_OK;
 }
 
+// Staging of the host rank buffers.  Every cudaMemcpyAsync pays a fixed
+// cost of a few microseconds on its copy stream, and the host-buffer
+// pipeline would issue W of them per chunk in each direction; when the
+// buffers are the rows of one host allocation (hpitch > 0) a single 2D copy
+// moves every rank's part.  (Equal spacing alone is not enough: separate
+// pinned allocations can lie at equal distances, and the runtime refuses a
+// 2D copy that spans several allocations.)
+// Bytes [off, off + bytes) of every rank buffer between the host buffers and
+// the context's rank copies, in the direction `kind`.
+gb_status stage_ranks(gb_ctx *c, void *const *host, void *const *dev, size_t dpitch, size_t hpitch, size_t off,
+                      size_t bytes, cudaMemcpyKind kind, cudaStream_t s) {
+    if (bytes == 0) return GB_OK;
+    const bool in = kind == cudaMemcpyHostToDevice;
+    const char *what = in ? "host -> device staging" : "device -> host copy back";
+    if (hpitch) {
+        unsigned char *d0 = (unsigned char *)dev[0] + off, *h0 = (unsigned char *)host[0] + off;
+        cudaError_t e = in ? cudaMemcpy2DAsync(d0, dpitch, h0, hpitch, bytes, (size_t)c->W, kind, s)
+                           : cudaMemcpy2DAsync(h0, hpitch, d0, dpitch, bytes, (size_t)c->W, kind, s);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, what, e);
+        return GB_OK;
+    }
+    for (int r = 0; r < c->W; ++r) {
+        unsigned char *d = (unsigned char *)dev[r] + off, *h = (unsigned char *)host[r] + off;
+        cudaError_t e = in ? cudaMemcpyAsync(d, h, bytes, kind, s) : cudaMemcpyAsync(h, d, bytes, kind, s);
+        if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, what, e);
+    }
+    return GB_OK;
+}
+
 // gb_all_reduce_host, pipelined: chunk c of every host rank buffer goes to
 // the device (copy stream H), is encoded (s), its payload crosses the
 // bridge (D, then H), is decoded into the device rank chunks (s) and copied
 // back to the host buffers (D).  Issued one chunk ahead so that both copy
 // directions stay busy: H carries in(0), in(1), bridge-in(0), in(2), ...; D
 // carries bridge-out(0), bridge-out(1), out(0), bridge-out(2), out(1), ...
-gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, cudaStream_t s) {
+gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, size_t dpitch,
+                                size_t hpitch, cudaStream_t s) {
     const int I = p.I, W = p.W;
     auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
     auto inbox = [&](int g, int ch, int j) {
@@ -610,11 +643,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
     auto issue_front = [&](int ch) -> gb_status {  // in(ch), encode(ch), bridge-out(ch)
         uint64_t e0, m;
         range(ch, &e0, &m);
-        for (int r = 0; r < W; ++r) {
-            cudaError_t e = cudaMemcpyAsync((unsigned char *)dev[r] + e0 * p.eb, (const unsigned char *)host[r] + e0 * p.eb,
-                                            m * p.eb, cudaMemcpyHostToDevice, H);
-            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "host -> device staging", e);
-        }
+        GB_TRY(stage_ranks(c, host, dev, dpitch, hpitch, e0 * p.eb, m * p.eb, cudaMemcpyHostToDevice, H));
         GB_TRY(record(c, c->ev_in[ch], H));
         GB_TRY(wait_on(c, s, c->ev_in[ch]));
         gb::ReduceEncodeArgs ra;
@@ -678,11 +707,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
         GB_TRY(launch_decode(c, p, da, s));
         GB_TRY(record(c, c->ev_k2[ch], s));
         GB_TRY(wait_on(c, D, c->ev_k2[ch]));
-        for (int r = 0; r < W; ++r) {
-            cudaError_t e = cudaMemcpyAsync((unsigned char *)host[r] + e0 * p.eb, (const unsigned char *)dev[r] + e0 * p.eb,
-                                            m * p.eb, cudaMemcpyDeviceToHost, D);
-            if (e != cudaSuccess) return fail(c, GB_ERR_CUDA, "device -> host copy back", e);
-        }
+        GB_TRY(stage_ranks(c, host, dev, dpitch, hpitch, e0 * p.eb, m * p.eb, cudaMemcpyDeviceToHost, D));
         return GB_OK;
     };
     GB_TRY(issue_front(0));

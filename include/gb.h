@@ -406,6 +406,23 @@ gb_status gb_broadcast(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype d
 gb_status gb_all_reduce_host(gb_ctx *ctx, void *const *host_bufs, size_t n, gb_dtype dtype,
                              gb_op op, gb_codec codec, int block, gb_stream stream);
 
+/* gb_all_reduce_host for W host rank buffers that are the rows of ONE host
+ * allocation: rank r's n elements start at host + r * pitch bytes, as in a
+ * pinned [W, n] tensor (pitch >= n * element bytes when W > 1; ignored when
+ * W == 1).  Same semantics, ordering and results as gb_all_reduce_host.
+ * The staging and the copy-back move every rank's chunk with one 2D copy
+ * (cudaMemcpy2DAsync) per chunk and direction instead of W copies, each of
+ * which costs a few microseconds of fixed time on its copy stream.  The rows
+ * must lie in one allocation: the CUDA runtime refuses a 2D copy across
+ * separate ones (even at equal spacing), which fails the call and the
+ * context with GB_ERR_CUDA.  A pitch beyond the device's 2D copy limit
+ * (cudaDevAttrMaxPitch) is staged row by row instead.  Errors as
+ * gb_all_reduce_host, plus GB_ERR_INVALID_ARG for a NULL host, pitch
+ * < n * element bytes (rows that would overlap) or rows past the end of the
+ * address space. */
+gb_status gb_all_reduce_host_rows(gb_ctx *ctx, void *host, size_t pitch, size_t n, gb_dtype dtype,
+                                  gb_op op, gb_codec codec, int block, gb_stream stream);
+
 /* ------------------------------------------------------ gradient buckets */
 
 /* Greedy bucket plan (gpubridge README, DDP comm hook: one all_reduce per

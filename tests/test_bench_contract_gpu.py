@@ -49,6 +49,7 @@ def test_default_line_contract():
     e = d["e2e"]
     assert e["unit"] == "GB/s" and e["h2d_bytes_per_step"] == 4 * n * 4 and e["d2h_bytes_per_step"] == 4 * n * 4
     assert 0 < e["value"] < d["value"]  # the host link bounds it below the device-resident step
+    assert "rows" in e["api"] and e["separate_buffers"]["ms_per_step"] > 0  # both host layouts timed
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
     assert d["gpu_launches"] == 20 * 8  # 4 chunks x (encode + decode) per graph-replayed step

@@ -541,8 +541,10 @@ def run_gb(args, world, rank, local, pg):
                    "policy": (("sharded-bridge, %d links%s" % (
                        min(w.island_sizes), ", CUDA graph replay" if not args.no_graphs else ""))
                               if args.sharded and min(w.island_sizes) > 1 else
-                              ("pipelined-reduce-bridge-broadcast, equal payload chunks of at most %d KiB%s" % (
-                                  chunk_bytes >> 10, ", CUDA graph replay" if not args.no_graphs else ""))
+                              ("pipelined-reduce-bridge-broadcast, equal payload chunks of at most %d KiB x "
+                               "max(1, sqrt(P / (3 x %d KiB))) for one island's payload P%s" % (
+                                  chunk_bytes >> 10, chunk_bytes >> 10,
+                                  ", CUDA graph replay" if not args.no_graphs else ""))
                               if chunk_bytes else "reduce-bridge-broadcast"),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB "
                                      "read so that no dirty line is left); inputs restored from a device "

@@ -26,6 +26,7 @@ constexpr int kMarks = 4 + 2 * kMaxChunks;
 constexpr int kMaxGraphs = 16;
 // sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
 constexpr int kMaxLinks = 8;
+constexpr double kChunkGrowRef = 3.0;    // single-buffer all_reduce: the chunk grows beyond 3 chunks of payload
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
 constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
 constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2

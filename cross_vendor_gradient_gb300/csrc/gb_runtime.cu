@@ -2,6 +2,8 @@
 // buffers, timing marks, and the pipelines that compose the kernels with the
 // bridge hop through pinned host memory.  The C entry points are in
 // gb_api.cu; the contracts in include/gb.h.
+#include <cmath>
+
 #include "gb_internal.cuh"
 
 namespace gbrt {
@@ -321,6 +323,7 @@ size_t part_bytes(const Plan &p, uint64_t m) {
 
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
                bool sharded_ok, size_t chunk_bytes, bool balance) {
+    const bool grow = chunk_bytes == 0;  // the single-buffer all_reduce's chunk: grows with the payload
     if (chunk_bytes == 0) chunk_bytes = c->chunk_bytes;
     Plan p;
     p.I = c->I;
@@ -348,7 +351,19 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
     } else if (c->I > 1 && chunk_bytes > 0) {
         // chunk_bytes of one island's payload per chunk
         const double per_elem = (double)p.cb + (is_fp8(p.eff) ? 4.0 / p.blk : 0.0);
-        uint64_t ch = (uint64_t)((double)chunk_bytes / per_elem) / gb::kTile * gb::kTile;
+        // The pipeline's fill and drain (the first chunk's device -> host copy
+        // and the last one's host -> device copy, each alone on the link)
+        // grow with the chunk; the copies' fixed costs grow with the chunk
+        // count.  Their sum is least at a count proportional to sqrt(P), so
+        // above kChunkGrowRef chunks' worth of one island's payload P the
+        // chunk grows as sqrt(P / (kChunkGrowRef * chunk_bytes)).  On GB300
+        // this matched the best fixed chunk of 2 .. 16 MiB measured at 16 ..
+        // 256 MiB per rank for every codec (64 MiB uncompressed: 947 us
+        // against 1099 us with 2 MiB chunks).
+        double cbytes = (double)chunk_bytes;
+        const double P = per_elem * (double)n;
+        if (grow && !rs && P > kChunkGrowRef * cbytes) cbytes *= sqrt(P / (kChunkGrowRef * cbytes));
+        uint64_t ch = (uint64_t)(cbytes / per_elem) / gb::kTile * gb::kTile;
         if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
         const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
         if (ch < min_ch) ch = min_ch;

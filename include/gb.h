@@ -174,9 +174,13 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  *   chunk_bytes > 0 (default 2 MiB, measured best on GB300 for 25 MiB
  *     buckets; the README's policy defaults to 4M): pipelined-
  *     reduce-bridge-broadcast.  The leaders' bridge step is cut into the
- *     fewest chunks of at most about chunk_bytes of one island's payload,
+ *     fewest chunks of at most about S bytes of one island's payload P,
  *     of equal size (whole 256-element tiles, at least one tile, at most 32
- *     chunks per call); chunk c's device ->
+ *     chunks per call), where for gb_all_reduce and gb_all_reduce_ef
+ *     S = chunk_bytes while P <= 3 * chunk_bytes and
+ *     S = chunk_bytes * sqrt(P / (3 * chunk_bytes)) above (the fill and
+ *     drain of the pipeline grow with the chunk, the copies' fixed costs
+ *     with the chunk count); chunk c's device ->
  *     host copy, chunk c-1's host -> device copy and the kernels of other
  *     chunks overlap on the context's two copy streams, ordered with CUDA
  *     events.  Chunks are whole codec blocks, so the result is the same

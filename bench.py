@@ -1132,7 +1132,7 @@ def run_collective(args, world, rank, local, pg):
     k1, br, k2 = (float(np.mean(ph[:, j])) for j in range(3))
     P = payload_bytes(codec, w.block, n) if coll == "reduce_scatter" else m * b
     if coll == "reduce_scatter":
-        kern = [("k_reduce_encode", W * n * b + I * P, k1), ("k_decode_bcast (slices)", I * P + n * b, k2)]
+        kern = [("k_reduce_encode", W * n * b + I * P, k1), ("k_decode_slices", I * P + n * b, k2)]
         link = I * P + I * (I - 1) * P
     elif coll == "all_gather":
         kern = [("k_copy", W * m * b + W * W * m * b, k2)]
@@ -1149,7 +1149,7 @@ def run_collective(args, world, rank, local, pg):
     Kb = max(3, min(K, 20))
     if coll == "reduce_scatter":
         ks = kernel_stream(ctx, pristine, I, P, codec, w.block, w.op, stream, clean, 1, Kb,
-                           ("k_reduce_encode", "k_decode_bcast (slices)"), scatter=True)
+                           ("k_reduce_encode", "k_decode_slices"), scatter=True)
         b2b = [(k, nb, ks[k]) for k, nb, _ in kern]
         sets_used = ks["sets"]
     else:
@@ -1183,8 +1183,10 @@ def run_collective(args, world, rank, local, pg):
                                "(n=%d), %s%s" % (w.key, W, list(w.island_sizes), coll, n * b / 2 ** 20, n, w.dist,
                                                  (", op %s, codec %s block %d" % (w.op, codec, w.block))
                                                  if coll == "reduce_scatter" else ", exact"),
-                   "policy": {"reduce_scatter": "pipelined, equal payload chunks of at most %d KiB" % (
-                                  chunk_bytes >> 11),
+                   "policy": {"reduce_scatter": "pipelined, equal payload chunks of at most max(%d KiB, S - %d KiB), "
+                                                "S = %d KiB x max(1, sqrt(P / (3 x %d KiB))) for one island's "
+                                                "payload P" % (chunk_bytes >> 11, chunk_bytes >> 11,
+                                                               chunk_bytes >> 10, chunk_bytes >> 10),
                               "all_gather": "pipelined, groups of whole rank blocks of about %d KiB" % (
                                   chunk_bytes >> 10),
                               "broadcast": "pipelined, equal pieces of up to %d KiB" % (chunk_bytes >> 8)}[coll]

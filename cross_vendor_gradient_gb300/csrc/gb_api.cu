@@ -115,7 +115,7 @@ gb_status gb_reserve(gb_ctx *c, size_t n, gb_dtype dtype, gb_codec codec, int bl
     GB_TRY(check_n(c, n));
     GB_TRY(bind(c));
     const Plan ar = make_plan(c, n, dtype, GB_SUM, codec, block, 0, true);
-    const Plan rs = make_plan(c, n, dtype, GB_SUM, codec, block, 1, false, c->chunk_bytes / kRsChunkDiv);
+    const Plan rs = make_plan(c, n, dtype, GB_SUM, codec, block, 1, false);
     const size_t ag_host = (size_t)c->W * n * elem_bytes(dtype);
     size_t dev = ar.dev_bytes > rs.dev_bytes ? ar.dev_bytes : rs.dev_bytes;
     size_t host = ar.host_bytes > rs.host_bytes ? ar.host_bytes : rs.host_bytes;

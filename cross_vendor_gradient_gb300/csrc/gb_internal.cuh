@@ -30,7 +30,7 @@ constexpr double kChunkGrowRef = 3.0;    // single-buffer all_reduce: the chunk 
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
 constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
 constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2
-constexpr size_t kRsChunkDiv = 2;        // gb_reduce_scatter: chunk = the pipeline chunk / 2
+constexpr size_t kRsChunkDiv = 2;        // gb_reduce_scatter: chunk = the all_reduce chunk - the pipeline chunk / 2, >= chunk / 2
 constexpr size_t kBcastPieceScale = 4;   // gb_broadcast: pieces of up to 4 x the pipeline chunk
 constexpr uint64_t kMaxElems = 1ull << 38;
 }  // namespace gbrt

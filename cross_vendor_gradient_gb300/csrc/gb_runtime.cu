@@ -323,7 +323,9 @@ size_t part_bytes(const Plan &p, uint64_t m) {
 
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
                bool sharded_ok, size_t chunk_bytes, bool balance) {
-    const bool grow = chunk_bytes == 0;  // the single-buffer all_reduce's chunk: grows with the payload
+    // chunk_bytes == 0: the single-buffer all_reduce's or reduce_scatter's
+    // chunk, derived from the pipeline chunk and grown with the payload
+    const bool grow = chunk_bytes == 0;
     if (chunk_bytes == 0) chunk_bytes = c->chunk_bytes;
     Plan p;
     p.I = c->I;
@@ -356,13 +358,22 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
         // grow with the chunk; the copies' fixed costs grow with the chunk
         // count.  Their sum is least at a count proportional to sqrt(P), so
         // above kChunkGrowRef chunks' worth of one island's payload P the
-        // chunk grows as sqrt(P / (kChunkGrowRef * chunk_bytes)).  On GB300
-        // this matched the best fixed chunk of 2 .. 16 MiB measured at 16 ..
-        // 256 MiB per rank for every codec (64 MiB uncompressed: 947 us
-        // against 1099 us with 2 MiB chunks).
+        // all_reduce chunk grows as sqrt(P / (kChunkGrowRef * chunk_bytes)).
+        // On GB300 this matched the best fixed chunk of 2 .. 16 MiB measured
+        // at 16 .. 256 MiB per rank for every codec (64 MiB uncompressed:
+        // 947 us against 1099 us with 2 MiB chunks).  reduce_scatter's
+        // decodes write only the slices, so its drain is shorter: it takes
+        // that chunk less half the pipeline chunk, at least half of it (the
+        // half chunk up to 3 chunks of payload; on the 25 MiB float32 E4M3
+        // bucket 147 us against 152 us with whole chunks; at 256 MiB E4M3 991
+        // us against 1107 us with half chunks).
         double cbytes = (double)chunk_bytes;
         const double P = per_elem * (double)n;
-        if (grow && !rs && P > kChunkGrowRef * cbytes) cbytes *= sqrt(P / (kChunkGrowRef * cbytes));
+        if (grow) {
+            const double s_ar = P > kChunkGrowRef * cbytes ? cbytes * sqrt(P / (kChunkGrowRef * cbytes)) : cbytes;
+            const double half = cbytes / (double)kRsChunkDiv;
+            cbytes = !rs ? s_ar : s_ar - half > half ? s_ar - half : half;
+        }
         uint64_t ch = (uint64_t)(cbytes / per_elem) / gb::kTile * gb::kTile;
         if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
         const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
@@ -1105,9 +1116,8 @@ gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *con
 // buffers and shape (the first runs directly) and replayed afterwards.
 gb_status run_rbb(gb_ctx *c, const void *const *in, void *const *out, size_t n, gb_dtype dtype,
                   gb_op op, gb_codec codec, int block, cudaStream_t s, int rs, float *const *res) {
-    // reduce_scatter's decodes write only the slices, so its chunks are half
-    // the size (on GB300, 25 MiB float32 E4M3: 147 us with 1 MiB, 152 us with 2 MiB)
-    const Plan p = make_plan(c, n, dtype, op, codec, block, rs, true, rs ? c->chunk_bytes / kRsChunkDiv : 0);
+    // the chunk follows the payload; reduce_scatter's is shorter (make_plan)
+    const Plan p = make_plan(c, n, dtype, op, codec, block, rs, true);
     GB_TRY(ensure_links(c, p.links));
     GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));
     if (p.host_bytes) GB_TRY(grow_host(c, p.host_bytes));

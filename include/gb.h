@@ -188,8 +188,9 @@ gb_status gb_reserve(gb_ctx *ctx, size_t n, gb_dtype dtype, gb_codec codec, int 
  *   use_graphs != 0 (default): a pipelined call is captured into a CUDA
  *     graph the second time the same buffers and shape are seen, and
  *     replayed from then on (one launch instead of a few dozen).
- * reduce_scatter follows the same policy with chunks of half chunk_bytes
- * (its chunks' decodes write the parts of the slices they cover).
+ * reduce_scatter follows the same policy with chunks of at most
+ * max(chunk_bytes / 2, S - chunk_bytes / 2) (its chunks' decodes write only
+ * the parts of the slices they cover, so its drain is shorter).
  * all_gather with chunk_bytes > 0 moves groups of whole rank blocks of
  * about chunk_bytes: one group's host -> device copies overlap the next
  * group's device -> host copies.  broadcast with chunk_bytes > 0 moves the

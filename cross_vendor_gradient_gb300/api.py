@@ -186,6 +186,8 @@ class Context:
             if host_tensors.dim() != 2:
                 raise GbError(B.GB_ERR_INVALID_ARG, "a host tensor of ranks must be [W, n]")
             host_tensors = list(host_tensors.unbind(0))
+        if any(t.device.type != "cpu" for t in host_tensors):
+            raise GbError(B.GB_ERR_INVALID_ARG, "all_reduce_host takes host (CPU) tensors; use all_reduce for CUDA tensors")
         dt = _dtype(host_tensors)
         n = host_tensors[0].numel()
         pitch = _row_pitch(host_tensors)

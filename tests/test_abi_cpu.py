@@ -245,3 +245,20 @@ def test_plain_c_caller(tmp_path):
     assert got["status_string"] == "GB_ERR_MISALIGNED"
     _, _, bn = orc.bucket_plan([600, 500, 1200, 10, 990], 4, 4000, 1)
     assert got["plan"].split() == ["0", str(len(bn))] + [str(int(v)) for v in bn]
+
+
+def test_host_rows_detection():
+    """Context.all_reduce_host takes the rows entry point only for equally
+    spaced, ascending rows of one storage at least a row apart."""
+    import torch
+    from cross_vendor_gradient_gb300.api import _row_pitch
+    blk = torch.zeros((4, 1000))
+    assert _row_pitch(list(blk.unbind(0))) == 4000
+    padded = torch.zeros((4, 1040))
+    assert _row_pitch([padded[r, 20:1020] for r in range(4)]) == 4160
+    assert _row_pitch([blk[r] for r in (3, 2, 1, 0)]) is None  # descending
+    assert _row_pitch([blk[r] for r in (0, 1, 3, 2)]) is None  # not equally spaced
+    assert _row_pitch([torch.zeros(1000) for _ in range(4)]) is None  # separate storages
+    assert _row_pitch([blk[0]]) is None  # one rank: the pointer entry point
+    flat = torch.zeros(4000)
+    assert _row_pitch([flat[r * 900:r * 900 + 1000] for r in range(4)]) is None  # overlapping rows

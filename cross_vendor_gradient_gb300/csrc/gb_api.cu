@@ -621,12 +621,17 @@ static gb_status host_all_reduce(gb_ctx *c, void *const *host_bufs, size_t row_p
     void *dev[GB_MAX_RANKS];
     for (int r = 0; r < c->W; ++r) dev[r] = c->d_ranks + (size_t)r * stride;
     const size_t hpitch = row_pitch && row_pitch <= c->max_pitch && stride <= c->max_pitch ? row_pitch : 0;
-    // chunks of half the pipeline chunk: here every chunk also carries W rank
-    // buffers' worth of staging in and out, so the pipeline's fill and drain
-    // weigh more (1 MiB beat 0.5, 0.75, 1.5 and 2 MiB on GB300).  The
-    // chunks are not balanced: a short last chunk shortens the drain of the
-    // copy back to the host (25.2-25.7 GB/s, against 24.8-25.0 balanced)
-    const Plan p = make_plan(c, n, dtype, op, codec, block, 0, false, c->chunk_bytes / kHostChunkDiv, false);
+    // Every chunk here also carries W rank buffers' worth of staging in and
+    // out, which outweighs its payload, so a chunk is sized by that staging:
+    // the elements whose W rank slices total kHostStageScale pipeline chunks
+    // (16 MiB at the default).  On GB300 this kept the 25 MiB float32 E4M3
+    // step (951 against 951 us with chunks of 1 MiB of payload, the earlier
+    // rule) and took 64 MiB uncompressed from 2940 to 2792 us.  The chunks
+    // are not balanced: a short last chunk shortens the drain of the copy
+    // back to the host (25.2-25.7 GB/s, against 24.8-25.0 balanced).
+    const uint64_t stage_elems = (uint64_t)(kHostStageScale * c->chunk_bytes) / ((uint64_t)c->W * elem_bytes(dtype));
+    const Plan p = make_plan(c, n, dtype, op, codec, block, 0, false, c->chunk_bytes, false,
+                             stage_elems > 0 ? stage_elems : 1);
     if (p.C > 1 && c->tcap == 0) {
         // pipelined: staging in, bridge and copy-back overlap chunk by chunk
         GB_TRY(grow_device(c, &c->d_stage, &c->d_stage_bytes, p.dev_bytes));

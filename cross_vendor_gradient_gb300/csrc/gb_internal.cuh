@@ -29,7 +29,7 @@ constexpr int kMaxLinks = 8;
 constexpr double kChunkGrowRef = 3.0;    // single-buffer all_reduce: the chunk grows beyond 3 chunks of payload
 constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
 constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
-constexpr size_t kHostChunkDiv = 2;      // gb_all_reduce_host: chunk = the pipeline chunk / 2
+constexpr size_t kHostStageScale = 8;    // gb_all_reduce_host: a chunk stages 8 x the pipeline chunk of rank data
 constexpr size_t kRsChunkDiv = 2;        // gb_reduce_scatter: chunk = the all_reduce chunk - the pipeline chunk / 2, >= chunk / 2
 constexpr size_t kBcastPieceScale = 4;   // gb_broadcast: pieces of up to 4 x the pipeline chunk
 constexpr uint64_t kMaxElems = 1ull << 38;
@@ -193,8 +193,10 @@ bool is_fp8(int codec);
 size_t part_bytes(const Plan &p, uint64_t m);
 // balance: cut n into equal chunks of whole tiles (no short remainder);
 // the bucket pipeline balances per bucket itself and passes false.
+// chunk_elems > 0: chunks of that many elements (rounded down to whole tiles)
+// instead of a payload size.
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
-               bool sharded_ok = false, size_t chunk_bytes = 0, bool balance = true);
+               bool sharded_ok = false, size_t chunk_bytes = 0, bool balance = true, uint64_t chunk_elems = 0);
 gb_status check_launch(gb_ctx *c, cudaError_t e, const char *what);
 gb_status launch_encode(gb_ctx *c, const Plan &p, const gb::ReduceEncodeArgs &ra, cudaStream_t s);
 gb_status launch_decode(gb_ctx *c, const Plan &p, const gb::DecodeBcastArgs &da, cudaStream_t s);

@@ -322,7 +322,7 @@ size_t part_bytes(const Plan &p, uint64_t m) {
 }
 
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
-               bool sharded_ok, size_t chunk_bytes, bool balance) {
+               bool sharded_ok, size_t chunk_bytes, bool balance, uint64_t chunk_elems) {
     // chunk_bytes == 0: the single-buffer all_reduce's or reduce_scatter's
     // chunk, derived from the pipeline chunk and grown with the payload
     const bool grow = chunk_bytes == 0;
@@ -374,7 +374,7 @@ Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec c
             const double half = cbytes / (double)kRsChunkDiv;
             cbytes = !rs ? s_ar : s_ar - half > half ? s_ar - half : half;
         }
-        uint64_t ch = (uint64_t)(cbytes / per_elem) / gb::kTile * gb::kTile;
+        uint64_t ch = (chunk_elems ? chunk_elems : (uint64_t)(cbytes / per_elem)) / gb::kTile * gb::kTile;
         if (ch < (uint64_t)gb::kTile) ch = gb::kTile;
         const uint64_t min_ch = round_up((n + kMaxChunks - 1) / kMaxChunks, gb::kTile);
         if (ch < min_ch) ch = min_ch;

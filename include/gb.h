@@ -401,9 +401,10 @@ gb_status gb_broadcast(gb_ctx *ctx, void *const *rank_bufs, size_t n, gb_dtype d
  * there and copied back (gpubridge README, torch.distributed backend, CPU
  * tensors: staged onto the rank's GPU, carried by the same topology and
  * copied back).  Under the pipelined policy (no phase marks kept) the
- * staging, the bridge hop and the copy-back run chunk by chunk (chunks of
- * half of chunk_bytes of payload: every chunk also carries the rank buffers
- * in and out) on the context's copy streams so that both directions of the
+ * staging, the bridge hop and the copy-back run chunk by chunk (every chunk
+ * carries the rank buffers in and out, so a chunk is the elements whose W
+ * rank slices total 8 x chunk_bytes, whole 256-element tiles, at most 32
+ * chunks) on the context's copy streams so that both directions of the
  * host link stay busy, replayed as a CUDA graph from the second call with
  * the same buffers; otherwise staging, all_reduce and copy-back run in
  * sequence.  Host buffers need no alignment; they must not be touched until

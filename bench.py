@@ -909,7 +909,7 @@ def sweep_rows(args, dev, stream, flush, clean, link_peak, max_steps, emit=None)
         pristine = [wl.draw_device(w.dist, n, wl.seed_of(w.cid, r), dev, torch.float32) for r in range(W)]
         bufs = [p.clone() for p in pristine]
         # up to 1 MiB a step is a few tens of microseconds: 50 of them, for the comparison with the floor
-        K = 50 if n * 4 <= (1 << 20) else max(5, min(max_steps, int(4e9 // (n * 4 * W))))
+        K = 50 if n * 4 <= (1 << 20) else max(10, min(max_steps, int(4e9 // (n * 4 * W))))
         Pmax = max(payload_bytes(c, w.block, n) for c in codecs)
         sets = make_sets(pristine, I, Pmax, stream_set_count(W * n * 4 + I * Pmax))
         for codec in codecs:

@@ -553,7 +553,12 @@ def run_gb(args, world, rank, local, pg):
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "alg_bytes_per_launch": dom[1], "avg_launch_ms": dom[2], "traffic": None,
-                     "region": region},
+                     "region": region,
+                     "bytes_from": ("HBM, all of them: the inputs of every timed launch (rank buffers, or the "
+                                    "payloads the encode batch wrote) are read after a clean L2; ncu with the "
+                                    "cache control off found the decode's DRAM reads at 100.2 % of its payload "
+                                    "bytes; written lines still dirty in L2 when a launch ends are written back "
+                                    "during the next one") if ks else "one-hop steps: payloads may hit L2"},
         **({"kernels_stream_ms": ks,
             "kernels_stream_hbm_frac": {names[0]: k1_bytes / (ks[names[0]] * 1e-3) / 1e9 / peak,
                                         names[1]: k2_bytes / (ks[names[1]] * 1e-3) / 1e9 / peak}}

@@ -3,8 +3,9 @@ lengths, dtypes, ops, codecs, pipeline chunk sizes and rank-view offsets (16
 or 32 bytes into the allocation), through all_reduce (twice on the same
 buffers: the second replays a graph where the policy captures one; every
 third case under the sharded-bridge policy), reduce_scatter, all_gather,
-broadcast, and the same inputs as a bucket set of three through the bucket
-all_reduce and reduce_scatter then all_gather of the set.  Each case is
+broadcast, the host-buffer all_reduce (rows of one pinned block or separate
+pinned tensors), and the same inputs as a bucket set of three through the
+bucket all_reduce and reduce_scatter then all_gather of the set.  Each case is
 reproducible from its index."""
 import numpy as np
 import pytest
@@ -121,6 +122,22 @@ def test_random_case_matches_oracle(seed):
             assert_bits_equal(to_host(bc[r].t), xs[src], "BC %s rank %d" % (what, r))
         for v in ranks + bc:
             assert v.intact(), what
+        # the host-buffer entry points: the ranks as rows of one pinned [W, n] block (even seeds, the rows
+        # entry point with its 2D staging copies) or as separate pinned tensors (odd seeds)
+        want = orc.all_reduce(xs, sizes, op, codec, block)
+        hx = [torch.from_numpy(x.view(np.int16) if dtype == "bf16" else x) for x in xs]
+        if seed % 2 == 0:
+            blk = torch.stack(hx).pin_memory()
+            host = [blk[r] for r in range(W)]
+        else:
+            host = [h.clone().pin_memory() for h in hx]
+        if dtype == "bf16":
+            host = [h.view(torch.bfloat16) for h in host]
+        ctx.all_reduce_host(host, op, codec, block)
+        torch.cuda.synchronize()
+        for r in range(W):
+            got = host[r].view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else host[r].numpy()
+            assert_bits_equal(got, want[r], "host %s rank %d" % (what, r))
         # the same inputs as a bucket set of three (bucket sizes multiples of W for reduce_scatter)
         if n >= 3 * W:  # (the sharded policy, where on, stays on: bucket sets keep one link under it)
             cut = [0, (n // 3) // W * W, (2 * n // 3) // W * W, n]

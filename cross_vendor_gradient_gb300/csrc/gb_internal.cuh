@@ -191,6 +191,7 @@ size_t payload_bytes(int codec, int block, size_t n);
 size_t scales_offset(int codec, size_t n);
 bool is_fp8(int codec);
 size_t part_bytes(const Plan &p, uint64_t m);
+size_t chunk_stride(const Plan &p, uint64_t m);  // a chunk's part stride in its staging region
 // balance: cut n into equal chunks of whole tiles (no short remainder);
 // the bucket pipeline balances per bucket itself and passes false.
 // chunk_elems > 0: chunks of that many elements (rounded down to whole tiles)

@@ -321,6 +321,14 @@ size_t part_bytes(const Plan &p, uint64_t m) {
     return b;
 }
 
+// The stride of a chunk's I parts inside its I-part staging region (I x
+// p.part bytes): the chunk's own part rounded to 256 bytes, so that the one
+// copy that moves several parts carries no padding when the chunk is shorter
+// than the plan's longest (a bucket set's smaller buckets, a short last
+// chunk).  Copying the full part stride had moved up to 15 % more bytes over
+// the host link on the 1.1B bucket set.
+size_t chunk_stride(const Plan &p, uint64_t m) { return round_up(part_bytes(p, m), 256); }
+
 Plan make_plan(const gb_ctx *c, uint64_t n, gb_dtype dtype, gb_op op, gb_codec codec, int block, int rs,
                bool sharded_ok, size_t chunk_bytes, bool balance, uint64_t chunk_elems) {
     // chunk_bytes == 0: the single-buffer all_reduce's or reduce_scatter's
@@ -451,14 +459,19 @@ gb_status record(gb_ctx *c, cudaEvent_t ev, cudaStream_t s) {
 gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *const *out,
                       float *const *res, cudaStream_t s, int markmode, bool multi) {
     const int I = p.I;
-    auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
+    auto stride = [&](int ch) {
+        uint64_t e0, m;
+        chunk_range(p, ch, &e0, &m);
+        return chunk_stride(p, m);
+    };
+    auto outbox = [&](int ch, int i) { return c->d_stage + (size_t)ch * I * p.part + (size_t)i * stride(ch); };
     // leader g's received copy of island j's part of chunk ch (j != g)
     auto inbox = [&](int g, int ch, int j) {
         unsigned char *base = c->d_stage + (size_t)I * p.C * p.part;
-        if (I == 2) return base + ((size_t)ch * I + j) * p.part;  // mirror of the host slots
-        return base + (((size_t)g * p.C + ch) * I + j) * p.part;
+        if (I == 2) return base + (size_t)ch * I * p.part + (size_t)j * stride(ch);  // mirror of the host slots
+        return base + ((size_t)g * p.C + ch) * I * p.part + (size_t)j * stride(ch);
     };
-    auto host = [&](int ch, int j) { return c->h_stage + ((size_t)ch * I + j) * p.part; };
+    auto host = [&](int ch, int j) { return c->h_stage + (size_t)ch * I * p.part + (size_t)j * stride(ch); };
     multi = multi && I > 1 && p.C > 1;
 
     // 1. island reduce + encode, chunk by chunk
@@ -495,28 +508,28 @@ gb_status enqueue_rbb(gb_ctx *c, const Plan &p, const void *const *in, void *con
         for (int ch = 0; ch < p.C; ++ch) {
             uint64_t e0, m;
             chunk_range(p, ch, &e0, &m);
-            const size_t pb = part_bytes(p, m);
+            const size_t pb = part_bytes(p, m), st = chunk_stride(p, m);
             if (multi) {
                 D = link_d(ch);
                 H = link_h(ch);
             }
             if (multi) GB_TRY(wait_on(c, D, c->ev_k1[ch]));
             if (ch == 0) GB_TRY(mark(c, markmode, 2, D));
-            GB_TRY(copy_async(c, host(ch, 0), outbox(ch, 0), (size_t)(I - 1) * p.part + pb, cudaMemcpyDeviceToHost, D));
+            GB_TRY(copy_async(c, host(ch, 0), outbox(ch, 0), (size_t)(I - 1) * st + pb, cudaMemcpyDeviceToHost, D));
             if (multi) {
                 GB_TRY(record(c, c->ev_d2h[ch], D));
                 GB_TRY(wait_on(c, H, c->ev_d2h[ch]));
             }
             if (I == 2) {  // island 0's part to leader 1, island 1's part to leader 0: one copy
-                GB_TRY(copy_async(c, inbox(1, ch, 0), host(ch, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+                GB_TRY(copy_async(c, inbox(1, ch, 0), host(ch, 0), st + pb, cudaMemcpyHostToDevice, H));
             } else {
                 for (int g = 0; g < I; ++g) {
                     if (g > 0)
-                        GB_TRY(copy_async(c, inbox(g, ch, 0), host(ch, 0), (size_t)(g - 1) * p.part + pb,
+                        GB_TRY(copy_async(c, inbox(g, ch, 0), host(ch, 0), (size_t)(g - 1) * st + pb,
                                           cudaMemcpyHostToDevice, H));
                     if (g < I - 1)
                         GB_TRY(copy_async(c, inbox(g, ch, g + 1), host(ch, g + 1),
-                                          (size_t)(I - g - 2) * p.part + pb, cudaMemcpyHostToDevice, H));
+                                          (size_t)(I - g - 2) * st + pb, cudaMemcpyHostToDevice, H));
                 }
             }
             if (multi) GB_TRY(record(c, c->ev_h2d[ch], H));
@@ -650,14 +663,19 @@ gb_status stage_ranks(gb_ctx *c, void *const *host, void *const *dev, size_t dpi
 gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, void *const *dev, size_t dpitch,
                                 size_t hpitch, cudaStream_t s) {
     const int I = p.I, W = p.W;
-    auto outbox = [&](int ch, int i) { return c->d_stage + ((size_t)ch * I + i) * p.part; };
+    auto range = [&](int ch, uint64_t *e0, uint64_t *m) { chunk_range(p, ch, e0, m); };
+    auto stride = [&](int ch) {
+        uint64_t e0, m;
+        range(ch, &e0, &m);
+        return chunk_stride(p, m);
+    };
+    auto outbox = [&](int ch, int i) { return c->d_stage + (size_t)ch * I * p.part + (size_t)i * stride(ch); };
     auto inbox = [&](int g, int ch, int j) {
         unsigned char *base = c->d_stage + (size_t)I * p.C * p.part;
-        if (I == 2) return base + ((size_t)ch * I + j) * p.part;
-        return base + (((size_t)g * p.C + ch) * I + j) * p.part;
+        if (I == 2) return base + (size_t)ch * I * p.part + (size_t)j * stride(ch);
+        return base + ((size_t)g * p.C + ch) * I * p.part + (size_t)j * stride(ch);
     };
-    auto hslot = [&](int ch, int j) { return c->h_stage + ((size_t)ch * I + j) * p.part; };
-    auto range = [&](int ch, uint64_t *e0, uint64_t *m) { chunk_range(p, ch, e0, m); };
+    auto hslot = [&](int ch, int j) { return c->h_stage + (size_t)ch * I * p.part + (size_t)j * stride(ch); };
     cudaStream_t D = c->sd, H = c->sh;
     if (c->inject == GB_INJECT_BRIDGE) {
         c->inject = 0;
@@ -685,7 +703,7 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
         GB_TRY(record(c, c->ev_k1[ch], s));
         if (I > 1) {
             GB_TRY(wait_on(c, D, c->ev_k1[ch]));
-            GB_TRY(copy_async(c, hslot(ch, 0), outbox(ch, 0), (size_t)(I - 1) * p.part + part_bytes(p, m),
+            GB_TRY(copy_async(c, hslot(ch, 0), outbox(ch, 0), (size_t)(I - 1) * stride(ch) + part_bytes(p, m),
                               cudaMemcpyDeviceToHost, D));
             GB_TRY(record(c, c->ev_d2h[ch], D));
         }
@@ -694,18 +712,18 @@ gb_status enqueue_host_pipeline(gb_ctx *c, const Plan &p, void *const *host, voi
     auto issue_back = [&](int ch) -> gb_status {  // bridge-in(ch), decode(ch), out(ch)
         uint64_t e0, m;
         range(ch, &e0, &m);
-        const size_t pb = part_bytes(p, m);
+        const size_t pb = part_bytes(p, m), st = chunk_stride(p, m);
         if (I > 1) {
             GB_TRY(wait_on(c, H, c->ev_d2h[ch]));
             if (I == 2) {
-                GB_TRY(copy_async(c, inbox(1, ch, 0), hslot(ch, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+                GB_TRY(copy_async(c, inbox(1, ch, 0), hslot(ch, 0), st + pb, cudaMemcpyHostToDevice, H));
             } else {
                 for (int g = 0; g < I; ++g) {
                     if (g > 0)
-                        GB_TRY(copy_async(c, inbox(g, ch, 0), hslot(ch, 0), (size_t)(g - 1) * p.part + pb,
+                        GB_TRY(copy_async(c, inbox(g, ch, 0), hslot(ch, 0), (size_t)(g - 1) * st + pb,
                                           cudaMemcpyHostToDevice, H));
                     if (g < I - 1)
-                        GB_TRY(copy_async(c, inbox(g, ch, g + 1), hslot(ch, g + 1), (size_t)(I - g - 2) * p.part + pb,
+                        GB_TRY(copy_async(c, inbox(g, ch, g + 1), hslot(ch, g + 1), (size_t)(I - g - 2) * st + pb,
                                           cudaMemcpyHostToDevice, H));
                 }
             }
@@ -765,13 +783,18 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
                           void *const *out, const size_t *numel, int rs, float *const *res, cudaStream_t s) {
     const int I = p.I, W = p.W;
     constexpr int R = kBucketSlots;
-    auto outbox = [&](int slot, int i) { return c->d_stage + ((size_t)slot * I + i) * p.part; };
-    auto inbox = [&](int g, int slot, int j) {
-        unsigned char *base = c->d_stage + (size_t)I * R * p.part;
-        if (I == 2) return base + ((size_t)slot * I + j) * p.part;
-        return base + (((size_t)g * R + slot) * I + j) * p.part;
+    // slot `slot` holds the parts of one chunk of m elements at its own stride
+    auto outbox = [&](int slot, int i, uint64_t m) {
+        return c->d_stage + (size_t)slot * I * p.part + (size_t)i * chunk_stride(p, m);
     };
-    auto hslot = [&](int slot, int j) { return c->h_stage + ((size_t)slot * I + j) * p.part; };
+    auto inbox = [&](int g, int slot, int j, uint64_t m) {
+        unsigned char *base = c->d_stage + (size_t)I * R * p.part;
+        if (I == 2) return base + (size_t)slot * I * p.part + (size_t)j * chunk_stride(p, m);
+        return base + ((size_t)g * R + slot) * I * p.part + (size_t)j * chunk_stride(p, m);
+    };
+    auto hslot = [&](int slot, int j, uint64_t m) {
+        return c->h_stage + (size_t)slot * I * p.part + (size_t)j * chunk_stride(p, m);
+    };
     if (c->inject == GB_INJECT_BRIDGE) {
         c->inject = 0;
         return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
@@ -785,7 +808,7 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         memset(&ra, 0, sizeof ra);
         for (int r = 0; r < W; ++r) ra.src[r] = (const unsigned char *)in[(size_t)w.b * W + r] + w.e0 * p.eb;
         for (int q = 0; res && q < I; ++q) ra.residual[q] = res[(size_t)w.b * I + q] + w.e0;  // error feedback
-        for (int q = 0; q < I; ++q) ra.payload[q] = outbox(slot, q);
+        for (int q = 0; q < I; ++q) ra.payload[q] = outbox(slot, q, w.m);
         for (int q = 0; q <= I; ++q) ra.first[q] = c->first[q];
         ra.n_islands = I;
         ra.n = w.m;
@@ -794,26 +817,26 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         GB_TRY(launch_encode(c, p, ra, s));
         GB_TRY(record(c, c->ev_k1[ev], s));
         GB_TRY(wait_on(c, D, c->ev_k1[ev]));
-        GB_TRY(copy_async(c, hslot(slot, 0), outbox(slot, 0), (size_t)(I - 1) * p.part + part_bytes(p, w.m),
-                          cudaMemcpyDeviceToHost, D));
+        GB_TRY(copy_async(c, hslot(slot, 0, w.m), outbox(slot, 0, w.m),
+                          (size_t)(I - 1) * chunk_stride(p, w.m) + part_bytes(p, w.m), cudaMemcpyDeviceToHost, D));
         GB_TRY(record(c, c->ev_d2h[ev], D));
         return GB_OK;
     };
     auto back = [&](int i) -> gb_status {
         const WorkChunk &w = work[i];
         const int slot = i % R, ev = i % kMaxChunks;
-        const size_t pb = part_bytes(p, w.m);
+        const size_t pb = part_bytes(p, w.m), st = chunk_stride(p, w.m);
         GB_TRY(wait_on(c, H, c->ev_d2h[ev]));
         if (I == 2) {
-            GB_TRY(copy_async(c, inbox(1, slot, 0), hslot(slot, 0), p.part + pb, cudaMemcpyHostToDevice, H));
+            GB_TRY(copy_async(c, inbox(1, slot, 0, w.m), hslot(slot, 0, w.m), st + pb, cudaMemcpyHostToDevice, H));
         } else {
             for (int g = 0; g < I; ++g) {
                 if (g > 0)
-                    GB_TRY(copy_async(c, inbox(g, slot, 0), hslot(slot, 0), (size_t)(g - 1) * p.part + pb,
+                    GB_TRY(copy_async(c, inbox(g, slot, 0, w.m), hslot(slot, 0, w.m), (size_t)(g - 1) * st + pb,
                                       cudaMemcpyHostToDevice, H));
                 if (g < I - 1)
-                    GB_TRY(copy_async(c, inbox(g, slot, g + 1), hslot(slot, g + 1), (size_t)(I - g - 2) * p.part + pb,
-                                      cudaMemcpyHostToDevice, H));
+                    GB_TRY(copy_async(c, inbox(g, slot, g + 1, w.m), hslot(slot, g + 1, w.m),
+                                      (size_t)(I - g - 2) * st + pb, cudaMemcpyHostToDevice, H));
             }
         }
         GB_TRY(record(c, c->ev_h2d[ev], H));
@@ -839,7 +862,7 @@ gb_status enqueue_buckets(gb_ctx *c, const Plan &p, const std::vector<WorkChunk>
         }
         const void *received[GB_MAX_ISLANDS];
         for (int j = 0; j < I; ++j)
-            received[j] = I == 1 ? (const void *)outbox(slot, 0) : (const void *)inbox((j + 1) % I, slot, j);
+            received[j] = I == 1 ? (const void *)outbox(slot, 0, w.m) : (const void *)inbox((j + 1) % I, slot, j, w.m);
         gb::decode_once(da, W, I, received);
         da.avg = p.op == GB_AVG;
         da.world = (float)W;

@@ -774,7 +774,7 @@ def run_buckets_bench(args, world, rank, local, pg):
             ms_rs[sets] = float(np.mean([ev0[i].elapsed_time(ev1[i]) for i in range(Ks)]))
         per = sum(bn) * w.elem_bytes
         rs_line = {"what": "gb_reduce_scatter_buckets then gb_all_gather_buckets of the whole set (one pipeline "
-                           "and one graph each, payload chunks of at most 3 x %d KiB; all_gather in groups of "
+                           "and one graph each, payload chunks of at most 6 x %d KiB; all_gather in groups of "
                            "whole rank blocks)" % (chunk_bytes >> 10),
                    "ms_per_step": ms_rs[True], "value": per / (ms_rs[True] * 1e-3) / 1e9, "unit": "GB/s",
                    "steps": Ks,
@@ -827,7 +827,7 @@ def run_buckets_bench(args, world, rank, local, pg):
                                    w.dist, w.op, codec, w.block),
                    "buckets": len(bn), "values_per_rank": sum(bn),
                    "error_feedback": bool(ef),
-                   "policy": "one pipeline over all buckets (payload chunks of at most 3 x %d KiB, each bucket "
+                   "policy": "one pipeline over all buckets (payload chunks of at most 6 x %d KiB, each bucket "
                              "cut evenly), one CUDA graph per step" % (chunk_bytes >> 10),
                    "l2": "flushed before every timed step (512 MiB write, then a 256 MiB read)"},
         "roofline": {"bound": "hbm", "kernel": dom[0], "achieved": achieved, "peak": peak, "peak_kind": peak_kind,

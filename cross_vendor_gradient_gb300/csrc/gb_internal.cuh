@@ -27,7 +27,7 @@ constexpr int kMaxGraphs = 16;
 // sharded-bridge: copy stream pairs ("bridge links"); segment j uses link j % kMaxLinks
 constexpr int kMaxLinks = 8;
 constexpr double kChunkGrowRef = 3.0;    // single-buffer all_reduce: the chunk grows beyond 3 chunks of payload
-constexpr size_t kBucketChunkScale = 3;  // gb_all_reduce_buckets: chunk = 3 x the pipeline chunk
+constexpr size_t kBucketChunkScale = 6;  // gb_all_reduce_buckets: chunk = 6 x the pipeline chunk
 constexpr int kBucketSlots = 3;          // gb_all_reduce_buckets: staging ring slots (chunks in flight)
 constexpr size_t kHostStageScale = 8;    // gb_all_reduce_host: a chunk stages 8 x the pipeline chunk of rank data
 constexpr size_t kRsChunkDiv = 2;        // gb_reduce_scatter: chunk = the all_reduce chunk - the pipeline chunk / 2, >= chunk / 2

@@ -956,9 +956,10 @@ gb_status run_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out
                       cudaStream_t s) {
     // the chunk shape of the largest bucket fixes the slot size.  Chunks are
     // kBucketChunkScale x the pipeline chunk: across a gradient set the
-    // pipeline fills once, so larger copies only save per-copy cost (on
-    // GB300, 6 MiB beat 2, 4 and 8 MiB for both the GPT-2 small and the 1.1B
-    // Llama-style bf16 sets)
+    // pipeline fills once, so larger copies only save per-chunk cost (two
+    // copies, two launches and their event waits).  On GB300 12 MiB, which
+    // leaves most buckets of both bf16 sets (GPT-2 small, the 1.1B
+    // Llama-style set) in one chunk, beat 6 MiB by 4-5 % and tied 16-24 MiB
     size_t nmax = 0;
     for (int b = 0; b < nb; ++b) nmax = numel[b] > nmax ? numel[b] : nmax;
     Plan p = make_plan(c, nmax, dtype, op, codec, block, 0, false, kBucketChunkScale * c->chunk_bytes, false);

@@ -452,7 +452,7 @@ gb_status gb_bucket_plan(const size_t *numel, int n_tensors, size_t elem_bytes, 
  * flat buffers, so nothing is copied in or out.  Under the pipelined policy
  * (two or more islands, no phase marks kept) the buckets run as one
  * pipeline of chunks (each bucket cut evenly into chunks of at most
- * 3 x chunk_bytes of payload: the pipeline fills once per set, so larger
+ * 6 x chunk_bytes of payload: the pipeline fills once per set, so larger
  * copies pay) on a three-slot staging ring, the bridge of one bucket
  * overlapping the kernels of the next, captured as one
  * CUDA graph for the whole set from the second call with the same buffers

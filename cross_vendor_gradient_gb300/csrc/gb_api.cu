@@ -44,7 +44,7 @@ gb_status gb_destroy(gb_ctx *c) {
         if (c->done) cudaEventDestroy(c->done);
         drop_graphs(c);
         free_marks(c);
-        cudaStream_t streams[3] = {c->sd, c->sh, c->scap};
+        cudaStream_t streams[4] = {c->sd, c->sh, c->scap, c->sg};
         for (cudaStream_t st : streams)
             if (st) cudaStreamDestroy(st);
         for (int i = 0; i < kMaxChunks; ++i) {
@@ -873,7 +873,9 @@ gb_status gb_all_gather_buckets(gb_ctx *c, int n_buckets, const void *const *in_
                 key.push_back((uint64_t)(uintptr_t)out_bufs[(size_t)b * c->W + r]);
             }
         }
-        return run_set_graph(c, key, nonempty * c->I, enqueue, s);
+        int spreads = 0;  // per bucket: one gather, one spread per island of two or more ranks
+        for (int i = 0; i < c->I; ++i) spreads += c->size[i] > 1;
+        return run_set_graph(c, key, nonempty * (1 + spreads), enqueue, s);
     }
     for (int b = 0; b < n_buckets; ++b)
         if (bucket_numel_in[b] > 0)

@@ -84,6 +84,7 @@ struct gb_ctx {
     size_t chunk_bytes = 2u << 20;
     int use_graphs = 1;
     cudaStream_t sd = nullptr, sh = nullptr, scap = nullptr;
+    cudaStream_t sg = nullptr;  // gb_all_gather_buckets: the gather kernels, ahead of the copies
     cudaEvent_t ev_k1[gbrt::kMaxChunks] = {}, ev_d2h[gbrt::kMaxChunks] = {}, ev_h2d[gbrt::kMaxChunks] = {};
     cudaEvent_t ev_in[gbrt::kMaxChunks] = {}, ev_k2[gbrt::kMaxChunks] = {};  // host-buffer pipeline
     cudaEvent_t ev_join_d = nullptr, ev_join_h = nullptr;

@@ -144,7 +144,7 @@ gb_status bind(gb_ctx *c) {
     if (c->device < 0) {
         if ((e = cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming)) != cudaSuccess)
             return fail(c, GB_ERR_CUDA, "cudaEventCreate", e);
-        cudaStream_t *streams[3] = {&c->sd, &c->sh, &c->scap};
+        cudaStream_t *streams[4] = {&c->sd, &c->sh, &c->scap, &c->sg};
         for (cudaStream_t *st : streams)
             if ((e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking)) != cudaSuccess)
                 return fail(c, GB_ERR_CUDA, "cudaStreamCreate", e);
@@ -1060,40 +1060,65 @@ GraphEntry *new_graph_slot(gb_ctx *c) {
 }
 
 // all_gather of every bucket as one pipeline (bucket b: W inputs of
-// numel_in[b] elements, W outputs of W * numel_in[b]).  Bucket b's rank
-// blocks cross the bridge through host slot b % 2: groups of consecutive
-// ranks of one island (about chunk_bytes) go device -> host on copy stream
-// D, each group on to every other leader on stream H as soon as it has
-// landed; the in-island copy kernels of bucket b then run on s while the
-// next bucket's blocks are on the link.  A slot is written again only after
-// the host -> device copies that read it.
+// numel_in[b] elements, W outputs of W * numel_in[b]).  For bucket b, one
+// copy kernel on the context's gather stream first gathers each island's
+// rank blocks into its leader's output (gather(b)); groups of consecutive
+// blocks of one island (whole islands, up to kBucketChunkScale pipeline
+// chunks) then go device -> host from there through host slot b % 2 in one
+// copy each on stream D, and each group on to every other leader on stream
+// H as soon as it has landed; once bucket b has landed, one copy kernel per
+// island spreads the leader's W blocks to the island's other ranks
+// (spread(b), on s) while the next buckets' blocks are on the link.  Every
+// copy carries a fixed cost of a few microseconds on its stream, so
+// gathering first moves the same bytes in one device -> host copy per group
+// instead of one per rank block.  The gathers depend on nothing but the
+// caller's prior work, so on their own stream they run ahead of the copies
+// instead of waiting behind spreads.  A slot is written again only after the
+// host -> device copies that read it.
 gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *const *out, const size_t *numel_in,
                              size_t eb, size_t slot_bytes, cudaStream_t s) {
     const int W = c->W, I = c->I;
-    cudaStream_t D = c->sd, H = c->sh;
+    cudaStream_t D = c->sd, H = c->sh, G = c->sg;
     if (c->inject == GB_INJECT_BRIDGE) {
         c->inject = 0;
         return fail(c, GB_ERR_BRIDGE, "bridge hop failed (injected)");
     }
-    GB_TRY(record(c, c->ev_join_d, s));  // the copy streams start after the caller's prior work
+    GB_TRY(record(c, c->ev_join_d, s));  // the other streams start after the caller's prior work
     GB_TRY(wait_on(c, D, c->ev_join_d));
     GB_TRY(wait_on(c, H, c->ev_join_d));
-    int ng = 0, done = 0;
-    for (int b = 0; b < nb; ++b) {
-        if (numel_in[b] == 0) continue;
+    GB_TRY(wait_on(c, G, c->ev_join_d));
+    int ng = 0;
+    auto front = [&](int b, int slot, bool reuse) -> gb_status {  // gather(b), then its groups' copies
         const size_t mb = numel_in[b] * eb;
-        const int slot = done % 2;
         unsigned char *host = c->h_stage + (size_t)slot * slot_bytes;
         const void *const *bin = in + (size_t)b * W;
         void *const *bout = out + (size_t)b * W;
-        if (done >= 2) GB_TRY(wait_on(c, D, c->ev_in[slot]));  // the slot's last reader has finished
-        const size_t per_s = mb >= c->chunk_bytes ? 1 : c->chunk_bytes / mb;
+        gb::CopyArgs a;
+        memset(&a, 0, sizeof a);
+        a.n_jobs = W;
+        a.bytes = mb;
+        a.vec = (mb % 16) == 0;
+        for (int i = 0; i < I; ++i) a.dst[i] = (unsigned char *)bout[c->first[i]];
+        for (int q = 0; q < W; ++q) {
+            a.src[q] = (const unsigned char *)bin[q];
+            a.dst_off[q] = (size_t)q * mb;
+            a.dst_lo[q] = c->island_of[q];
+            a.dst_hi[q] = c->island_of[q] + 1;
+        }
+        GB_TRY(check_launch(c, gb::launch_copy(a, G), "all_gather gather"));
+        cudaEvent_t gathered = c->ev_ag[ng++ % GB_MAX_RANKS];
+        GB_TRY(record(c, gathered, G));
+        GB_TRY(wait_on(c, D, gathered));
+        if (reuse) GB_TRY(wait_on(c, D, c->ev_in[slot]));  // the slot's last reader has finished
+        const size_t target = kBucketChunkScale * c->chunk_bytes;
+        const size_t per_s = mb >= target ? 1 : target / mb;
         const int per = per_s > (size_t)W ? W : (int)per_s;
         for (int i = 0; i < I; ++i) {
+            const unsigned char *lead_i = (const unsigned char *)bout[c->first[i]];
             for (int q0 = c->first[i]; q0 < c->first[i + 1]; q0 += per) {
                 const int q1 = (q0 + per) < c->first[i + 1] ? (q0 + per) : c->first[i + 1];
-                for (int q = q0; q < q1; ++q)
-                    GB_TRY(copy_async(c, host + (size_t)q * mb, bin[q], mb, cudaMemcpyDeviceToHost, D));
+                GB_TRY(copy_async(c, host + (size_t)q0 * mb, lead_i + (size_t)q0 * mb, (size_t)(q1 - q0) * mb,
+                                  cudaMemcpyDeviceToHost, D));
                 cudaEvent_t ev = c->ev_ag[ng++ % GB_MAX_RANKS];
                 GB_TRY(record(c, ev, D));
                 GB_TRY(wait_on(c, H, ev));
@@ -1106,30 +1131,48 @@ gb_status enqueue_ag_buckets(gb_ctx *c, int nb, const void *const *in, void *con
             }
         }
         GB_TRY(record(c, c->ev_in[slot], H));  // bucket b has landed; slot free again
+        return GB_OK;
+    };
+    auto back = [&](int b, int slot) -> gb_status {  // spread(b)
+        const size_t mb = numel_in[b] * eb;
+        void *const *bout = out + (size_t)b * W;
         GB_TRY(wait_on(c, s, c->ev_in[slot]));
         for (int i = 0; i < I; ++i) {
+            if (c->size[i] < 2) continue;  // the leader already holds every block
             gb::CopyArgs a;
             memset(&a, 0, sizeof a);
-            const unsigned char *lead = (const unsigned char *)bout[c->first[i]];
-            a.n_jobs = W;
-            a.bytes = mb;
+            a.n_jobs = 1;
+            a.bytes = (size_t)W * mb;
             a.vec = (mb % 16) == 0;
-            for (int q = 0; q < W; ++q) {
-                const bool own = c->island_of[q] == i;
-                a.src[q] = own ? (const unsigned char *)bin[q] : lead + (size_t)q * mb;
-                a.dst_off[q] = (size_t)q * mb;
-                a.dst_lo[q] = 0;
-                a.dst_hi[q] = c->size[i];
-            }
-            for (int k = 0; k < c->size[i]; ++k) a.dst[k] = (unsigned char *)bout[c->first[i] + k];
-            GB_TRY(check_launch(c, gb::launch_copy(a, s), "all_gather copy"));
+            a.src[0] = (const unsigned char *)bout[c->first[i]];
+            a.dst_off[0] = 0;
+            a.dst_lo[0] = 0;
+            a.dst_hi[0] = c->size[i] - 1;
+            for (int k = 1; k < c->size[i]; ++k) a.dst[k - 1] = (unsigned char *)bout[c->first[i] + k];
+            GB_TRY(check_launch(c, gb::launch_copy(a, s), "all_gather spread"));
         }
+        return GB_OK;
+    };
+    // spread(b) is enqueued after front(b + 1) and before front(b + 2), which
+    // records the next landing in the same slot's event
+    int prev = -1, prev_slot = 0, done = 0;
+    for (int b = 0; b < nb; ++b) {
+        if (numel_in[b] == 0) continue;
+        const int slot = done % 2;
+        GB_TRY(front(b, slot, done >= 2));
+        if (prev >= 0) GB_TRY(back(prev, prev_slot));
+        prev = b;
+        prev_slot = slot;
         ++done;
     }
+    if (prev >= 0) GB_TRY(back(prev, prev_slot));
+    cudaEvent_t g_end = c->ev_ag[ng++ % GB_MAX_RANKS];
+    GB_TRY(record(c, g_end, G));
     GB_TRY(record(c, c->ev_join_d, D));
     GB_TRY(record(c, c->ev_join_h, H));
     GB_TRY(wait_on(c, s, c->ev_join_d));
     GB_TRY(wait_on(c, s, c->ev_join_h));
+    GB_TRY(wait_on(c, s, g_end));
     return GB_OK;
 }
 

@@ -491,9 +491,12 @@ gb_status gb_reduce_scatter_buckets(gb_ctx *ctx, int n_buckets, const void *cons
  * bucket_numel_in[b] elements) receives in_bufs[b * W + 0], ...,
  * in_bufs[b * W + W - 1] concatenated, for every r.  Under the pipelined
  * policy (two or more islands, no phase marks kept) the buckets run as one
- * pipeline: each bucket's rank blocks cross the bridge in groups of about
- * chunk_bytes through two alternating host slots, and its in-island copy
- * kernels overlap the next bucket's copies; captured as one CUDA graph per
+ * pipeline: a copy kernel on the context's gather stream gathers each
+ * island's blocks of a bucket into its leader's output, from where they
+ * cross the bridge in groups of whole islands (of up to 6 x chunk_bytes)
+ * through two alternating host slots, one copy per group and direction;
+ * the kernels that spread each leader's blocks to its island overlap the
+ * next buckets' copies; captured as one CUDA graph per
  * set from the second call with the same buffers.  Otherwise one
  * gb_all_gather per bucket.  Empty buckets are allowed (pointers may be
  * NULL).  Inputs must not overlap outputs. */

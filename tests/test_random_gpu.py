@@ -166,3 +166,4 @@ def test_random_case_matches_oracle(seed):
                 for r in range(W):
                     assert_bits_equal(to_host(bk[b][r].t), want[r], "RS+AG buckets %s bucket %d rank %d" % (
                         what, b, r))
+                    assert bk[b][r].intact() and rs[b][r].intact(), what  # nothing written around the views
